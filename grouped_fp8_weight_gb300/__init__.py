@@ -1,0 +1,11 @@
+"""GB300 (sm_103a) K-grouped FP8/BF16 MoE weight-gradient kernels.
+
+The product is the C-ABI library ``libdg.so`` (declared in
+``include/dg_wgrad.h``) built from ``csrc/``; ``binding`` is its thin Python
+binding with the same function names.
+"""
+from .binding import (  # noqa: F401
+    DGError, DG_OK, DG_ERR_INVALID_ARG, DG_ERR_UNSUPPORTED, DG_ERR_CUDA, DG_ERR_TIMEOUT,
+    dg_k_grouped_fp8_wgrad, dg_k_grouped_bf16_wgrad, dg_quant_transpose_fp8,
+    dg_last_error, dg_sync_check, dg_version, lib,
+)

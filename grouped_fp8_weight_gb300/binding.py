@@ -1,0 +1,169 @@
+"""Thin Python binding of the C ABI in ``include/dg_wgrad.h``.
+
+Argument marshalling only: every function checks shapes and dtypes of torch
+tensors, passes their device pointers and the current CUDA stream to the
+library of the same name, and raises ``DGError`` on a non-OK status.  All
+computation happens in the CUDA kernels of ``libdg.so``; there is no fallback.
+If the library has not been built, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libdg.so")
+
+DG_OK, DG_ERR_INVALID_ARG, DG_ERR_UNSUPPORTED, DG_ERR_CUDA, DG_ERR_TIMEOUT = range(5)
+DG_F32, DG_BF16 = 0, 1
+DG_TOKEN_MAJOR, DG_CHANNEL_MAJOR = 0, 1
+DG_MAX_GROUPS = 1024
+STATUS_NAMES = {0: "DG_OK", 1: "DG_ERR_INVALID_ARG", 2: "DG_ERR_UNSUPPORTED",
+                3: "DG_ERR_CUDA", 4: "DG_ERR_TIMEOUT"}
+
+# Every symbol the header declares, with (restype, argtypes).
+_VP, _U8P, _FP, _IP = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p
+_I, _I64 = ctypes.c_int, ctypes.c_int64
+SIGNATURES = {
+    "dg_k_grouped_fp8_wgrad": (_I, [_VP, _U8P, _VP, _U8P, _VP, _I, _FP, _I, _I, _I, _I64,
+                                    _IP, _IP, _I, _VP]),
+    "dg_k_grouped_bf16_wgrad": (_I, [_VP, _VP, _VP, _I, _FP, _I, _I, _I, _I64, _IP, _IP, _VP]),
+    "dg_quant_transpose_fp8": (_I, [_VP, _I64, _I, _VP, _U8P, _I, _I, _VP]),
+    "dg_last_error": (ctypes.c_char_p, []),
+    "dg_sync_check": (_I, [_VP]),
+    "dg_version": (_I, []),
+}
+
+
+class DGError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {msg}")
+        self.status = status
+
+
+_lib = None
+
+
+def lib():
+    """The loaded ``libdg.so`` with argument types set (raises if not built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is not built; run grouped_fp8_weight_gb300.build.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+    return _lib
+
+
+def _check(status: int):
+    if status != DG_OK:
+        raise DGError(status, lib().dg_last_error().decode())
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _ks_host(ks):
+    if isinstance(ks, torch.Tensor):
+        ks = ks.tolist()
+    return (ctypes.c_int * max(1, len(ks)))(*[int(k) for k in ks]), len(ks)
+
+
+def _dptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _need(t, dtype, name, ndim):
+    if t.dtype != dtype or t.dim() != ndim or not t.is_contiguous() or not t.is_cuda:
+        raise ValueError(f"{name}: expected a contiguous CUDA {dtype} tensor of rank {ndim}, "
+                         f"got {t.dtype} {tuple(t.shape)}")
+
+
+def dg_k_grouped_fp8_wgrad(a, sfa, b, sfb, d, c, ks_host, ks_dev, gran_k: int = 128,
+                           stream=None):
+    """D[e] (+)= A_e^T B_e with E4M3 operands and UE8M0 block scales.
+
+    a: uint8/float8_e4m3fn [sum_k, M]; sfa: uint8 [sum_k/gran_k, M]; b, sfb
+    likewise with N; d: float32 or bfloat16 [G, M, N]; c: None, d itself (in
+    place), or a separate float32 [G, M, N]; ks_host: G ints; ks_dev: int32
+    CUDA tensor [G].
+    """
+    a8 = a.view(torch.uint8) if a.dtype != torch.uint8 else a
+    b8 = b.view(torch.uint8) if b.dtype != torch.uint8 else b
+    _need(a8, torch.uint8, "a", 2)
+    _need(b8, torch.uint8, "b", 2)
+    _need(sfa, torch.uint8, "sfa", 2)
+    _need(sfb, torch.uint8, "sfb", 2)
+    if d.dim() != 3 or d.dtype not in (torch.float32, torch.bfloat16) or not d.is_contiguous():
+        raise ValueError("d: expected contiguous float32/bfloat16 [G, M, N]")
+    G, M, N = d.shape
+    if a8.shape[1] != M or b8.shape[1] != N or a8.shape[0] != b8.shape[0]:
+        raise ValueError("operand shapes do not match d")
+    if c is not None and c is not d:
+        _need(c, torch.float32, "c", 3)
+        if tuple(c.shape) != tuple(d.shape):
+            raise ValueError("c must have d's shape")
+    _need(ks_dev, torch.int32, "ks_dev", 1)
+    kh, g = _ks_host(ks_host)
+    if g != G or ks_dev.numel() != G:
+        raise ValueError("ks must have G entries")
+    _check(lib().dg_k_grouped_fp8_wgrad(
+        _dptr(a8), _dptr(sfa), _dptr(b8), _dptr(sfb), _dptr(d),
+        DG_BF16 if d.dtype == torch.bfloat16 else DG_F32,
+        _dptr(c), G, M, N, a8.shape[0], kh, _dptr(ks_dev), gran_k, _stream(stream)))
+
+
+def dg_k_grouped_bf16_wgrad(a, b, d, c, ks_host, ks_dev, stream=None):
+    """D[e] (+)= A_e^T B_e with BF16 operands (any per-expert token counts)."""
+    _need(a, torch.bfloat16, "a", 2)
+    _need(b, torch.bfloat16, "b", 2)
+    if d.dim() != 3 or d.dtype not in (torch.float32, torch.bfloat16) or not d.is_contiguous():
+        raise ValueError("d: expected contiguous float32/bfloat16 [G, M, N]")
+    G, M, N = d.shape
+    if a.shape[1] != M or b.shape[1] != N or a.shape[0] != b.shape[0]:
+        raise ValueError("operand shapes do not match d")
+    if c is not None and c is not d:
+        _need(c, torch.float32, "c", 3)
+    _need(ks_dev, torch.int32, "ks_dev", 1)
+    kh, g = _ks_host(ks_host)
+    if g != G or ks_dev.numel() != G:
+        raise ValueError("ks must have G entries")
+    _check(lib().dg_k_grouped_bf16_wgrad(
+        _dptr(a), _dptr(b), _dptr(d), DG_BF16 if d.dtype == torch.bfloat16 else DG_F32,
+        _dptr(c), G, M, N, a.shape[0], kh, _dptr(ks_dev), _stream(stream)))
+
+
+def dg_quant_transpose_fp8(x, q, sf, layout: str = "token", gran_k: int = 128, stream=None):
+    """Column-block E4M3 cast of bf16 x [T, C] into q ([T, C] or [C, T]) and sf [T/gran_k, C]."""
+    _need(x, torch.bfloat16, "x", 2)
+    q8 = q.view(torch.uint8) if q.dtype != torch.uint8 else q
+    _need(q8, torch.uint8, "q", 2)
+    _need(sf, torch.uint8, "sf", 2)
+    T, C = x.shape
+    want = (T, C) if layout == "token" else (C, T)
+    if tuple(q8.shape) != want or tuple(sf.shape) != (T // gran_k, C):
+        raise ValueError("q / sf shapes do not match x")
+    _check(lib().dg_quant_transpose_fp8(
+        _dptr(x), T, C, _dptr(q8), _dptr(sf),
+        DG_TOKEN_MAJOR if layout == "token" else DG_CHANNEL_MAJOR, gran_k, _stream(stream)))
+
+
+def dg_last_error() -> str:
+    return lib().dg_last_error().decode()
+
+
+def dg_sync_check(stream=None):
+    _check(lib().dg_sync_check(_stream(stream)))
+
+
+def dg_version() -> int:
+    return lib().dg_version()

@@ -1,0 +1,363 @@
+// C-ABI entry points: argument validation, the expert schedule, TMA tensor
+// maps and kernel launches.  No allocation per call; the only allocation is
+// one status word per device on first use.
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <memory>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include "dg_wgrad.h"
+#include "wgrad_params.h"
+
+static_assert(DG_MAX_GROUPS == dg::kMaxGroups, "group limit mismatch");
+
+namespace {
+
+thread_local std::string g_err;
+
+dg_status fail(dg_status s, const char *fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return s;
+}
+
+dg_status ok() {
+  g_err.clear();
+  return DG_OK;
+}
+
+struct DeviceState {
+  bool init = false;
+  bool arch_ok = false;
+  int major = 0, minor = 0;
+  int sms = 0;
+  dg::DevStatus *status = nullptr;
+};
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+dg_status device_state(DeviceState **out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(DG_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= kMaxDevices) return fail(DG_ERR_UNSUPPORTED, "device index %d", dev);
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState &st = g_dev[dev];
+  if (!st.init) {
+    if ((e = cudaDeviceGetAttribute(&st.major, cudaDevAttrComputeCapabilityMajor, dev)) !=
+            cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&st.minor, cudaDevAttrComputeCapabilityMinor, dev)) !=
+            cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&st.sms, cudaDevAttrMultiProcessorCount, dev)) !=
+            cudaSuccess)
+      return fail(DG_ERR_CUDA, "device query: %s", cudaGetErrorString(e));
+    st.arch_ok = (st.major == 10 && st.minor == 3);
+    if (st.arch_ok) {
+      if ((e = cudaMalloc(&st.status, sizeof(dg::DevStatus))) != cudaSuccess ||
+          (e = cudaMemset(st.status, 0, sizeof(dg::DevStatus))) != cudaSuccess)
+        return fail(DG_ERR_CUDA, "status word: %s", cudaGetErrorString(e));
+    }
+    if (g_encode == nullptr) {
+      void *fn = nullptr;
+      cudaDriverEntryPointQueryResult q{};
+      e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                           cudaEnableDefault, &q);
+      if (e != cudaSuccess || fn == nullptr || q != cudaDriverEntryPointSuccess)
+        return fail(DG_ERR_CUDA, "cuTensorMapEncodeTiled not available");
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    st.init = true;
+  }
+  if (!st.arch_ok)
+    return fail(DG_ERR_UNSUPPORTED, "device is sm_%d%d; this library is built for sm_103a only",
+                st.major, st.minor);
+  *out = &st;
+  return DG_OK;
+}
+
+uint64_t wait_limit_ns() {
+  const char *s = std::getenv("DG_WAIT_LIMIT_MS");
+  long ms = 4000;
+  if (s != nullptr && *s) {
+    char *end = nullptr;
+    long v = std::strtol(s, &end, 10);
+    if (end != s && v > 0) ms = v;
+  }
+  return static_cast<uint64_t>(ms) * 1000000ull;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+dg_status encode(CUtensorMap *m, CUtensorMapDataType dt, const void *ptr, int rank,
+                 const uint64_t *dims, const uint64_t *strides_bytes, const uint32_t *box,
+                 CUtensorMapSwizzle sw, CUtensorMapL2promotion l2, const char *what) {
+  cuuint64_t gd[3];
+  cuuint64_t gs[2];
+  cuuint32_t bx[3], es[3];
+  for (int i = 0; i < rank; ++i) {
+    gd[i] = dims[i];
+    bx[i] = box[i];
+    es[i] = 1;
+  }
+  for (int i = 0; i + 1 < rank; ++i) gs[i] = strides_bytes[i];
+  CUresult r = g_encode(m, dt, static_cast<cuuint32_t>(rank), const_cast<void *>(ptr), gd, gs,
+                        bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, l2,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(DG_ERR_CUDA, "tensor map for %s failed (%d)", what, (int)r);
+  return DG_OK;
+}
+
+struct GroupedArgs {
+  bool fp8;
+  const void *a, *b;
+  const uint8_t *sfa, *sfb;
+  void *d;
+  dg_dtype d_dtype;
+  const float *c;
+  int G, M, N;
+  int64_t sum_k;
+  const int *ks_host, *ks_dev;
+  int gran_k;
+  cudaStream_t stream;
+};
+
+dg_status run_grouped(const GroupedArgs &x) {
+  const char *fn = x.fp8 ? "dg_k_grouped_fp8_wgrad" : "dg_k_grouped_bf16_wgrad";
+  // ---- validation (nothing is enqueued on failure)
+  if (x.G < 0) return fail(DG_ERR_INVALID_ARG, "%s: G = %d < 0", fn, x.G);
+  if (x.G > DG_MAX_GROUPS)
+    return fail(DG_ERR_UNSUPPORTED, "%s: G = %d above DG_MAX_GROUPS", fn, x.G);
+  const int mult = x.fp8 ? 16 : 8;
+  if (x.M <= 0 || x.N <= 0 || x.M % mult || x.N % mult)
+    return fail(DG_ERR_INVALID_ARG, "%s: M = %d, N = %d must be positive multiples of %d", fn,
+                x.M, x.N, mult);
+  if (x.sum_k < 0) return fail(DG_ERR_INVALID_ARG, "%s: sum_k < 0", fn);
+  if (x.sum_k > (int64_t)0x7FFFFF00)
+    return fail(DG_ERR_UNSUPPORTED, "%s: sum_k above 2^31 - 256", fn);
+  if (x.fp8 && x.gran_k != 32 && x.gran_k != 128)
+    return fail(DG_ERR_INVALID_ARG, "%s: gran_k = %d (must be 32 or 128)", fn, x.gran_k);
+  if (x.d_dtype != DG_F32 && x.d_dtype != DG_BF16)
+    return fail(DG_ERR_INVALID_ARG, "%s: unknown output dtype %d", fn, (int)x.d_dtype);
+  if (x.d_dtype == DG_BF16 && x.c != nullptr)
+    return fail(DG_ERR_INVALID_ARG, "%s: an accumulator needs FP32 output", fn);
+  if (x.G == 0) {
+    if (x.sum_k != 0)
+      return fail(DG_ERR_INVALID_ARG, "%s: G = 0 but sum_k = %lld", fn, (long long)x.sum_k);
+    return ok();
+  }
+  if (x.ks_host == nullptr || x.ks_dev == nullptr)
+    return fail(DG_ERR_INVALID_ARG, "%s: ks_host and ks_dev are required", fn);
+  int64_t total = 0;
+  for (int e = 0; e < x.G; ++e) {
+    const int k = x.ks_host[e];
+    if (k < 0) return fail(DG_ERR_INVALID_ARG, "%s: ks[%d] = %d < 0", fn, e, k);
+    if (x.fp8 && k % 128)
+      return fail(DG_ERR_INVALID_ARG, "%s: ks[%d] = %d is not a multiple of 128", fn, e, k);
+    total += k;
+  }
+  if (total != x.sum_k)
+    return fail(DG_ERR_INVALID_ARG, "%s: sum of ks (%lld) != sum_k (%lld)", fn,
+                (long long)total, (long long)x.sum_k);
+  if (x.d == nullptr || !aligned16(x.d))
+    return fail(DG_ERR_INVALID_ARG, "%s: d must be a 16-byte aligned device pointer", fn);
+  if (x.c != nullptr && x.c != x.d && !aligned16(x.c))
+    return fail(DG_ERR_INVALID_ARG, "%s: c must be 16-byte aligned", fn);
+  if (x.sum_k > 0) {
+    if (x.a == nullptr || x.b == nullptr || !aligned16(x.a) || !aligned16(x.b))
+      return fail(DG_ERR_INVALID_ARG, "%s: a and b must be 16-byte aligned device pointers", fn);
+    if (x.fp8 && (x.sfa == nullptr || x.sfb == nullptr || !aligned16(x.sfa) ||
+                  !aligned16(x.sfb)))
+      return fail(DG_ERR_INVALID_ARG, "%s: sfa and sfb must be 16-byte aligned device pointers",
+                  fn);
+  }
+  DeviceState *dev = nullptr;
+  dg_status s = device_state(&dev);
+  if (s != DG_OK) return s;
+
+  // ---- schedule: longest experts first, then output-only (fill) experts
+  std::unique_ptr<dg::WgradParams> hold(new dg::WgradParams);   // ~17 KB: off the stack
+  dg::WgradParams &p = *hold;
+  std::memset(&p, 0, sizeof(p));
+  std::vector<int> order;
+  order.reserve(x.G);
+  std::vector<int64_t> off(x.G + 1, 0);
+  for (int e = 0; e < x.G; ++e) off[e + 1] = off[e] + x.ks_host[e];
+  for (int e = 0; e < x.G; ++e)
+    if (x.ks_host[e] > 0) order.push_back(e);
+  std::stable_sort(order.begin(), order.end(),
+                   [&](int u, int v) { return x.ks_host[u] > x.ks_host[v]; });
+  const int n_mma = static_cast<int>(order.size());
+  const bool fill_empty = (x.c != x.d);    // no accumulator, or a separate one
+  if (fill_empty)
+    for (int e = 0; e < x.G; ++e)
+      if (x.ks_host[e] == 0) order.push_back(e);
+  const int n_groups = static_cast<int>(order.size());
+  for (int i = 0; i < n_groups; ++i) {
+    const int e = order[i];
+    p.sched[i].expert = e;
+    p.sched[i].k_off = static_cast<int>(off[e]);
+    p.sched[i].k_len = x.ks_host[e];
+  }
+  const int bn = x.fp8 ? dg::fp8_pick_block_n(x.N) : dg::bf16_pick_block_n(x.N);
+  p.M = x.M;
+  p.N = x.N;
+  p.G = x.G;
+  p.m_tiles = (x.M + dg::kBlockM - 1) / dg::kBlockM;
+  p.n_tiles = (x.N + bn - 1) / bn;
+  p.tiles_per_group = p.m_tiles * p.n_tiles;
+  p.num_mma_tiles = n_mma * p.tiles_per_group;
+  p.num_tiles = n_groups * p.tiles_per_group;
+  p.gran_k = x.fp8 ? x.gran_k : 0;
+  p.out_mode = (x.d_dtype == DG_BF16) ? dg::OUT_BF16
+               : (x.c == nullptr)     ? dg::OUT_F32
+               : (x.c == x.d)         ? dg::OUT_F32_REDUCE
+                                      : dg::OUT_F32_C;
+  p.wait_limit_ns = wait_limit_ns();
+  p.status = dev->status;
+  p.ks_dev = x.ks_dev;
+  if (p.num_tiles == 0) return ok();     // every expert empty and D accumulates in place
+
+  // ---- tensor maps
+  const uint64_t M = x.M, N = x.N, G = x.G, SK = x.sum_k;
+  if (p.num_mma_tiles > 0) {
+    if (x.fp8) {
+      const uint64_t da[2] = {M, SK}, sa[1] = {M};
+      const uint64_t db[2] = {N, SK}, sb[1] = {N};
+      const uint32_t box[2] = {128, 128};
+      if ((s = encode(&p.tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, x.a, 2, da, sa, box,
+                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "a")) ||
+          (s = encode(&p.tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, x.b, 2, db, sb, box,
+                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "b")))
+        return s;
+      const uint64_t nb = SK / x.gran_k;
+      const uint64_t dsa[2] = {M, nb}, dsb[2] = {N, nb};
+      const uint32_t bsa[2] = {128, static_cast<uint32_t>(128 / x.gran_k)};
+      const uint32_t bsb[2] = {static_cast<uint32_t>(bn), static_cast<uint32_t>(128 / x.gran_k)};
+      if ((s = encode(&p.tmSFA, CU_TENSOR_MAP_DATA_TYPE_UINT8, x.sfa, 2, dsa, sa, bsa,
+                      CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE, "sfa")) ||
+          (s = encode(&p.tmSFB, CU_TENSOR_MAP_DATA_TYPE_UINT8, x.sfb, 2, dsb, sb, bsb,
+                      CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE, "sfb")))
+        return s;
+    } else {
+      const uint64_t da[2] = {M, SK}, sa[1] = {2 * M};
+      const uint64_t db[2] = {N, SK}, sb[1] = {2 * N};
+      const uint32_t box[2] = {64, 64};
+      if ((s = encode(&p.tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x.a, 2, da, sa, box,
+                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "a")) ||
+          (s = encode(&p.tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x.b, 2, db, sb, box,
+                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "b")))
+        return s;
+    }
+  }
+  {
+    const bool bf = (x.d_dtype == DG_BF16);
+    const uint64_t es = bf ? 2 : 4;
+    const uint64_t dd[3] = {N, M, G}, sd[2] = {es * N, es * N * M};
+    const uint32_t box[3] = {32, 128, 1};
+    if ((s = encode(&p.tmD,
+                    bf ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, x.d,
+                    3, dd, sd, box, bf ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_NONE, "d")))
+      return s;
+    if (p.out_mode == dg::OUT_F32_C &&
+        (s = encode(&p.tmC, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, x.c, 3, dd, sd, box,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE, "c")))
+      return s;
+  }
+
+  // ---- launch: one persistent CTA per SM (or per tile when there are fewer)
+  const int grid = std::min(dev->sms, p.num_tiles);
+  cudaError_t e = x.fp8 ? dg::launch_kgrouped_fp8(p, bn, grid, x.stream)
+                        : dg::launch_kgrouped_bf16(p, bn, grid, x.stream);
+  if (e != cudaSuccess)
+    return fail(DG_ERR_CUDA, "%s: launch failed: %s", fn, cudaGetErrorString(e));
+  return ok();
+}
+
+}  // namespace
+
+extern "C" {
+
+dg_status dg_k_grouped_fp8_wgrad(const void *a, const uint8_t *sfa, const void *b,
+                                 const uint8_t *sfb, void *d, dg_dtype d_dtype, const float *c,
+                                 int G, int M, int N, int64_t sum_k, const int *ks_host,
+                                 const int *ks_dev, int gran_k, dg_stream_t stream) {
+  GroupedArgs x{true, a, b, sfa, sfb, d, d_dtype, c, G, M, N, sum_k, ks_host, ks_dev, gran_k,
+                reinterpret_cast<cudaStream_t>(stream)};
+  return run_grouped(x);
+}
+
+dg_status dg_k_grouped_bf16_wgrad(const void *a, const void *b, void *d, dg_dtype d_dtype,
+                                  const float *c, int G, int M, int N, int64_t sum_k,
+                                  const int *ks_host, const int *ks_dev, dg_stream_t stream) {
+  GroupedArgs x{false, a, b, nullptr, nullptr, d, d_dtype, c, G, M, N, sum_k, ks_host, ks_dev,
+                0, reinterpret_cast<cudaStream_t>(stream)};
+  return run_grouped(x);
+}
+
+dg_status dg_quant_transpose_fp8(const void *x, int64_t T, int C, void *q, uint8_t *sf,
+                                 dg_layout q_layout, int gran_k, dg_stream_t stream) {
+  const char *fn = "dg_quant_transpose_fp8";
+  if (gran_k != 32 && gran_k != 128)
+    return fail(DG_ERR_INVALID_ARG, "%s: gran_k = %d (must be 32 or 128)", fn, gran_k);
+  if (q_layout != DG_TOKEN_MAJOR && q_layout != DG_CHANNEL_MAJOR)
+    return fail(DG_ERR_INVALID_ARG, "%s: unknown layout %d", fn, (int)q_layout);
+  if (T < 0 || T % gran_k)
+    return fail(DG_ERR_INVALID_ARG, "%s: T = %lld must be a non-negative multiple of gran_k",
+                fn, (long long)T);
+  if (C <= 0 || C % 16)
+    return fail(DG_ERR_INVALID_ARG, "%s: C = %d must be a positive multiple of 16", fn, C);
+  if ((C + 255) / 256 > 65535) return fail(DG_ERR_UNSUPPORTED, "%s: C too large", fn);
+  if ((T + 127) / 128 > 0x7FFFFFFFll) return fail(DG_ERR_UNSUPPORTED, "%s: T too large", fn);
+  if (T == 0) return ok();
+  if (x == nullptr || q == nullptr || sf == nullptr || !aligned16(x) || !aligned16(q) ||
+      !aligned16(sf))
+    return fail(DG_ERR_INVALID_ARG, "%s: x, q, sf must be 16-byte aligned device pointers", fn);
+  DeviceState *dev = nullptr;
+  dg_status s = device_state(&dev);
+  if (s != DG_OK) return s;
+  cudaError_t e = dg::launch_quant_colblock(x, T, C, q, sf, q_layout == DG_CHANNEL_MAJOR, gran_k,
+                                            reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess)
+    return fail(DG_ERR_CUDA, "%s: launch failed: %s", fn, cudaGetErrorString(e));
+  return ok();
+}
+
+const char *dg_last_error(void) { return g_err.c_str(); }
+
+dg_status dg_sync_check(dg_stream_t stream) {
+  DeviceState *dev = nullptr;
+  dg_status s = device_state(&dev);
+  if (s != DG_OK) return s;
+  cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(DG_ERR_CUDA, "stream synchronise: %s", cudaGetErrorString(e));
+  dg::DevStatus st{};
+  if ((e = cudaMemcpy(&st, dev->status, sizeof(st), cudaMemcpyDeviceToHost)) != cudaSuccess)
+    return fail(DG_ERR_CUDA, "status read: %s", cudaGetErrorString(e));
+  if (st.code == dg::DEV_OK) return ok();
+  if ((e = cudaMemset(dev->status, 0, sizeof(st))) != cudaSuccess)
+    return fail(DG_ERR_CUDA, "status reset: %s", cudaGetErrorString(e));
+  if (st.code == dg::DEV_TIMEOUT)
+    return fail(DG_ERR_TIMEOUT, "device wait timed out (site 0x%x, block %d, detail %d)",
+                st.where, st.block, st.detail);
+  return fail(DG_ERR_INVALID_ARG, "ks_dev does not match ks_host");
+}
+
+int dg_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,17 @@
+// BF16-input instantiations of the K-grouped kernel.
+#include "wgrad_kernel.cuh"
+
+namespace dg {
+
+int bf16_pick_block_n(int N) { return N >= 256 ? 256 : 128; }
+
+cudaError_t launch_kgrouped_bf16(const WgradParams &p, int block_n, int grid,
+                                 cudaStream_t stream) {
+  switch (block_n) {
+    case 256: return launch_wgrad_bn<false, 256>(p, grid, stream);
+    case 128: return launch_wgrad_bn<false, 128>(p, grid, stream);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace dg

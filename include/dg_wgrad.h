@@ -1,0 +1,176 @@
+/*
+ * dg_wgrad.h -- C ABI of the GB300 (sm_103a) K-grouped weight-gradient library.
+ *
+ * Mixture-of-Experts weight gradient, one GEMM per expert, all experts in one
+ * launch:  D[e] (+)= A_e^T B_e.  The operands are concatenated along tokens:
+ * A is [sum_k, M] (upstream gradients dy, M = h_out), B is [sum_k, N] (input
+ * activations x, N = h_in), and expert e owns the contiguous rows
+ * [off_e, off_e + K_e), off_e = K_0 + ... + K_{e-1}.  The GEMM's reduction
+ * axis is the token axis.
+ *   Sources: "How to Use DeepGEMM Weight Gradient Kernels for Training
+ *   Backward Passes" (sections "API Entry Points", "FP8 Implementation
+ *   Example", "BF16 Alternative", "Dispatch and Tensor-Map Handling");
+ *   "Is DeepGEMM directly applicable to backward in training?" (qijiaxing,
+ *   26 Mar 2025: dw = dy^T x, K = tokens, one scale per 128 tokens along K).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Every pointer argument named a, b, sfa, sfb, d, c, x, q, sf, ks_dev is a
+ *    DEVICE pointer on the current CUDA device; ks_host is a HOST pointer.
+ *  - All matrices are dense row-major with the last index contiguous (no
+ *    padding between rows).  Device pointers must be 16-byte aligned.
+ *  - The caller owns every buffer.  The library allocates nothing per call;
+ *    the first call on a device allocates one small status word for that
+ *    device, kept until process exit.
+ *  - Work is enqueued on `stream` (NULL = legacy default stream) and runs
+ *    asynchronously.  ks_host is read during the call only; device buffers
+ *    must stay valid until the enqueued work completes.
+ *  - Argument errors are returned before anything is enqueued; the output is
+ *    then untouched.  dg_last_error() gives a message for the calling thread.
+ *  - Device-side waits are bounded (default 4 s, environment variable
+ *    DG_WAIT_LIMIT_MS).  A wait that runs out makes the kernel stop early and
+ *    record DG_ERR_TIMEOUT in the device status word, which dg_sync_check()
+ *    reports; the output is then unspecified.
+ */
+#ifndef DG_WGRAD_H
+#define DG_WGRAD_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *dg_stream_t; /* identical to cudaStream_t */
+
+typedef enum {
+    DG_OK = 0,
+    DG_ERR_INVALID_ARG = 1,  /* bad shape, size, alignment, pointer or option */
+    DG_ERR_UNSUPPORTED = 2,  /* device is not sm_103, or a size above a stated limit */
+    DG_ERR_CUDA = 3,         /* a CUDA runtime / driver call failed */
+    DG_ERR_TIMEOUT = 4       /* a bounded device-side wait ran out (see above) */
+} dg_status;
+
+typedef enum { DG_F32 = 0, DG_BF16 = 1 } dg_dtype;
+
+typedef enum {
+    DG_TOKEN_MAJOR = 0,   /* q is [T, C]: same layout as x (what the TN GEMM reads) */
+    DG_CHANNEL_MAJOR = 1  /* q is [C, T]: the physical transpose of x */
+} dg_layout;
+
+/* Largest number of experts per call (one schedule entry per expert). */
+#define DG_MAX_GROUPS 1024
+
+/*
+ * dg_k_grouped_fp8_wgrad -- K-grouped FP8 weight gradient with 1x1xgran_k
+ * block scales.
+ *
+ *   D[e, m, n] = Cterm[e, m, n] + sum_{k in expert e}
+ *                fp8(a[k, m]) * 2^(sfa[k / gran_k, m] - 127)
+ *              * fp8(b[k, n]) * 2^(sfb[k / gran_k, n] - 127)
+ *
+ * Source: "How to Use DeepGEMM Weight Gradient Kernels for Training Backward
+ * Passes", sections "API Entry Points" (k_grouped_fp8_gemm_tn_contiguous: the
+ * TN form that reads [sum_k, M] / [sum_k, N] operands directly) and "FP8
+ * Implementation Example" ((tensor, scale) operand pairs, ks on host and as a
+ * device tensor, optional accumulator, recipe (1, 1, 128) with gran_k 32 or
+ * 128); the DeepGEMM knowledge-base article "UE8M0 Format in DeepGEMM" (scales
+ * are power-of-two UE8M0 bytes consumed by the SM100 tensor core).
+ *
+ *   a       E4M3 codes [sum_k, M]           sfa  UE8M0 bytes [sum_k / gran_k, M]
+ *   b       E4M3 codes [sum_k, N]           sfb  UE8M0 bytes [sum_k / gran_k, N]
+ *   d       output [G, M, N], FP32 or BF16 (d_dtype); BF16 is rounded to
+ *           nearest-even from the FP32 accumulator.
+ *   c       NULL: Cterm = 0.  c == d: accumulate in place (D += ...).  Any other
+ *           pointer: a separate FP32 [G, M, N] accumulator (not modified).
+ *           Only with d_dtype == DG_F32.
+ *   G       number of experts, 0 <= G <= DG_MAX_GROUPS.
+ *   M, N    positive multiples of 16.
+ *   sum_k   total tokens; must equal ks_host[0] + ... + ks_host[G-1].
+ *   ks_host, ks_dev  per-expert token counts (host / device copies, same
+ *           values).  Each K_e >= 0 and a multiple of 128 (an expert's slice is
+ *           whole 128-token blocks).  K_e == 0 experts are skipped: with c == d
+ *           their D[e] is untouched, with c == NULL it is zeroed, with a
+ *           separate c it is a copy of C[e] ("Dispatch and Tensor-Map
+ *           Handling": zero-size groups are skipped).  ks_dev is read by the
+ *           kernel to confirm the host copy; a mismatch is recorded as
+ *           DG_ERR_INVALID_ARG in the status word (see dg_sync_check).
+ *   gran_k  32 or 128: tokens per scale block ("FP8 Implementation Example").
+ * Errors: DG_ERR_INVALID_ARG for any violated condition above (including
+ * NULL pointers where data is needed and misaligned pointers),
+ * DG_ERR_UNSUPPORTED off sm_103, DG_ERR_CUDA on a failed launch.
+ */
+dg_status dg_k_grouped_fp8_wgrad(const void *a, const uint8_t *sfa,
+                                 const void *b, const uint8_t *sfb,
+                                 void *d, dg_dtype d_dtype, const float *c,
+                                 int G, int M, int N, int64_t sum_k,
+                                 const int *ks_host, const int *ks_dev,
+                                 int gran_k, dg_stream_t stream);
+
+/*
+ * dg_k_grouped_bf16_wgrad -- K-grouped weight gradient with BF16 operands and
+ * FP32 accumulation, no scales:  D[e] = Cterm[e] + A_e^T B_e.
+ *
+ * Source: "How to Use DeepGEMM Weight Gradient Kernels for Training Backward
+ * Passes", section "BF16 Alternative" (k_grouped_bf16_gemm_tn_contiguous,
+ * same call shape as the FP8 form without scales).
+ *
+ *   a  BF16 [sum_k, M], b  BF16 [sum_k, N]; d, d_dtype, c as for the FP8 call.
+ *   M, N positive multiples of 8.  K_e >= 0 arbitrary (no block alignment).
+ * Errors as for the FP8 call.
+ */
+dg_status dg_k_grouped_bf16_wgrad(const void *a, const void *b,
+                                  void *d, dg_dtype d_dtype, const float *c,
+                                  int G, int M, int N, int64_t sum_k,
+                                  const int *ks_host, const int *ks_dev,
+                                  dg_stream_t stream);
+
+/*
+ * dg_quant_transpose_fp8 -- the cast a weight-gradient GEMM needs: per column,
+ * per gran_k-token block, one power-of-two scale, values to E4M3.
+ *
+ *   amax    = max_{k in block} |x[k, col]|
+ *   e       = clamp(ceil(log2(amax / 448)), -127, 127)   (amax == 0 -> -127)
+ *   sf      = e + 127                                     (UE8M0 byte)
+ *   q[k, col] = E4M3 round-to-nearest-even of x[k, col] * 2^-e
+ *
+ * Source: "Is DeepGEMM directly applicable to backward in training?"
+ * (LyricZhao, 26 Feb 2025: weight gradients need fused transpose + cast
+ * kernels; hxdtest quoting the DeepSeek-V3 workflow, 4 May 2025: activations
+ * are transposed and re-quantised into 128x1 tiles; qijiaxing, 26 Mar 2025:
+ * every 128 elements along the token axis share one scale).  448 is the
+ * largest E4M3 magnitude, so the cast never saturates.
+ *
+ *   x         BF16 [T, C] (tokens x channels).
+ *   T         non-negative multiple of gran_k.
+ *   C         positive multiple of 16.
+ *   q         E4M3 out: [T, C] (DG_TOKEN_MAJOR) or [C, T] (DG_CHANNEL_MAJOR).
+ *   sf        UE8M0 out [T / gran_k, C].
+ *   gran_k    32 or 128.
+ * Inputs must be finite.  Errors: DG_ERR_INVALID_ARG / DG_ERR_UNSUPPORTED /
+ * DG_ERR_CUDA as above.
+ */
+dg_status dg_quant_transpose_fp8(const void *x, int64_t T, int C,
+                                 void *q, uint8_t *sf,
+                                 dg_layout q_layout, int gran_k,
+                                 dg_stream_t stream);
+
+/* Message describing the calling thread's last non-OK status ("" if none). */
+const char *dg_last_error(void);
+
+/*
+ * Synchronise `stream`, then read and clear the current device's status word.
+ * Returns DG_ERR_TIMEOUT if a kernel gave up on a bounded wait,
+ * DG_ERR_INVALID_ARG if a kernel found ks_dev different from ks_host,
+ * DG_ERR_CUDA if the synchronisation failed, else DG_OK.
+ */
+dg_status dg_sync_check(dg_stream_t stream);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int dg_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DG_WGRAD_H */

@@ -1,0 +1,135 @@
+"""The C-ABI boundary on the host: the library loads, exports every symbol
+the header declares, and rejects bad arguments with the documented status
+before touching the device (so these run without a GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from grouped_fp8_weight_gb300 import binding as B
+from grouped_fp8_weight_gb300 import build as build_mod
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dg_wgrad.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    build_mod.build()
+    return B.lib()
+
+
+def _declared():
+    txt = open(HEADER).read()
+    return sorted(set(re.findall(r"^\S.*?\b(dg_[a-z0-9_]+)\s*\(", txt, re.M)))
+
+
+def test_header_declares_the_api():
+    assert _declared() == sorted(B.SIGNATURES)
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in _declared():
+        assert hasattr(L, name), name
+    assert L.dg_version() == 100
+
+
+FAKE = 0x10000          # aligned, never dereferenced: validation fails first
+MIS = 0x10008           # 8-byte aligned only
+
+
+def _ks(v):
+    return (ctypes.c_int * max(1, len(v)))(*v)
+
+
+def _fp8(L, **kw):
+    a = dict(a=FAKE, sfa=FAKE, b=FAKE, sfb=FAKE, d=FAKE, dt=B.DG_F32, c=None, G=2, M=128,
+             N=256, sk=256, ks=[128, 128], ksd=FAKE, g=128)
+    a.update(kw)
+    return L.dg_k_grouped_fp8_wgrad(a["a"], a["sfa"], a["b"], a["sfb"], a["d"], a["dt"], a["c"],
+                                    a["G"], a["M"], a["N"], a["sk"], _ks(a["ks"]), a["ksd"],
+                                    a["g"], None)
+
+
+@pytest.mark.parametrize("kw,why", [
+    (dict(G=-1), "G = -1"),
+    (dict(M=100), "multiples of 16"),
+    (dict(N=0), "multiples of 16"),
+    (dict(g=64), "gran_k = 64"),
+    (dict(ks=[128, 64], sk=192), "not a multiple of 128"),
+    (dict(ks=[128, -128], sk=0), "< 0"),
+    (dict(sk=512), "!= sum_k"),
+    (dict(dt=B.DG_BF16, c=FAKE), "accumulator needs FP32"),
+    (dict(dt=7), "unknown output dtype"),
+    (dict(a=MIS), "16-byte aligned"),
+    (dict(sfb=None), "sfa and sfb"),
+    (dict(d=None), "d must be"),
+    (dict(c=MIS), "c must be"),
+    (dict(ksd=None), "ks_host and ks_dev"),
+    (dict(G=0, sk=128), "G = 0 but"),
+])
+def test_fp8_invalid_arguments(L, kw, why):
+    assert _fp8(L, **kw) == B.DG_ERR_INVALID_ARG
+    assert why in L.dg_last_error().decode()
+
+
+def test_fp8_group_limit(L):
+    ks = [0] * (B.DG_MAX_GROUPS + 1)
+    assert _fp8(L, G=len(ks), ks=ks, sk=0) == B.DG_ERR_UNSUPPORTED
+
+
+def test_fp8_empty_problem_is_ok_without_device(L):
+    assert _fp8(L, G=0, sk=0) == B.DG_OK
+    assert L.dg_last_error().decode() == ""
+
+
+def _bf16(L, **kw):
+    a = dict(a=FAKE, b=FAKE, d=FAKE, dt=B.DG_F32, c=None, G=2, M=64, N=72, sk=7, ks=[3, 4],
+             ksd=FAKE)
+    a.update(kw)
+    return L.dg_k_grouped_bf16_wgrad(a["a"], a["b"], a["d"], a["dt"], a["c"], a["G"], a["M"],
+                                     a["N"], a["sk"], _ks(a["ks"]), a["ksd"], None)
+
+
+@pytest.mark.parametrize("kw,why", [
+    (dict(M=60), "multiples of 8"),
+    (dict(ks=[3, 5]), "!= sum_k"),
+    (dict(b=MIS), "16-byte aligned"),
+    (dict(dt=B.DG_BF16, c=FAKE), "accumulator"),
+])
+def test_bf16_invalid_arguments(L, kw, why):
+    assert _bf16(L, **kw) == B.DG_ERR_INVALID_ARG
+    assert why in L.dg_last_error().decode()
+
+
+def _quant(L, **kw):
+    a = dict(x=FAKE, T=256, C=64, q=FAKE, sf=FAKE, lay=B.DG_TOKEN_MAJOR, g=128)
+    a.update(kw)
+    return L.dg_quant_transpose_fp8(a["x"], a["T"], a["C"], a["q"], a["sf"], a["lay"], a["g"],
+                                    None)
+
+
+@pytest.mark.parametrize("kw,why", [
+    (dict(T=200), "multiple of gran_k"),
+    (dict(T=-128), "multiple of gran_k"),
+    (dict(C=24), "multiple of 16"),
+    (dict(g=16), "gran_k = 16"),
+    (dict(lay=5), "unknown layout"),
+    (dict(q=MIS), "16-byte aligned"),
+    (dict(sf=None), "16-byte aligned"),
+])
+def test_quant_invalid_arguments(L, kw, why):
+    assert _quant(L, **kw) == B.DG_ERR_INVALID_ARG
+    assert why in L.dg_last_error().decode()
+
+
+def test_quant_zero_tokens_is_ok(L):
+    assert _quant(L, T=0) == B.DG_OK
+
+
+def test_binding_raises_when_library_missing(monkeypatch, tmp_path):
+    monkeypatch.setattr(B, "LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(B, "_lib", None)
+    with pytest.raises(RuntimeError, match="not built"):
+        B.lib()
