@@ -41,6 +41,10 @@ struct WgradCfg {
   static constexpr int A_BYTES = A_ATOMS * ATOM_BYTES;
   static constexpr int B_BYTES = B_ATOMS * ATOM_BYTES;
   static constexpr int KSTEP_BYTES = MMA_K * 128;
+  // Descriptor strides: SBO = 1024 (8 token rows x 128 B) between K groups,
+  // LBO = ATOM_BYTES between 128-byte atoms along M/N.  A single-atom operand
+  // never steps along M/N, so its LBO is set to the K-group stride as well.
+  static constexpr int A_LBO = A_ATOMS > 1 ? ATOM_BYTES : 1024;
   static constexpr int STAGES = kBN > 128 ? 3 : 5;
   static constexpr int NUM_ACC = 2;
   static constexpr int SF_CHUNKS_B = kFP8 ? (kBN + 127) / 128 : 0;
@@ -291,7 +295,7 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
             for (int ks = 0; ks < Cfg::KSTEPS; ++ks) {
               const uint64_t ad =
-                  smem_desc(a0 + ks * Cfg::KSTEP_BYTES, Cfg::ATOM_BYTES, 1024, 2);
+                  smem_desc(a0 + ks * Cfg::KSTEP_BYTES, Cfg::A_LBO, 1024, 2);
               const uint64_t bd =
                   smem_desc(b0 + ks * Cfg::KSTEP_BYTES, Cfg::ATOM_BYTES, 1024, 2);
               mma_mxf8(d_tmem, ad, bd, idesc_mxf8(Cfg::BM, kBN, ks, ks), sfa_t, sfb_t,
@@ -301,7 +305,7 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
             for (int ks = 0; ks < Cfg::KSTEPS; ++ks) {
               const uint64_t ad =
-                  smem_desc(a0 + ks * Cfg::KSTEP_BYTES, Cfg::ATOM_BYTES, 1024, 2);
+                  smem_desc(a0 + ks * Cfg::KSTEP_BYTES, Cfg::A_LBO, 1024, 2);
               const uint64_t bd =
                   smem_desc(b0 + ks * Cfg::KSTEP_BYTES, Cfg::ATOM_BYTES, 1024, 2);
               mma_bf16(d_tmem, ad, bd, idesc_bf16(Cfg::BM, kBN), (j | ks) != 0);
