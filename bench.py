@@ -1,0 +1,411 @@
+"""Throughput of the K-grouped FP8 weight-gradient hot path on GB300.
+
+Default workload: the MoE up/gate-proj weight gradient (G=32 experts,
+M=4096, N=7168, sum K=32768 routed tokens with Zipf(1.2) counts in 128-token
+units, E4M3 operands with UE8M0 1x128 column-block scales, FP32 output).  One
+step = one dg_k_grouped_fp8_wgrad call over inputs resident in HBM; the metric
+is 2*M*N*sum(K) / step time in TFLOP/s.
+
+The same JSON line also carries:
+  roofline      the GEMM kernel's algorithmic bytes / CUDA-event launch time
+                against the measured HBM copy bandwidth, plus its tensor
+                fraction against the FP8 peak (2 x measured BF16);
+  pipeline      the cast-inclusive step (BF16 dY, X -> dg_quant_transpose_fp8
+                x2 -> GEMM) on the same shapes, and the cast's own roofline;
+  e2e           the same metric through the C ABI with pinned host buffers:
+                H2D of the step's operands and D2H of the result D in the
+                timed region;
+  cpu_baseline  the float64 CPU oracle timed on a bounded sample;
+  clocks        nvidia-smi samples taken during warm-up + timed region.
+
+``--impl reference`` times the oracle (the reference arm of this build) on a
+bounded sample of the same workload.  Under torchrun each rank runs its own
+replica of the workload (weak scaling, no data-path collective); rank 0
+prints the line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from grouped_fp8_weight_gb300 import workloads  # noqa: E402
+
+METRIC = "K-grouped FP8 wgrad TFLOP/s (2·M·N·ΣK_i) and % of GB300 dense FP8 peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+CSRC = os.path.join(ROOT, "grouped_fp8_weight_gb300", "csrc")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.txt")
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+GEMM_SOURCES = ("ptx.cuh", "wgrad_params.h", "wgrad_kernel.cuh", "wgrad_fp8.cu")
+
+
+def kernel_source_sha() -> str:
+    """Hash of the FP8 GEMM kernel's sources (traffic figures expire with it)."""
+    h = hashlib.sha256()
+    for f in GEMM_SOURCES:
+        with open(os.path.join(CSRC, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """Per-launch DRAM bytes for (kernel, workload) from the committed ncu
+    summary, or None if absent or taken on a different kernel source."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    sha = kernel_source_sha()
+    with open(TRAFFIC_FILE) as f:
+        for line in f:
+            parts = line.split()
+            if len(parts) >= 4 and parts[0] == kernel and parts[1] == workload and parts[2] == sha:
+                return float(parts[3])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples every 200 ms while running."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        rows = []
+        for line in (self.out or "").strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                rows.append((float(f[1]), float(f[2]), f[5:9]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r)
+                          if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": rows[0][1],
+                "reasons": reasons, "samples": len(rows)}
+
+
+def make_inputs(w, dev):
+    """Operands for the workload, built on the device: BF16 N(0, 1) draws cast
+    by the library's own column-block quantiser (dg_quant_transpose_fp8)."""
+    import grouped_fp8_weight_gb300 as dg
+    ks = workloads.counts_for(w.name)
+    gen = torch.Generator(device=dev).manual_seed(w.seed)
+    a_raw = torch.randn(w.sum_k, w.M, generator=gen, device=dev).to(torch.bfloat16)
+    b_raw = torch.randn(w.sum_k, w.N, generator=gen, device=dev).to(torch.bfloat16)
+    qa = torch.empty(w.sum_k, w.M, dtype=torch.uint8, device=dev)
+    sa = torch.empty(w.sum_k // 128, w.M, dtype=torch.uint8, device=dev)
+    qb = torch.empty(w.sum_k, w.N, dtype=torch.uint8, device=dev)
+    sb = torch.empty(w.sum_k // 128, w.N, dtype=torch.uint8, device=dev)
+    dg.dg_quant_transpose_fp8(a_raw, qa, sa)
+    dg.dg_quant_transpose_fp8(b_raw, qb, sb)
+    torch.cuda.synchronize()
+    return ks, a_raw, b_raw, qa, sa, qb, sb
+
+
+def algorithmic_bytes(w, ks):
+    """Bytes the GEMM must move: operands and scales once, D written once
+    (read too when accumulating in place)."""
+    sk = sum(ks)
+    ops = sk * (w.M + w.N) + (sk // 128) * (w.M + w.N)
+    d_bytes = w.G * w.M * w.N * (4 if w.out_dtype == "f32" else 2)
+    return ops + d_bytes * (2 if w.accumulate else 1)
+
+
+def time_events(fn, steps, stream):
+    """Mean ms of fn() over `steps` launches, CUDA events on `stream`."""
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(steps):
+        fn()
+    end.record(stream)
+    end.synchronize()
+    return start.elapsed_time(end) / steps
+
+
+def cpu_oracle_sample(w, ks, qa, sa, qb, sb, n_rows=16):
+    """Time the float64 oracle on all experts x n_rows seeded rows of M x all N."""
+    import oracle
+    rows = np.sort(np.random.default_rng(w.seed).choice(w.M, n_rows, replace=False))
+    qa_h = qa[:, torch.from_numpy(rows).to(qa.device)].cpu().numpy()
+    sa_h = sa[:, torch.from_numpy(rows).to(sa.device)].cpu().numpy()
+    qb_h, sb_h = qb.cpu().numpy(), sb.cpu().numpy()
+    t0 = time.perf_counter()
+    oracle.kgrouped_fp8_wgrad_rows(qa_h, sa_h, qb_h, sb_h, ks, np.arange(n_rows), 128)
+    dt = time.perf_counter() - t0
+    flops = 2.0 * n_rows * w.N * sum(ks)
+    cores = len(os.sched_getaffinity(0))
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "seconds": dt,
+            "sample": f"all {w.G} experts x {n_rows} seeded rows of M x all N "
+                      f"({flops / 1e9:.1f} of {w.flops / 1e9:.0f} GFLOP), float64 numpy"}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def run_reference(args):
+    """Reference arm: the CPU oracle, timed on a bounded sample of the workload
+    per step (all experts x 8 seeded rows of M x 64 seeded columns of N)."""
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    w = workloads.WORKLOADS[args.workload]
+    import oracle
+    ks = workloads.counts_for(w.name)
+    n_rows, n_cols = 8, 64
+    gen = torch.Generator().manual_seed(w.seed)
+    # Operands: N(0, 1) columns quantised by the oracle itself (columns are
+    # independent, so the sampled columns are exactly the workload's columns).
+    a_cols = torch.randn(w.sum_k, n_rows, generator=gen).numpy()
+    b_cols = torch.randn(w.sum_k, n_cols, generator=gen).numpy()
+    qa, sa = oracle.quant_colblock(a_cols, 128)
+    qb, sb = oracle.quant_colblock(b_cols, 128)
+    flops = 2.0 * n_rows * n_cols * w.sum_k
+    times = []
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        oracle.kgrouped_fp8_wgrad_rows(qa, sa, qb, sb, ks, np.arange(n_rows), 128)
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    t = sum(times) / len(times)
+    v = flops / t / 1e12
+    cores = len(os.sched_getaffinity(0))
+    sample = (f"per step: all {w.G} experts x {n_rows} seeded rows of M x {n_cols} columns "
+              f"of N ({flops / 1e6:.1f} MFLOP of {w.flops / 1e9:.0f} GFLOP), float64 numpy")
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s",
+            "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": workload_config(w, ks),
+            "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(w, ks):
+    return {"workload": w.name, "G": w.G, "M": w.M, "N": w.N, "sum_k": w.sum_k,
+            "empty_experts": sum(1 for k in ks if k == 0), "max_k": max(ks),
+            "gran_k": 128, "operands": "e4m3 + ue8m0 1x128", "out": w.out_dtype,
+            "accumulate": w.accumulate, "parallelism": "replicas (one workload per GPU)",
+            "l2": (f"inputs and output larger than L2 (operands "
+                   f"{w.sum_k * (w.M + w.N) / 1e9:.2f} GB, D "
+                   f"{w.G * w.M * w.N * (4 if w.out_dtype == 'f32' else 2) / 1e9:.2f} GB); no flush")}
+
+
+def run_ours(args):
+    import grouped_fp8_weight_gb300 as dg
+    from grouped_fp8_weight_gb300 import build as build_mod
+    build_mod.build()
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if ws > 1:
+        import torch.distributed as tdist
+        tdist.init_process_group("nccl", device_id=dev)
+    w = workloads.WORKLOADS[args.workload]
+    if w.kind != "fp8":
+        raise SystemExit("bench.py times the FP8 workloads (moe_upgate_fp8_g32, moe_down_fp8_g32)")
+    pk, pk_kind = peaks()
+    ks, a_raw, b_raw, qa, sa, qb, sb = make_inputs(w, dev)
+    ks_dev = torch.tensor(ks, dtype=torch.int32, device=dev)
+    out_dt = torch.float32 if w.out_dtype == "f32" else torch.bfloat16
+    d = torch.empty(w.G, w.M, w.N, dtype=out_dt, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        dg.dg_k_grouped_fp8_wgrad(qa, sa, qb, sb, d, None, ks, ks_dev, 128)
+
+    def barrier():
+        if ws > 1:
+            import torch.distributed as tdist
+            tdist.barrier()
+
+    # ---- device-resident timing (the headline value)
+    with ClockSampler(local) as clk:
+        for _ in range(args.warmup):
+            step()
+        torch.cuda.synchronize()
+        barrier()
+        torch.cuda.synchronize()
+        ms = time_events(step, args.steps, stream)
+        torch.cuda.synchronize()
+        barrier()
+    dg.dg_sync_check()
+    ms_max = ms
+    if ws > 1:
+        import torch.distributed as tdist
+        t = torch.tensor([ms], device=dev)
+        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+        ms_max = float(t.item())
+    flops = w.flops
+    value = ws * flops / (ms_max * 1e-3) / 1e12
+
+    # ---- roofline of the GEMM kernel (the only kernel of the step)
+    alg = algorithmic_bytes(w, ks)
+    gbs = alg / (ms * 1e-3) / 1e9
+    fp8_peak = 2.0 * pk["bf16_tflops"]
+    tflops = flops / (ms * 1e-3) / 1e12
+    t_hbm = alg / (pk["hbm_gbs"] * 1e9)
+    t_tc = flops / (fp8_peak * 1e12)
+    bound = "hbm" if t_hbm >= t_tc else "tensor"
+    traffic = recorded_traffic("kgrouped_fp8", w.name)
+    if bound == "hbm":
+        roof = {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": gbs / pk["hbm_gbs"], "traffic": traffic}
+    else:
+        roof = {"bound": "tensor", "achieved": tflops, "peak": fp8_peak, "unit": "TFLOP/s",
+                "frac": tflops / fp8_peak, "traffic": traffic}
+    roof.update({"kernel": "kgrouped_wgrad_kernel<fp8, 224, f32>", "peak_source": pk_kind,
+                 "algorithmic_bytes": alg, "tensor_tflops": tflops,
+                 "tensor_peak_tflops": fp8_peak, "tensor_frac": tflops / fp8_peak,
+                 "attainable_frac": max(t_hbm, t_tc) / (ms * 1e-3),
+                 "note": "FP8 peak = 2 x measured BF16 burst (nominal fp8/bf16 ratio)"})
+
+    if args.profile:
+        if rank == 0:
+            print(json.dumps({"metric": METRIC, "value": value, "unit": "TFLOP/s",
+                              "ms_per_step": ms_max, "config": workload_config(w, ks),
+                              "roofline": roof, "profile_only": True}), flush=True)
+        return 0
+
+    # ---- the cast-inclusive step on the same shapes (all hot-path kernels)
+    def cast_only():
+        dg.dg_quant_transpose_fp8(a_raw, qa, sa)
+        dg.dg_quant_transpose_fp8(b_raw, qb, sb)
+
+    for _ in range(3):
+        cast_only()
+    ms_cast = time_events(cast_only, max(5, args.steps // 4), stream)
+    for _ in range(2):
+        cast_only()
+        step()
+    ms_pipe = time_events(lambda: (cast_only(), step()), max(5, args.steps // 4), stream)
+    cast_bytes = w.sum_k * (w.M + w.N) * 3 + (w.sum_k // 128) * (w.M + w.N)
+    pipeline = {"ms_per_step": ms_pipe, "value": flops / (ms_pipe * 1e-3) / 1e12,
+                "unit": "TFLOP/s", "steps": "cast(dY) + cast(X) + GEMM",
+                "cast_ms": ms_cast, "cast_roofline": {
+                    "bound": "hbm", "achieved": cast_bytes / (ms_cast * 1e-3) / 1e9,
+                    "peak": pk["hbm_gbs"], "unit": "GB/s",
+                    "frac": cast_bytes / (ms_cast * 1e-3) / 1e9 / pk["hbm_gbs"],
+                    "algorithmic_bytes": cast_bytes}}
+    dg.dg_sync_check()
+
+    # ---- end to end through the C ABI with pinned host buffers
+    h_qa, h_sa = qa.cpu().pin_memory(), sa.cpu().pin_memory()
+    h_qb, h_sb = qb.cpu().pin_memory(), sb.cpu().pin_memory()
+    h_d = torch.empty(d.shape, dtype=d.dtype).pin_memory()
+
+    def e2e_step():
+        qa.copy_(h_qa, non_blocking=True)
+        sa.copy_(h_sa, non_blocking=True)
+        qb.copy_(h_qb, non_blocking=True)
+        sb.copy_(h_sb, non_blocking=True)
+        step()
+        h_d.copy_(d, non_blocking=True)
+
+    e2e_steps = max(2, min(5, args.steps))
+    e2e_step()
+    torch.cuda.synchronize()
+    ms_e2e = time_events(e2e_step, e2e_steps, stream)
+    h2d = sum(t.numel() * t.element_size() for t in (h_qa, h_sa, h_qb, h_sb))
+    d2h = h_d.numel() * h_d.element_size()
+    e2e = {"value": flops / (ms_e2e * 1e-3) / 1e12, "unit": "TFLOP/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e,
+           "steps": e2e_steps}
+    del h_qa, h_sa, h_qb, h_sb, h_d
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        cpu = cpu_oracle_sample(w, ks, qa, sa, qb, sb)
+
+    line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "e4m3 x e4m3 -> f32", "data": "synthetic",
+            "config": workload_config(w, ks), "fp8_peak_frac": tflops / fp8_peak,
+            "roofline": roof, "pipeline": pipeline, "e2e": e2e, "cpu_baseline": cpu,
+            "clocks": clk.summary(), "gpu_launches": args.steps}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as tdist
+        tdist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="moe_upgate_fp8_g32")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", action="store_true",
+                    help="device-timed leg only (for ncu captures)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

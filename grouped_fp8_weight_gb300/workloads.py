@@ -55,6 +55,10 @@ WORKLOADS = {
     # MoE up/gate-proj wgrad: M = 2 x 2048 (gate + up), N = 7168 hidden.
     "moe_upgate_fp8_g32": Workload("moe_upgate_fp8_g32", 1, 32, 4096, 7168, 32768,
                                    "fp8", "f32", False),
+    # Profiling-size up/gate case: same M, N and count law, 8 experts, 8192
+    # tokens (output 0.94 GB, operands 92 MB: still well above L2).
+    "moe_upgate_fp8_g8": Workload("moe_upgate_fp8_g8", 5, 8, 4096, 7168, 8192,
+                                  "fp8", "f32", False),
     # MoE down-proj wgrad with 1% outliers x100, BF16 output.
     "moe_down_fp8_g32": Workload("moe_down_fp8_g32", 2, 32, 7168, 2048, 32768,
                                  "fp8", "bf16", False, outlier_p=0.01, outlier_mul=100.0),
