@@ -29,6 +29,8 @@ _I, _I64 = ctypes.c_int, ctypes.c_int64
 SIGNATURES = {
     "dg_k_grouped_fp8_wgrad": (_I, [_VP, _U8P, _VP, _U8P, _VP, _I, _FP, _I, _I, _I, _I64,
                                     _IP, _IP, _I, _VP]),
+    "dg_k_grouped_fp8_wgrad_noalloc": (_I, [_VP, _U8P, _VP, _U8P, _VP, _I, _FP, _I, _I, _I,
+                                            _I64, _IP, _IP, _I, _VP]),
     "dg_k_grouped_bf16_wgrad": (_I, [_VP, _VP, _VP, _I, _FP, _I, _I, _I, _I64, _IP, _IP, _VP]),
     "dg_quant_transpose_fp8": (_I, [_VP, _I64, _I, _VP, _U8P, _I, _I, _VP]),
     "dg_last_error": (ctypes.c_char_p, []),

@@ -291,6 +291,11 @@ dg_status run_grouped(const GroupedArgs &x) {
 
 }  // namespace
 
+namespace dg {
+// Lets the allocation-free entry point (noalloc.cu) report through dg_last_error.
+void set_last_error(const char *msg) { g_err = (msg != nullptr) ? msg : ""; }
+}  // namespace dg
+
 extern "C" {
 
 dg_status dg_k_grouped_fp8_wgrad(const void *a, const uint8_t *sfa, const void *b,

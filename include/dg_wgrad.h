@@ -155,6 +155,37 @@ dg_status dg_quant_transpose_fp8(const void *x, int64_t T, int C,
                                  dg_layout q_layout, int gran_k,
                                  dg_stream_t stream);
 
+/*
+ * dg_k_grouped_fp8_wgrad_noalloc -- dg_k_grouped_fp8_wgrad for callers that
+ * cannot allocate device memory.  The pages have no counterpart: this is an
+ * addition of this library.
+ *
+ * The ordinary call allocates a 16-byte status record per device (cudaMalloc)
+ * on its first use.  A caller whose device memory is owned by its own caching
+ * allocator, or that must not take the device synchronisation cudaMalloc can
+ * cause, cannot accept that.  This entry point computes exactly what
+ * dg_k_grouped_fp8_wgrad computes, with the same arguments and errors, and
+ * allocates nothing: the kernel's status record lives in a 256-byte
+ * file-scope device array of the library (every GPU that loads the library
+ * holds it until the process exits).
+ *  - The first call on a device does the set-up (device queries, the
+ *    array's device address via cudaGetSymbolAddress); make that first call
+ *    before any stream capture.
+ *  - Each call clears the record on `stream` before its launch; calls that
+ *    overlap on the GPU (on different streams) share the array and race on it.
+ *  - It never synchronises, so device-side timeouts and ks_dev mismatches are
+ *    not reported (waits stay bounded: the kernel ends early, D unspecified).
+ *  - The record needs the same 16 bytes for every problem size; sizes above
+ *    the kernel's limits (G > DG_MAX_GROUPS, sum_k >= 2^31 - 256) are rejected
+ *    with DG_ERR_UNSUPPORTED and a message.
+ */
+dg_status dg_k_grouped_fp8_wgrad_noalloc(const void *a, const uint8_t *sfa,
+                                         const void *b, const uint8_t *sfb,
+                                         void *d, dg_dtype d_dtype, const float *c,
+                                         int G, int M, int N, int64_t sum_k,
+                                         const int *ks_host, const int *ks_dev,
+                                         int gran_k, dg_stream_t stream);
+
 /* Message describing the calling thread's last non-OK status ("" if none). */
 const char *dg_last_error(void);
 
