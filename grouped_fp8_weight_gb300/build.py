@@ -50,16 +50,19 @@ def up_to_date() -> bool:
     return all(os.path.getmtime(p) <= t for p in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    """Compile and link the library; returns its path."""
-    if not force and up_to_date():
+def build(force: bool = False, verbose: bool = False, extra_flags=(), lib_path: str = LIB,
+          build_dir: str = BUILD) -> str:
+    """Compile and link the library; returns its path.  ``extra_flags`` /
+    ``lib_path`` / ``build_dir`` make a separate variant (e.g. a profiling
+    build with -DDG_KERNEL_TIMERS) without touching the product library."""
+    if not force and lib_path == LIB and up_to_date():
         return LIB
     nvcc = _nvcc()
-    os.makedirs(BUILD, exist_ok=True)
+    os.makedirs(build_dir, exist_ok=True)
     srcs = _sources()
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
         cmd = [nvcc, *ARCH, *FLAGS, *extra_flags, "-c", src, "-o", obj]
         if verbose:
             cmd.insert(1, "-Xptxas=-v")
@@ -72,13 +75,13 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
 
     with ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
         objs = list(ex.map(compile_one, srcs))
-    tmp = LIB + ".tmp"
+    tmp = lib_path + ".tmp"
     cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs, "-cudart", "static"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":

@@ -19,6 +19,13 @@
 
 static_assert(DG_MAX_GROUPS == dg::kMaxGroups, "group limit mismatch");
 
+#ifdef DG_KERNEL_TIMERS
+// Profiling builds only: device buffer receiving the kernel's per-role cycle
+// counters (32 per CTA).
+static unsigned long long *g_timers = nullptr;
+extern "C" void dg_debug_set_timers(unsigned long long *p) { g_timers = p; }
+#endif
+
 namespace {
 
 thread_local std::string g_err;
@@ -217,12 +224,16 @@ dg_status run_grouped(const GroupedArgs &x) {
   p.M = x.M;
   p.N = x.N;
   p.G = x.G;
-  p.m_tiles = (x.M + dg::kBlockM - 1) / dg::kBlockM;
+  p.m_tiles = (x.M + dg::kPairM - 1) / dg::kPairM;
   p.n_tiles = (x.N + bn - 1) / bn;
   p.tiles_per_group = p.m_tiles * p.n_tiles;
   p.num_mma_tiles = n_mma * p.tiles_per_group;
   p.num_tiles = n_groups * p.tiles_per_group;
   p.gran_k = x.fp8 ? x.gran_k : 0;
+  // Sweep the smaller operand's tiles fastest: the concurrently running tiles
+  // then share the larger operand's slices, and the smaller one stays in L2
+  // from one sweep to the next.
+  p.m_fastest = (x.M <= x.N) ? 1 : 0;
   p.out_mode = (x.d_dtype == DG_BF16) ? dg::OUT_BF16
                : (x.c == nullptr)     ? dg::OUT_F32
                : (x.c == x.d)         ? dg::OUT_F32_REDUCE
@@ -230,6 +241,9 @@ dg_status run_grouped(const GroupedArgs &x) {
   p.wait_limit_ns = wait_limit_ns();
   p.status = dev->status;
   p.ks_dev = x.ks_dev;
+#ifdef DG_KERNEL_TIMERS
+  p.timers = g_timers;
+#endif
   if (p.num_tiles == 0) return ok();     // every expert empty and D accumulates in place
 
   // ---- tensor maps
@@ -240,14 +254,17 @@ dg_status run_grouped(const GroupedArgs &x) {
       const uint64_t db[2] = {N, SK}, sb[1] = {N};
       const uint32_t box[2] = {128, 128};
       if ((s = encode(&p.tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, x.a, 2, da, sa, box,
-                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "a")) ||
-          (s = encode(&p.tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, x.b, 2, db, sb, box,
-                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "b")))
+                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "a")))
         return s;
+      s = encode(&p.tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, x.b, 2, db, sb, box,
+                 CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "b");
+      if (s) return s;
       const uint64_t nb = SK / x.gran_k;
       const uint64_t dsa[2] = {M, nb}, dsb[2] = {N, nb};
-      const uint32_t bsa[2] = {128, static_cast<uint32_t>(128 / x.gran_k)};
-      const uint32_t bsb[2] = {static_cast<uint32_t>(bn), static_cast<uint32_t>(128 / x.gran_k)};
+      // Four scale rows per box: one scale group of the kernel (four k-blocks
+      // at gran_k 128, the four sub-blocks of one k-block at gran_k 32).
+      const uint32_t bsa[2] = {128, 4};
+      const uint32_t bsb[2] = {static_cast<uint32_t>(bn), 4};
       if ((s = encode(&p.tmSFA, CU_TENSOR_MAP_DATA_TYPE_UINT8, x.sfa, 2, dsa, sa, bsa,
                       CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE, "sfa")) ||
           (s = encode(&p.tmSFB, CU_TENSOR_MAP_DATA_TYPE_UINT8, x.sfb, 2, dsb, sb, bsb,
@@ -280,10 +297,10 @@ dg_status run_grouped(const GroupedArgs &x) {
       return s;
   }
 
-  // ---- launch: one persistent CTA per SM (or per tile when there are fewer)
-  const int grid = std::min(dev->sms, p.num_tiles);
-  cudaError_t e = x.fp8 ? dg::launch_kgrouped_fp8(p, bn, grid, x.stream)
-                        : dg::launch_kgrouped_bf16(p, bn, grid, x.stream);
+  // ---- launch: one persistent CTA pair per two SMs (or per tile when fewer)
+  const int pairs = std::min(dev->sms / 2, p.num_tiles);
+  cudaError_t e = x.fp8 ? dg::launch_kgrouped_fp8(p, bn, pairs, x.stream)
+                        : dg::launch_kgrouped_bf16(p, bn, pairs, x.stream);
   if (e != cudaSuccess)
     return fail(DG_ERR_CUDA, "%s: launch failed: %s", fn, cudaGetErrorString(e));
   return ok();

@@ -212,12 +212,13 @@ extern "C" dg_status dg_k_grouped_fp8_wgrad_noalloc(
   p.M = M;
   p.N = N;
   p.G = G;
-  p.m_tiles = (M + dg::kBlockM - 1) / dg::kBlockM;
+  p.m_tiles = (M + dg::kPairM - 1) / dg::kPairM;
   p.n_tiles = (N + bn - 1) / bn;
   p.tiles_per_group = p.m_tiles * p.n_tiles;
   p.num_mma_tiles = n_mma * p.tiles_per_group;
   p.num_tiles = order_len * p.tiles_per_group;
   p.gran_k = gran_k;
+  p.m_fastest = (M <= N) ? 1 : 0;
   p.out_mode = (d_dtype == DG_BF16) ? dg::OUT_BF16
                : (c == nullptr)     ? dg::OUT_F32
                : (c == d)           ? dg::OUT_F32_REDUCE
@@ -236,7 +237,7 @@ extern "C" dg_status dg_k_grouped_fp8_wgrad_noalloc(
     return DG_OK;
   }
   const uint64_t SK = sum_k, nb = sum_k / gran_k;
-  const uint32_t rows = static_cast<uint32_t>(128 / gran_k);
+  const uint32_t rows = 4;   // scale rows per box: one scale group of the kernel
   if (p.num_mma_tiles > 0 &&
       ((s = map2d(&p.tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, a, M, SK, M, 128, 128,
                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "a")) ||
@@ -254,7 +255,7 @@ extern "C" dg_status dg_k_grouped_fp8_wgrad_noalloc(
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = cudaMemsetAsync(dev->scratch, 0, sizeof(dg::DevStatus), st);
   if (e != cudaSuccess) return nfail(DG_ERR_CUDA, "%s: clearing scratch: %s", fn, cudaGetErrorString(e));
-  e = dg::launch_kgrouped_fp8(p, bn, std::min(dev->sms, p.num_tiles), st);
+  e = dg::launch_kgrouped_fp8(p, bn, std::min(dev->sms / 2, p.num_tiles), st);
   if (e != cudaSuccess) return nfail(DG_ERR_CUDA, "%s: launch failed: %s", fn, cudaGetErrorString(e));
   dg::set_last_error("");
   return DG_OK;

@@ -7,11 +7,11 @@ namespace dg {
 // 512 tensor-memory columns; other widths fall back to 128.
 int fp8_pick_block_n(int N) { return (N % 224 == 0) ? 224 : 128; }
 
-cudaError_t launch_kgrouped_fp8(const WgradParams &p, int block_n, int grid,
+cudaError_t launch_kgrouped_fp8(const WgradParams &p, int block_n, int pairs,
                                 cudaStream_t stream) {
   switch (block_n) {
-    case 224: return launch_wgrad_bn<true, 224>(p, grid, stream);
-    case 128: return launch_wgrad_bn<true, 128>(p, grid, stream);
+    case 224: return launch_wgrad_bn<true, 224>(p, pairs, stream);
+    case 128: return launch_wgrad_bn<true, 128>(p, pairs, stream);
   }
   return cudaErrorInvalidValue;
 }

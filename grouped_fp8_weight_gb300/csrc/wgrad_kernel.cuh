@@ -1,23 +1,44 @@
-// Persistent, warp-specialised K-grouped weight-gradient kernel for sm_103a.
+// Persistent, warp-specialised K-grouped weight-gradient kernel for sm_103a,
+// run by CTA pairs (clusters of two CTAs on two SMs) with the 2-SM tensor-core
+// MMA (tcgen05 cta_group::2).
 //
 //   D[e] (+)= A_e^T B_e,   A_e = A[off_e : off_e + K_e, :],  B_e likewise.
 //
-// One CTA per SM walks the tile list (expert, m-tile, n-tile) with a stride of
-// gridDim.x; experts are ordered longest-first so that the heavy tiles start
-// first and the tail of the launch is made of short tiles.  Roles:
-//   warp 0      TMA producer: A/B tiles (and, for FP8, the raw UE8M0 scale rows)
-//               of each token block into an S-stage shared-memory ring.
-//   warp 1      tensor-memory owner and MMA issuer: repacks the stage's scale
-//               bytes for tcgen05.cp, copies them into tensor memory, issues
-//               four tcgen05.mma per stage (block-scaled E4M3, or BF16), and
-//               commits stage release / accumulator-ready to mbarriers.
+// A pair computes a 256 x BN tile: each CTA holds 128 rows of the A operand
+// (its half of M) and BN/2 columns of the B operand in its shared memory, and
+// its 128 x BN half of the accumulator in its tensor memory.  The even CTA's
+// MMA thread issues every MMA for both; the operands of one stage are thus
+// loaded once per pair, halving each SM's B traffic.
+//
+// Pairs walk the tile list (expert, 256-row M tile, BN-column N tile) with a
+// stride of the number of pairs.  The host sorts experts longest-first; the
+// list is dealt in rounds taken alternately from its head (long, MMA-heavy
+// tiles) and its tail (short, store-heavy tiles), so a pair alternates the two
+// kinds and the epilogue of one overlaps the MMAs of the next.
+//
+// Roles per CTA (224 threads):
+//   warp 0      TMA producer (one thread): A/B stages of 128 (FP8) or 64
+//               (BF16) tokens; both CTAs' bytes complete on the even CTA's
+//               `full` barrier.
+//   warp 1      tensor-memory allocation (collective over the pair); in the
+//               even CTA one thread issues tcgen05.cp per scale group and four
+//               tcgen05.mma per stage, committing to both CTAs' barriers.
 //   warps 2..5  epilogue: tensor memory -> registers -> swizzled shared-memory
-//               staging -> TMA store (or TMA reduce-add for in-place D += acc).
+//               staging -> TMA store (or TMA reduce-add for in-place D += acc)
+//               of this CTA's 128 rows.
+//   warp 6      FP8: scale warp -- fetches this CTA's scale rows (its 128 rows
+//               of A, all BN columns of B) per group of four UE8M0 rows, up to
+//               four groups ahead, and repacks them into the tensor-memory
+//               scale layout.  BF16 (even CTA): stage gate -- zeroes the token
+//               rows past an expert's slice in both CTAs' last stage.
 // Two accumulators live in tensor memory, so the epilogue of one tile overlaps
 // the MMAs of the next.
 //
 // Operands are MN-major (the token axis is K and is the slow axis in memory):
 // an operand tile for one stage is BK token rows x 128-byte swizzle atoms.
+//
+// Building with -DDG_KERNEL_TIMERS adds per-role cycle counters written to
+// WgradParams::timers (profiling builds only).
 #pragma once
 
 #include <cuda_bf16.h>
@@ -28,15 +49,15 @@ namespace dg {
 
 template <bool kFP8, int kBN>
 struct WgradCfg {
-  static constexpr int BM = 128;
+  static constexpr int BM = 128;                        // rows per CTA (pair: 256)
   static constexpr int ELEM = kFP8 ? 1 : 2;
   static constexpr int BK = kFP8 ? 128 : 64;            // tokens per stage
   static constexpr int ATOM = 128 / ELEM;               // elements per swizzle row
   static constexpr int MMA_K = kFP8 ? 32 : 16;          // K of one tcgen05.mma
   static constexpr int KSTEPS = BK / MMA_K;             // 4
-  static constexpr int BN_LOAD = (kBN + ATOM - 1) / ATOM * ATOM;
+  static constexpr int BN_CTA = kBN / 2;                // B columns held per CTA
   static constexpr int A_ATOMS = BM / ATOM;
-  static constexpr int B_ATOMS = BN_LOAD / ATOM;
+  static constexpr int B_ATOMS = (BN_CTA + ATOM - 1) / ATOM;
   static constexpr int ATOM_BYTES = BK * 128;           // BK rows x 128 bytes
   static constexpr int A_BYTES = A_ATOMS * ATOM_BYTES;
   static constexpr int B_BYTES = B_ATOMS * ATOM_BYTES;
@@ -45,40 +66,45 @@ struct WgradCfg {
   // LBO = ATOM_BYTES between 128-byte atoms along M/N.  A single-atom operand
   // never steps along M/N, so its LBO is set to the K-group stride as well.
   static constexpr int A_LBO = A_ATOMS > 1 ? ATOM_BYTES : 1024;
-  static constexpr int STAGES = kBN > 128 ? 3 : 5;
+  static constexpr int B_LBO = B_ATOMS > 1 ? ATOM_BYTES : 1024;
+  static constexpr int STAGES = 5;
   static constexpr int NUM_ACC = 2;
+  // FP8 scale groups: four UE8M0 rows (four k-blocks at gran_k 128, the four
+  // 32-token sub-blocks of one k-block at gran_k 32), in a ring of SF_SLOTS.
+  static constexpr int SF_SLOTS = kFP8 ? 4 : 0;
   static constexpr int SF_CHUNKS_B = kFP8 ? (kBN + 127) / 128 : 0;
-  static constexpr int SFA_RAW = kFP8 ? 512 : 0;        // up to 4 rows x 128
-  static constexpr int SFB_RAW = kFP8 ? ((kBN * 4 + 127) / 128) * 128 : 0;
-  static constexpr int UT_A = kFP8 ? 512 : 0;           // 32 rows x 16 bytes
+  static constexpr int SFA_RAW = 512;                   // 4 rows x 128
+  static constexpr int SFB_RAW = ((kBN * 4 + 127) / 128) * 128;
+  static constexpr int UT_A = 512;                      // 32 rows x 16 bytes
   static constexpr int UT_B = 512 * SF_CHUNKS_B;
+  static constexpr int SF_COLS = 4 + 4 * SF_CHUNKS_B;   // tensor-memory columns per slot
+  static constexpr int SF_COL0 = NUM_ACC * kBN;
   static constexpr int STG_BYTES = 16384;               // 128 rows x 128 bytes
-  static constexpr int SF_BUFS = 4;                     // tensor-memory scale buffers
-  static constexpr int SFA_COL = NUM_ACC * kBN;
-  static constexpr int SFB_COL = SFA_COL + 4 * SF_BUFS;
   static constexpr int TMEM_COLS = 512;
-  static_assert(!kFP8 || SFB_COL + 4 * SF_CHUNKS_B * SF_BUFS <= TMEM_COLS, "tmem budget");
-  static_assert(NUM_ACC * kBN <= TMEM_COLS, "tmem budget");
+  static_assert(SF_COL0 + SF_SLOTS * SF_COLS <= TMEM_COLS, "tmem budget");
   static_assert(kBN % 32 == 0 && kBN <= 256, "block N");
 
   static constexpr int OFF_B = 0;
   static constexpr int OFF_A = OFF_B + STAGES * B_BYTES;
   static constexpr int OFF_STG = OFF_A + STAGES * A_BYTES;
   static constexpr int OFF_SFA = OFF_STG + 2 * STG_BYTES;
-  static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_RAW;
-  static constexpr int OFF_UTA = OFF_SFB + STAGES * SFB_RAW;
-  static constexpr int OFF_UTB = OFF_UTA + STAGES * UT_A;
-  static constexpr int OFF_BAR = (OFF_UTB + STAGES * UT_B + 7) / 8 * 8;
-  // barriers: full[S], empty[S], accf[2], acce[2], cbar[2], drain
-  static constexpr int NUM_BARS = 2 * STAGES + 2 * NUM_ACC + 2 + 1;
+  static constexpr int OFF_SFB = OFF_SFA + SF_SLOTS * SFA_RAW;
+  static constexpr int OFF_UTA = OFF_SFB + SF_SLOTS * SFB_RAW;
+  static constexpr int OFF_UTB = OFF_UTA + SF_SLOTS * UT_A;
+  static constexpr int OFF_BAR = (OFF_UTB + SF_SLOTS * UT_B + 7) / 8 * 8;
+  // barriers: full[S], empty[S], gate[S], accf[2], acce[2], cbar[2], sff/sfr/sfe[SLOTS], drain
+  static constexpr int NUM_BARS = 3 * STAGES + 2 * NUM_ACC + 2 + 3 * SF_SLOTS + 1;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;   // + alignment slack
   static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
 
+constexpr int kWgradThreads = 224;
+
 // Roles' wait sites, reported in DevStatus::where.
-enum : int { W_PROD_EMPTY = 0x01, W_PROD_DRAIN = 0x02, W_MMA_ACCE = 0x11, W_MMA_FULL = 0x12,
-             W_MMA_DRAIN = 0x13, W_EPI_ACCF = 0x21, W_EPI_C = 0x22 };
+enum : int { W_PROD_EMPTY = 0x01, W_PROD_DRAIN = 0x02, W_PROD_SFE = 0x03, W_MMA_ACCE = 0x11,
+             W_MMA_FULL = 0x12, W_MMA_DRAIN = 0x13, W_MMA_SFR = 0x14, W_EPI_ACCF = 0x21,
+             W_EPI_C = 0x22, W_SF_FULL = 0x31 };
 
 // AND-reduce a predicate over the 128 epilogue threads (named barrier 1), so
 // that all four epilogue warps take the same branch.
@@ -95,48 +121,131 @@ __device__ __forceinline__ bool epi_all(bool ok) {
   return r != 0;
 }
 
+// Position t of a pair's walk -> index into the longest-first tile list:
+// rounds of R tiles alternate between the head and the tail of the list.
+__device__ __forceinline__ int interleaved_tile(int t, int n, int R) {
+  const int r = t / R;
+  const int q = (r >> 1) * R + (t - r * R);
+  return (r & 1) ? n - 1 - q : q;
+}
+
+struct TileCoord {
+  int expert, k_off, k_len, m0, n0;   // m0: this CTA's first row; n0: the pair's first column
+};
+
+__device__ __forceinline__ TileCoord tile_coord(const WgradParams &p, int u, int bn,
+                                                uint32_t rank) {
+  const int gi = u / p.tiles_per_group;
+  const int lt = u - gi * p.tiles_per_group;
+  const SchedEntry se = p.sched[gi];
+  const int mt = p.m_fastest ? lt % p.m_tiles : lt / p.n_tiles;
+  const int nt = p.m_fastest ? lt / p.m_tiles : lt % p.n_tiles;
+  return TileCoord{se.expert, se.k_off, se.k_len, mt * 256 + static_cast<int>(rank) * 128,
+                   nt * bn};
+}
+
+// Walks the FP8 scale groups of a pair's tiles in order: a group is gs
+// consecutive k-blocks of one tile.
+struct GroupCursor {
+  int t, j, nk;
+  TileCoord tc;
+};
+
+__device__ __forceinline__ void group_cursor_init(GroupCursor &c, int pid, int R) {
+  c.t = pid - R;
+  c.j = 0;
+  c.nk = 0;
+}
+
+__device__ __forceinline__ bool group_cursor_next(GroupCursor &c, const WgradParams &p, int gs,
+                                                  int bn, int R, uint32_t rank) {
+  c.j += gs;
+  while (c.j >= c.nk) {
+    c.t += R;
+    if (c.t >= p.num_tiles) return false;
+    const int u = interleaved_tile(c.t, p.num_tiles, R);
+    c.j = 0;
+    c.nk = 0;
+    if (u >= p.num_mma_tiles) continue;
+    c.tc = tile_coord(p, u, bn, rank);
+    c.nk = c.tc.k_len / 128;
+  }
+  return true;
+}
+
+#ifdef DG_KERNEL_TIMERS
+#define DG_T0(v) const unsigned long long v = clock64()
+#define DG_TACC(slot, v) (tm[slot] += clock64() - (v))
+#else
+#define DG_T0(v)
+#define DG_TACC(slot, v)
+#endif
+
 template <bool kFP8, int kBN, int kOut>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(kWgradThreads, 1)
     kgrouped_wgrad_kernel(const __grid_constant__ WgradParams p) {
   using Cfg = WgradCfg<kFP8, kBN>;
   constexpr int S = Cfg::STAGES;
+  constexpr int NS = Cfg::SF_SLOTS;
   extern __shared__ uint8_t smem_raw[];
+  // The dynamic shared window starts at the same offset in both CTAs, so the
+  // aligned base (and every buffer offset) matches across the pair.
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Cfg::OFF_BAR);
-  uint64_t *full = bars;
-  uint64_t *empty = bars + S;
-  uint64_t *accf = bars + 2 * S;
-  uint64_t *acce = accf + 2;
-  uint64_t *cbar = acce + 2;
-  uint64_t *drain = cbar + 2;
+  uint64_t *full = bars;           // even CTA: both CTAs' stage bytes landed
+  uint64_t *empty = bars + S;      // stage consumed by the pair's MMAs
+  uint64_t *gate = bars + 2 * S;   // BF16, even CTA: tail rows masked in both CTAs
+  uint64_t *accf = bars + 3 * S;   // accumulator ready (multicast commit)
+  uint64_t *acce = accf + 2;       // even CTA: accumulator drained by both epilogues
+  uint64_t *cbar = acce + 2;       // separate-C tile landed
+  uint64_t *sff = cbar + 2;        // scale group landed (this CTA)
+  uint64_t *sfr = sff + NS;        // even CTA: scale group repacked in both CTAs
+  uint64_t *sfe = sfr + NS;        // scale slot free (its tcgen05.cp completed)
+  uint64_t *drain = sfe + NS;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Cfg::OFF_MISC);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + Cfg::OFF_MISC + 4);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint64_t lim = p.wait_limit_ns;
+  const uint32_t rank = cluster_ctarank();          // 0 = even CTA (issues the MMAs)
+  const bool leader = (rank == 0);
+  const int pid = blockIdx.x >> 1;                  // pair index
+  const int R = gridDim.x >> 1;                     // number of pairs
+  // k-blocks covered by one scale group
+  const int gs = kFP8 ? (p.gran_k == 128 ? 4 : 1) : 1;
+#ifdef DG_KERNEL_TIMERS
+  unsigned long long tm[4] = {0, 0, 0, 0};
+  const unsigned long long t_start = clock64();
+#endif
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < S; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], 1);
+      mbar_init(&gate[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&accf[i], 1);
-      mbar_init(&acce[i], 4);
+      mbar_init(&acce[i], 8);       // four epilogue warps in each CTA
       mbar_init(&cbar[i], 1);
+    }
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(&sff[i], 1);
+      mbar_init(&sfr[i], 2);        // the scale warp of each CTA
+      mbar_init(&sfe[i], 1);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
-    tmem_relinquish();
+    tmem_alloc_pair(tmem_slot, Cfg::TMEM_COLS);
+    tmem_relinquish_pair();
   }
   tc_fence_before();
-  __syncthreads();
+  cluster_sync();                   // barriers of both CTAs initialised before any remote arrive
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -145,186 +254,291 @@ __global__ void __launch_bounds__(192, 1)
     if (lane == 0) {
       prefetch_tmap(&p.tmA);
       prefetch_tmap(&p.tmB);
-      if constexpr (kFP8) {
-        prefetch_tmap(&p.tmSFA);
-        prefetch_tmap(&p.tmSFB);
-      }
-      const int sf_rows = kFP8 ? Cfg::BK / p.gran_k : 0;
-      const uint32_t tx = Cfg::A_BYTES + Cfg::B_BYTES + (kFP8 ? (128 + kBN) * sf_rows : 0);
-      uint32_t it = 0;
+      const uint32_t tx = 2 * (Cfg::A_BYTES + Cfg::B_BYTES);   // both CTAs' bytes
+      const uint64_t keep = l2_policy_evict_last();   // operands are re-read by other tiles
+      int s = 0;
+      uint32_t ph = 0, armed = 0;
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < p.num_mma_tiles; t += gridDim.x) {
-        const int gi = t / p.tiles_per_group;
-        const int lt = t - gi * p.tiles_per_group;
-        const SchedEntry se = p.sched[gi];
-        const int mt = lt / p.n_tiles;
-        const int m0 = mt * Cfg::BM;
-        const int n0 = (lt - mt * p.n_tiles) * kBN;
-        if (p.ks_dev != nullptr && lt == 0 && p.ks_dev[se.expert] != se.k_len)
+      for (int t = pid; ok && t < p.num_tiles; t += R) {
+        const int u = interleaved_tile(t, p.num_tiles, R);
+        if (u >= p.num_mma_tiles) continue;
+        const TileCoord tc = tile_coord(p, u, kBN, rank);
+        if (leader && p.ks_dev != nullptr && tc.m0 == 0 && tc.n0 == 0 &&
+            p.ks_dev[tc.expert] != tc.k_len)
           atomicCAS(&p.status->code, DEV_OK, DEV_KS_MISMATCH);
-        const int nk = (se.k_len + Cfg::BK - 1) / Cfg::BK;
-        for (int j = 0; j < nk; ++j, ++it) {
-          const int s = it % S;
-          const uint32_t ph = (it / S) & 1;
-          if (!mbar_wait(&empty[s], ph ^ 1, abort_flag, lim, p.status, W_PROD_EMPTY, t)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(&full[s], tx);
-          const int k = se.k_off + j * Cfg::BK;
+        const int nk = (tc.k_len + Cfg::BK - 1) / Cfg::BK;
+        const int nb = tc.n0 + static_cast<int>(rank) * Cfg::BN_CTA;   // this CTA's B columns
+        for (int j = 0; j < nk; ++j) {
+          const int k = tc.k_off + j * Cfg::BK;
+          DG_T0(w1);
+          ok = mbar_wait(&empty[s], ph ^ 1, abort_flag, lim, p.status, W_PROD_EMPTY, t);
+          DG_TACC(0, w1);
+          if (!ok) break;
+          if (leader) mbar_arrive_expect_tx(&full[s], tx);
+          const uint32_t fbar = mapa_shared(smem_u32(&full[s]), 0);
           uint8_t *sa = smem + Cfg::OFF_A + s * Cfg::A_BYTES;
           uint8_t *sb = smem + Cfg::OFF_B + s * Cfg::B_BYTES;
 #pragma unroll
           for (int a = 0; a < Cfg::A_ATOMS; ++a)
-            tma_load_2d(sa + a * Cfg::ATOM_BYTES, &p.tmA, &full[s], m0 + a * Cfg::ATOM, k);
+            tma_load_2d_pair(sa + a * Cfg::ATOM_BYTES, &p.tmA, fbar, tc.m0 + a * Cfg::ATOM, k,
+                             keep);
 #pragma unroll
           for (int b = 0; b < Cfg::B_ATOMS; ++b)
-            tma_load_2d(sb + b * Cfg::ATOM_BYTES, &p.tmB, &full[s], n0 + b * Cfg::ATOM, k);
-          if constexpr (kFP8) {
-            tma_load_2d(smem + Cfg::OFF_SFA + s * Cfg::SFA_RAW, &p.tmSFA, &full[s], m0,
-                        k / p.gran_k);
-            tma_load_2d(smem + Cfg::OFF_SFB + s * Cfg::SFB_RAW, &p.tmSFB, &full[s], n0,
-                        k / p.gran_k);
-          }
+            tma_load_2d_pair(sb + b * Cfg::ATOM_BYTES, &p.tmB, fbar, nb + b * Cfg::ATOM, k, keep);
+          ++armed;
+          if (++s == S) { s = 0; ph ^= 1; }
         }
       }
-      // Let every load this CTA started land before the CTA can exit.
-      const uint32_t armed = it;
-      for (uint32_t i = (armed > static_cast<uint32_t>(S) ? armed - S : 0); i < armed; ++i)
-        mbar_wait(&full[i % S], (i / S) & 1, abort_flag, lim, p.status, W_PROD_DRAIN,
-                  static_cast<int>(i), false);
+      // Let every load this CTA started land before the pair can exit: the
+      // even CTA sees them on `full`; its partner sees the stages released.
+      for (uint32_t i = (armed > static_cast<uint32_t>(S) ? armed - S : 0); i < armed; ++i) {
+        if (leader)
+          mbar_wait(&full[i % S], (i / S) & 1, abort_flag, lim, p.status, W_PROD_DRAIN,
+                    static_cast<int>(i), false);
+        else
+          mbar_wait(&empty[i % S], (i / S) & 1, abort_flag, lim, p.status, W_PROD_DRAIN,
+                    static_cast<int>(i), false);
+      }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    uint32_t it = 0, tl = 0;
-    bool ok = true;
-    for (int t = blockIdx.x; ok && t < p.num_mma_tiles; t += gridDim.x, ++tl) {
-      const int gi = t / p.tiles_per_group;
-      const SchedEntry se = p.sched[gi];
-      const int nk = (se.k_len + Cfg::BK - 1) / Cfg::BK;
-      const int tail = se.k_len - (nk - 1) * Cfg::BK;  // rows valid in the last stage
-      const int b = tl & 1;
-      ok = mbar_wait(&acce[b], ((tl >> 1) & 1) ^ 1, abort_flag, lim, p.status, W_MMA_ACCE, t);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
-      tc_fence_after();
-      const uint32_t d_tmem = tmem_base + b * kBN;
-      for (int j = 0; j < nk; ++j, ++it) {
-        const int s = it % S;
-        const uint32_t ph = (it / S) & 1;
-        ok = mbar_wait(&full[s], ph, abort_flag, lim, p.status, W_MMA_FULL, t);
-        ok = __all_sync(0xffffffffu, ok);
+    // ------------------------------------------------------------ MMA issuer (even CTA)
+    // One thread; per stage only constant-offset descriptor updates and the
+    // four MMAs, so that issue keeps ahead of the tensor pipe.
+    if (lane == 0 && leader) {
+      int s = 0, g = 0, tl = 0;
+      uint32_t ph = 0, gph = 0, it = 0;
+      uint32_t sfa_t = 0, sfb_t = 0;
+      bool ok = true;
+      constexpr uint32_t kIdescBase =
+          kFP8 ? idesc_mxf8(2 * Cfg::BM, kBN, 0, 0) : idesc_bf16(2 * Cfg::BM, kBN);
+      // Descriptors of stage 0 / scale slot 0; later stages and k-steps add
+      // their byte offset >> 4 to the start-address field (shared addresses
+      // stay below 256 KB, so the field never carries out).
+      const uint64_t a_desc0 = smem_desc(smem_u32(smem + Cfg::OFF_A), Cfg::A_LBO, 1024, 2);
+      const uint64_t b_desc0 = smem_desc(smem_u32(smem + Cfg::OFF_B), Cfg::B_LBO, 1024, 2);
+      const uint64_t uta_desc0 = smem_desc(smem_u32(smem + Cfg::OFF_UTA), 0, 128, 0);
+      const uint64_t utb_desc0 = smem_desc(smem_u32(smem + Cfg::OFF_UTB), 0, 128, 0);
+      uint64_t a_desc = a_desc0, b_desc = b_desc0;
+      int q = pid;   // position of this pair's tile within the current head/tail round
+      for (int i = 0; ok; ++i) {
+        const int t = pid + i * R;
+        if (t >= p.num_tiles) break;
+        const int u = (i & 1) ? p.num_tiles - 1 - q : q;
+        if (i & 1) q += R;
+        if (u >= p.num_mma_tiles) continue;
+        const int k_len = p.sched[u / p.tiles_per_group].k_len;
+        const int nk = (k_len + Cfg::BK - 1) / Cfg::BK;
+        const int b = tl & 1;
+        DG_T0(w0);
+        ok = mbar_wait(&acce[b], ((tl >> 1) & 1) ^ 1, abort_flag, lim, p.status, W_MMA_ACCE, t);
+        DG_TACC(1, w0);
         if (!ok) break;
         tc_fence_after();
-        uint8_t *sa = smem + Cfg::OFF_A + s * Cfg::A_BYTES;
-        uint8_t *sb = smem + Cfg::OFF_B + s * Cfg::B_BYTES;
-        if constexpr (kFP8) {
-          // Repack the stage's scale bytes into the tensor-memory scale layout:
-          // for each 128-row chunk, 32 rows of 16 bytes where row r, word w holds
-          // the scales of matrix row 32w + r, one byte per 32-token sub-block.
-          const int rows = Cfg::BK / p.gran_k;  // 1 or 4 scale rows per stage
-          const uint8_t *ra = smem + Cfg::OFF_SFA + s * Cfg::SFA_RAW;
-          const uint8_t *rb = smem + Cfg::OFF_SFB + s * Cfg::SFB_RAW;
-          uint32_t w[4];
+        const uint32_t d_tmem = tmem_base + b * kBN;
+        int jg = 0;   // k-blocks left in the current scale group
+        for (int j = 0; j < nk; ++j) {
+          if constexpr (kFP8) {
+            if (jg == 0) {
+              jg = gs;
+              DG_T0(w1);
+              ok = mbar_wait(&sfr[g], gph, abort_flag, lim, p.status, W_MMA_SFR, t);
+              DG_TACC(2, w1);
+              if (!ok) break;
+              tc_fence_after();
+              sfa_t = tmem_base + Cfg::SF_COL0 + g * Cfg::SF_COLS;
+              sfb_t = sfa_t + 4;
+              tmem_cp_32x128b_warpx4_pair(sfa_t, uta_desc0 + static_cast<uint64_t>(g * (Cfg::UT_A >> 4)));
+#pragma unroll
+              for (int c = 0; c < Cfg::SF_CHUNKS_B; ++c)
+                tmem_cp_32x128b_warpx4_pair(
+                    sfb_t + 4 * c,
+                    utb_desc0 + static_cast<uint64_t>(g * (Cfg::UT_B >> 4) + c * (512 >> 4)));
+              mma_commit_pair(&sfe[g], 0x3);
+              if (++g == NS) { g = 0; gph ^= 1; }
+            }
+            --jg;
+          }
+          DG_T0(w2);
+          // Keep at most two stages queued in the tensor pipe: sleep on the
+          // completion of stage it-2 rather than stall in tcgen05.mma issue
+          // (a stalled issue also holds back the epilogue warp that shares
+          // this warp's scheduler).
+          if (it >= 2) {
+            const uint32_t pit = it - 2;
+            ok = mbar_wait(&empty[pit % S], (pit / S) & 1, abort_flag, lim, p.status, W_MMA_FULL, t);
+            if (!ok) break;
+          }
+          // FP8 stages are complete once both CTAs' bytes land; BF16 stages
+          // once warp 6 has also masked an expert's tail rows.
+          ok = mbar_wait(kFP8 ? &full[s] : &gate[s], ph, abort_flag, lim, p.status, W_MMA_FULL, t);
+          DG_TACC(2, w2);
+          if (!ok) break;
+          tc_fence_after();
+          // gran_k 128: byte j%4 of each scale word holds this k-block's
+          // scale; gran_k 32: byte ks holds this 32-token sub-block's.
+          const uint32_t idesc_j = kIdescBase | ((gs == 4) ? (static_cast<uint32_t>(j & 3) * 0x20000010u) : 0u);
+#pragma unroll
+          for (int ks = 0; ks < Cfg::KSTEPS; ++ks) {
+            const uint64_t ad = a_desc + static_cast<uint64_t>(ks * (Cfg::KSTEP_BYTES >> 4));
+            const uint64_t bd = b_desc + static_cast<uint64_t>(ks * (Cfg::KSTEP_BYTES >> 4));
+            if constexpr (kFP8) {
+              const uint32_t idesc = (gs == 4) ? idesc_j : (kIdescBase | (static_cast<uint32_t>(ks) * 0x20000010u));
+              mma_mxf8_pair(d_tmem, ad, bd, idesc, sfa_t, sfb_t, (j | ks) != 0);
+            } else {
+              mma_bf16_pair(d_tmem, ad, bd, kIdescBase, (j | ks) != 0);
+            }
+          }
+          mma_commit_pair(&empty[s], 0x3);
+          ++it;
+          if (++s == S) {
+            s = 0;
+            ph ^= 1;
+            a_desc = a_desc0;
+            b_desc = b_desc0;
+          } else {
+            a_desc += Cfg::A_BYTES >> 4;
+            b_desc += Cfg::B_BYTES >> 4;
+          }
+        }
+        if (!ok) break;
+        mma_commit_pair(&accf[b], 0x3);
+        ++tl;
+      }
+      // Drain: every tcgen05 op issued here completes before tensor memory
+      // is released.
+      mma_commit_pair(drain, 0x1);
+      mbar_wait(drain, 0, abort_flag, lim, p.status, W_MMA_DRAIN, 0, false);
+    }
+  } else if (warp == 6) {
+    if constexpr (!kFP8) {
+      // ---------------------------------------------------------- BF16 stage gate
+      // In the even CTA, every stage passes through here in order.  An
+      // expert's last stage may run past its slice: those token rows of both
+      // operands, in both CTAs, are zeroed so they add nothing (row k of an
+      // atom is bytes [k*128, k*128 + 128)).
+      if (leader) {
+        int s = 0;
+        uint32_t ph = 0;
+        bool ok = true;
+        for (int t = pid; ok && t < p.num_tiles; t += R) {
+          const int u = interleaved_tile(t, p.num_tiles, R);
+          if (u >= p.num_mma_tiles) continue;
+          const int k_len = p.sched[u / p.tiles_per_group].k_len;
+          const int nk = (k_len + Cfg::BK - 1) / Cfg::BK;
+          const int tail = k_len - (nk - 1) * Cfg::BK;
+          for (int j = 0; j < nk; ++j) {
+            ok = mbar_wait(&full[s], ph, abort_flag, lim, p.status, W_SF_FULL, t);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            if (j == nk - 1 && tail < Cfg::BK) {
+              const uint32_t sa = smem_u32(smem + Cfg::OFF_A + s * Cfg::A_BYTES);
+              const uint32_t sb = smem_u32(smem + Cfg::OFF_B + s * Cfg::B_BYTES);
+              const int per_atom = (Cfg::BK - tail) * 8;   // 16-byte chunks per atom
+              const int n_chunks = per_atom * (Cfg::A_ATOMS + Cfg::B_ATOMS);
+              for (int i = lane; i < 2 * n_chunks; i += 32) {
+                const int cta = i / n_chunks;
+                const int ii = i - cta * n_chunks;
+                const int atom = ii / per_atom;
+                const int r = ii - atom * per_atom;
+                const uint32_t base = atom < Cfg::A_ATOMS
+                                          ? sa + atom * Cfg::ATOM_BYTES
+                                          : sb + (atom - Cfg::A_ATOMS) * Cfg::ATOM_BYTES;
+                const uint32_t addr = mapa_shared(base + tail * 128 + r * 16, cta);
+                asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(addr),
+                             "r"(0u)
+                             : "memory");
+              }
+              asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&gate[s]);
+            if (++s == S) { s = 0; ph ^= 1; }
+          }
+        }
+      }
+    } else {
+      // ---------------------------------------------------------- scale warp
+      // Fetches each scale group of this CTA (TMA, up to SF_SLOTS groups
+      // ahead) and repacks it into the tensor-memory scale layout: for each
+      // 128-row chunk, 32 rows of 16 bytes where row l, word q, byte i holds
+      // scale row i of matrix row 32q + l.
+      if (lane == 0) {
+        prefetch_tmap(&p.tmSFA);
+        prefetch_tmap(&p.tmSFB);
+      }
+      GroupCursor ic, rc;
+      group_cursor_init(ic, pid, R);
+      group_cursor_init(rc, pid, R);
+      bool have_i = group_cursor_next(ic, p, gs, kBN, R, rank);
+      bool have_r = group_cursor_next(rc, p, gs, kBN, R, rank);
+      const uint32_t sfr_leader = mapa_shared(smem_u32(&sfr[0]), 0);
+      uint32_t ig = 0, rg = 0;
+      bool ok = true;
+      while (ok && have_r) {
+        while (have_i && ig < rg + NS) {
+          const int slot = ig % NS;
+          DG_T0(w0);
+          ok = mbar_wait(&sfe[slot], ((ig / NS) & 1) ^ 1, abort_flag, lim, p.status, W_PROD_SFE,
+                         ic.t);
+          ok = __all_sync(0xffffffffu, ok);
+          DG_TACC(2, w0);
+          if (!ok) break;
+          if (lane == 0) {
+            const int row = (ic.tc.k_off + ic.j * 128) / p.gran_k;
+            mbar_arrive_expect_tx(&sff[slot], (128 + kBN) * 4);
+            tma_load_2d(smem + Cfg::OFF_SFA + slot * Cfg::SFA_RAW, &p.tmSFA, &sff[slot],
+                        ic.tc.m0, row);
+            tma_load_2d(smem + Cfg::OFF_SFB + slot * Cfg::SFB_RAW, &p.tmSFB, &sff[slot],
+                        ic.tc.n0, row);
+          }
+          ++ig;
+          have_i = group_cursor_next(ic, p, gs, kBN, R, rank);
+        }
+        if (!ok) break;
+        const int g = rg % NS;
+        DG_T0(w1);
+        ok = mbar_wait(&sff[g], (rg / NS) & 1, abort_flag, lim, p.status, W_SF_FULL, rc.t);
+        ok = __all_sync(0xffffffffu, ok);
+        DG_TACC(3, w1);
+        if (!ok) break;
+        const uint8_t *ra = smem + Cfg::OFF_SFA + g * Cfg::SFA_RAW;
+        const uint8_t *rb = smem + Cfg::OFF_SFB + g * Cfg::SFB_RAW;
+        uint32_t w[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int m = 32 * q + lane;
+          w[q] = static_cast<uint32_t>(ra[m]) | (static_cast<uint32_t>(ra[128 + m]) << 8) |
+                 (static_cast<uint32_t>(ra[256 + m]) << 16) |
+                 (static_cast<uint32_t>(ra[384 + m]) << 24);
+        }
+        *reinterpret_cast<uint4 *>(smem + Cfg::OFF_UTA + g * Cfg::UT_A + 16 * lane) =
+            make_uint4(w[0], w[1], w[2], w[3]);
+#pragma unroll
+        for (int c = 0; c < Cfg::SF_CHUNKS_B; ++c) {
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            const int m = 32 * q + lane;
-            if (rows == 1) {
-              w[q] = static_cast<uint32_t>(ra[m]) * 0x01010101u;
-            } else {
-              w[q] = static_cast<uint32_t>(ra[m]) | (static_cast<uint32_t>(ra[128 + m]) << 8) |
-                     (static_cast<uint32_t>(ra[256 + m]) << 16) |
-                     (static_cast<uint32_t>(ra[384 + m]) << 24);
-            }
+            const int n = 128 * c + 32 * q + lane;
+            w[q] = (n < kBN) ? static_cast<uint32_t>(rb[n]) |
+                                   (static_cast<uint32_t>(rb[kBN + n]) << 8) |
+                                   (static_cast<uint32_t>(rb[2 * kBN + n]) << 16) |
+                                   (static_cast<uint32_t>(rb[3 * kBN + n]) << 24)
+                             : 0u;
           }
-          *reinterpret_cast<uint4 *>(smem + Cfg::OFF_UTA + s * Cfg::UT_A + 16 * lane) =
-              make_uint4(w[0], w[1], w[2], w[3]);
-#pragma unroll
-          for (int c = 0; c < Cfg::SF_CHUNKS_B; ++c) {
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const int n = 128 * c + 32 * q + lane;
-              uint32_t v = 0;
-              if (n < kBN) {
-                if (rows == 1) {
-                  v = static_cast<uint32_t>(rb[n]) * 0x01010101u;
-                } else {
-                  v = static_cast<uint32_t>(rb[n]) | (static_cast<uint32_t>(rb[kBN + n]) << 8) |
-                      (static_cast<uint32_t>(rb[2 * kBN + n]) << 16) |
-                      (static_cast<uint32_t>(rb[3 * kBN + n]) << 24);
-                }
-              }
-              w[q] = v;
-            }
-            *reinterpret_cast<uint4 *>(smem + Cfg::OFF_UTB + s * Cfg::UT_B + 512 * c +
-                                       16 * lane) = make_uint4(w[0], w[1], w[2], w[3]);
-          }
-          fence_proxy_async_smem();
-        } else {
-          // BF16: an expert's last stage may run past its slice; zero those
-          // token rows of both operands so they add nothing.
-          if (j == nk - 1 && tail < Cfg::BK) {
-            // Row k of an atom occupies bytes [k*128, k*128 + 128) of that atom.
-            const int per_atom = (Cfg::BK - tail) * 8;   // 16-byte chunks per atom
-            for (int i = lane; i < per_atom * (Cfg::A_ATOMS + Cfg::B_ATOMS); i += 32) {
-              const int atom = i / per_atom;
-              const int r = i - atom * per_atom;
-              uint8_t *base = atom < Cfg::A_ATOMS
-                                  ? sa + atom * Cfg::ATOM_BYTES
-                                  : sb + (atom - Cfg::A_ATOMS) * Cfg::ATOM_BYTES;
-              *reinterpret_cast<uint4 *>(base + tail * 128 + r * 16) = make_uint4(0, 0, 0, 0);
-            }
-            fence_proxy_async_smem();
-          }
+          *reinterpret_cast<uint4 *>(smem + Cfg::OFF_UTB + g * Cfg::UT_B + 512 * c +
+                                     16 * lane) = make_uint4(w[0], w[1], w[2], w[3]);
         }
+        fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) {
-          const uint32_t a0 = smem_u32(sa), b0 = smem_u32(sb);
-          if constexpr (kFP8) {
-            const uint32_t sfb = it % Cfg::SF_BUFS;
-            const uint32_t sfa_t = tmem_base + Cfg::SFA_COL + 4 * sfb;
-            const uint32_t sfb_t = tmem_base + Cfg::SFB_COL + 4 * Cfg::SF_CHUNKS_B * sfb;
-            tmem_cp_32x128b_warpx4(sfa_t,
-                                   smem_desc(smem_u32(smem + Cfg::OFF_UTA + s * Cfg::UT_A), 0,
-                                             128, 0));
-#pragma unroll
-            for (int c = 0; c < Cfg::SF_CHUNKS_B; ++c)
-              tmem_cp_32x128b_warpx4(
-                  sfb_t + 4 * c,
-                  smem_desc(smem_u32(smem + Cfg::OFF_UTB + s * Cfg::UT_B + 512 * c), 0, 128, 0));
-#pragma unroll
-            for (int ks = 0; ks < Cfg::KSTEPS; ++ks) {
-              const uint64_t ad =
-                  smem_desc(a0 + ks * Cfg::KSTEP_BYTES, Cfg::A_LBO, 1024, 2);
-              const uint64_t bd =
-                  smem_desc(b0 + ks * Cfg::KSTEP_BYTES, Cfg::ATOM_BYTES, 1024, 2);
-              mma_mxf8(d_tmem, ad, bd, idesc_mxf8(Cfg::BM, kBN, ks, ks), sfa_t, sfb_t,
-                       (j | ks) != 0);
-            }
-          } else {
-#pragma unroll
-            for (int ks = 0; ks < Cfg::KSTEPS; ++ks) {
-              const uint64_t ad =
-                  smem_desc(a0 + ks * Cfg::KSTEP_BYTES, Cfg::A_LBO, 1024, 2);
-              const uint64_t bd =
-                  smem_desc(b0 + ks * Cfg::KSTEP_BYTES, Cfg::ATOM_BYTES, 1024, 2);
-              mma_bf16(d_tmem, ad, bd, idesc_bf16(Cfg::BM, kBN), (j | ks) != 0);
-            }
-          }
-          mma_commit(&empty[s]);
-        }
-        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(sfr_leader + 8 * g);
+        ++rg;
+        have_r = group_cursor_next(rc, p, gs, kBN, R, rank);
       }
-      if (!ok) break;
-      if (lane == 0) mma_commit(&accf[b]);
-      __syncwarp();
+      // Let every scale load this warp started land before the CTA can exit.
+      if (lane == 0)
+        for (uint32_t i = rg; i < ig; ++i)
+          mbar_wait(&sff[i % NS], (i / NS) & 1, abort_flag, lim, p.status, W_PROD_DRAIN,
+                    static_cast<int>(i), false);
     }
-    // Drain: every tcgen05 op this thread issued completes before tensor
-    // memory is released.
-    if (lane == 0) mma_commit(drain);
-    __syncwarp();
-    mbar_wait(drain, 0, abort_flag, lim, p.status, W_MMA_DRAIN, 0, false);
-    __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;               // tensor-memory lane quadrant of this warp
@@ -333,45 +547,52 @@ __global__ void __launch_bounds__(192, 1)
     uint32_t tl = 0, nchunk_done = 0;
     uint32_t cuse[2] = {0, 0};
     constexpr bool kHasC = (kOut == OUT_F32_C);
-    for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
-      const int gi = t / p.tiles_per_group;
-      const int lt = t - gi * p.tiles_per_group;
-      const int e = p.sched[gi].expert;
-      const int mt = lt / p.n_tiles;
-      const int m0 = mt * Cfg::BM;
-      const int n0 = (lt - mt * p.n_tiles) * kBN;
-      const bool mma_tile = t < p.num_mma_tiles;
+    const uint64_t stream_out = l2_policy_evict_first();   // D is written once
+    const uint32_t acce_leader = mapa_shared(smem_u32(&acce[0]), 0);
+    uint32_t r[32];   // tensor-memory chunk in flight
+    for (int t = pid; t < p.num_tiles; t += R) {
+      const int u = interleaved_tile(t, p.num_tiles, R);
+      const TileCoord tc = tile_coord(p, u, kBN, rank);
+      const bool mma_tile = u < p.num_mma_tiles;
       const int b = tl & 1;
       if (mma_tile) {
+        DG_T0(w0);
         const bool got =
             mbar_wait(&accf[b], (tl >> 1) & 1, abort_flag, lim, p.status, W_EPI_ACCF, t);
+        DG_TACC(1, w0);
         if (!epi_all(got)) break;
         tc_fence_after();
       }
-      const int ncols = min(kBN, p.N - n0);
+      const int ncols = min(kBN, p.N - tc.n0);
       const int nch = (ncols + 31) / 32;
+      const uint32_t tmem_row = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + b * kBN;
+      if (mma_tile) tmem_ld_32x32b_x32(tmem_row, r);
       bool ok = true;
       for (int c = 0; c < nch; ++c, ++nchunk_done) {
         const int sbuf = nchunk_done & 1;
         uint8_t *stg = smem + Cfg::OFF_STG + sbuf * Cfg::STG_BYTES;
+        DG_T0(w1);
         if (etid == 0) bulk_wait_read<1>();    // the store that last used stg is done reading
         named_bar_sync(1, 128);
+        DG_TACC(2, w1);
         if (kHasC && etid == 0) {
           mbar_arrive_expect_tx(&cbar[sbuf], 128 * 128);
-          tma_load_3d(stg, &p.tmC, &cbar[sbuf], n0 + 32 * c, m0, e);
+          tma_load_3d(stg, &p.tmC, &cbar[sbuf], tc.n0 + 32 * c, tc.m0, tc.expert);
         }
         float v[32];
         if (mma_tile) {
-          uint32_t r[32];
-          tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(32 * q) << 16) + b * kBN + 32 * c,
-                             r);
+          // Chunk c was requested one iteration earlier; request chunk c + 1
+          // now so that it streams in while this one is staged.
           tmem_wait_ld();
+          tmem_reg_fence(r);
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-          if (c == nch - 1) {
+          if (c + 1 < nch) {
+            tmem_ld_32x32b_x32(tmem_row + 32 * (c + 1), r);
+          } else {
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&acce[b]);
+            if (lane == 0) mbar_arrive_cluster(acce_leader + 8 * b);
           }
         } else {
 #pragma unroll
@@ -415,12 +636,14 @@ __global__ void __launch_bounds__(192, 1)
                 make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
         }
         fence_proxy_async_smem();
+        DG_T0(w2);
         named_bar_sync(1, 128);
+        DG_TACC(3, w2);
         if (etid == 0) {
           if constexpr (kOut == OUT_F32_REDUCE)
-            tma_reduce_add_3d(&p.tmD, stg, n0 + 32 * c, m0, e);
+            tma_reduce_add_3d_hint(&p.tmD, stg, tc.n0 + 32 * c, tc.m0, tc.expert, stream_out);
           else
-            tma_store_3d(&p.tmD, stg, n0 + 32 * c, m0, e);
+            tma_store_3d_hint(&p.tmD, stg, tc.n0 + 32 * c, tc.m0, tc.expert, stream_out);
           bulk_commit();
         }
       }
@@ -430,36 +653,67 @@ __global__ void __launch_bounds__(192, 1)
     if (etid == 0) bulk_wait<0>();
   }
 
+#ifdef DG_KERNEL_TIMERS
+  // Per CTA 32 counters, 8 per role (producer, MMA, warp 6, epilogue warp 2):
+  // the role's wait counters tm[0..3], then its total cycles.
+  if (lane == 0 && p.timers != nullptr && (warp <= 2 || warp == 6)) {
+    const int role = warp == 0 ? 0 : warp == 1 ? 1 : warp == 6 ? 2 : 3;
+    unsigned long long *o = p.timers + blockIdx.x * 32 + role * 8;
+    for (int i = 0; i < 4; ++i) o[i] = tm[i];
+    o[4] = clock64() - t_start;
+  }
+#endif
+
+  // Neither CTA may release its shared or tensor memory while the pair's MMAs
+  // or the partner's remote arrivals may still touch it.
   tc_fence_before();
-  __syncthreads();
+  cluster_sync();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+    tmem_dealloc_pair(tmem_base, Cfg::TMEM_COLS);
   }
 }
 
 template <bool kFP8, int kBN, int kOut>
-cudaError_t launch_wgrad_variant(const WgradParams &p, int grid, cudaStream_t stream) {
+cudaError_t launch_wgrad_variant(const WgradParams &p, int pairs, cudaStream_t stream) {
   using Cfg = WgradCfg<kFP8, kBN>;
   auto kern = kgrouped_wgrad_kernel<kFP8, kBN, kOut>;
   static bool attr_set = false;
+  static int max_pairs = 0;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kWgradThreads, 1, 1);
+  cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   if (!attr_set) {
     cudaError_t err =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
     if (err != cudaSuccess) return err;
+    cfg.gridDim = dim3(2 * pairs, 1, 1);
+    int n = 0;
+    err = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+    if (err != cudaSuccess) return err;
+    max_pairs = n;
     attr_set = true;
   }
-  kern<<<grid, 192, Cfg::SMEM_BYTES, stream>>>(p);
-  return cudaGetLastError();
+  if (max_pairs > 0) pairs = min(pairs, max_pairs);
+  cfg.gridDim = dim3(2 * pairs, 1, 1);
+  return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
 template <bool kFP8, int kBN>
-cudaError_t launch_wgrad_bn(const WgradParams &p, int grid, cudaStream_t stream) {
+cudaError_t launch_wgrad_bn(const WgradParams &p, int pairs, cudaStream_t stream) {
   switch (p.out_mode) {
-    case OUT_F32: return launch_wgrad_variant<kFP8, kBN, OUT_F32>(p, grid, stream);
-    case OUT_F32_REDUCE: return launch_wgrad_variant<kFP8, kBN, OUT_F32_REDUCE>(p, grid, stream);
-    case OUT_F32_C: return launch_wgrad_variant<kFP8, kBN, OUT_F32_C>(p, grid, stream);
-    case OUT_BF16: return launch_wgrad_variant<kFP8, kBN, OUT_BF16>(p, grid, stream);
+    case OUT_F32: return launch_wgrad_variant<kFP8, kBN, OUT_F32>(p, pairs, stream);
+    case OUT_F32_REDUCE: return launch_wgrad_variant<kFP8, kBN, OUT_F32_REDUCE>(p, pairs, stream);
+    case OUT_F32_C: return launch_wgrad_variant<kFP8, kBN, OUT_F32_C>(p, pairs, stream);
+    case OUT_BF16: return launch_wgrad_variant<kFP8, kBN, OUT_BF16>(p, pairs, stream);
   }
   return cudaErrorInvalidValue;
 }
