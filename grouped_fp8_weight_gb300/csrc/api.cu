@@ -1,6 +1,8 @@
 // C-ABI entry points: argument validation, the expert schedule, TMA tensor
-// maps and kernel launches.  No allocation per call; the only allocation is
-// one status word per device on first use.
+// maps and kernel launches.  Allocation: one status word per device on first
+// use and, per FP8 call, stream-ordered scratch for the packed scale factors
+// from a memory pool this library owns (returned to the pool on the same
+// stream once the GEMM is queued; the pool keeps it for the next call).
 #include <algorithm>
 #include <cstdarg>
 #include <cstdio>
@@ -51,6 +53,7 @@ struct DeviceState {
   int major = 0, minor = 0;
   int sms = 0;
   dg::DevStatus *status = nullptr;
+  cudaMemPool_t pool = nullptr;   // packed scale-factor scratch
 };
 
 constexpr int kMaxDevices = 64;
@@ -78,6 +81,16 @@ dg_status device_state(DeviceState **out) {
       if ((e = cudaMalloc(&st.status, sizeof(dg::DevStatus))) != cudaSuccess ||
           (e = cudaMemset(st.status, 0, sizeof(dg::DevStatus))) != cudaSuccess)
         return fail(DG_ERR_CUDA, "status word: %s", cudaGetErrorString(e));
+      cudaMemPoolProps props{};
+      props.allocType = cudaMemAllocationTypePinned;
+      props.handleTypes = cudaMemHandleTypeNone;
+      props.location.type = cudaMemLocationTypeDevice;
+      props.location.id = dev;
+      uint64_t keep = ~0ull;   // keep freed blocks for reuse instead of releasing them
+      if ((e = cudaMemPoolCreate(&st.pool, &props)) != cudaSuccess ||
+          (e = cudaMemPoolSetAttribute(st.pool, cudaMemPoolAttrReleaseThreshold, &keep)) !=
+              cudaSuccess)
+        return fail(DG_ERR_CUDA, "memory pool: %s", cudaGetErrorString(e));
     }
     if (g_encode == nullptr) {
       void *fn = nullptr;
@@ -245,6 +258,10 @@ dg_status run_grouped(const GroupedArgs &x) {
   p.timers = g_timers;
 #endif
   if (p.num_tiles == 0) return ok();     // every expert empty and D accumulates in place
+  std::unique_ptr<dg::PackParams> pk_hold(new dg::PackParams);   // ~12 KB
+  dg::PackParams &pk = *pk_hold;
+  std::memset(&pk, 0, sizeof(pk));
+  const size_t sf_bytes = (x.fp8 && n_mma > 0) ? dg::plan_scale_pack(p, pk, n_mma, x.gran_k, bn) : 0;
 
   // ---- tensor maps
   const uint64_t M = x.M, N = x.N, G = x.G, SK = x.sum_k;
@@ -259,17 +276,8 @@ dg_status run_grouped(const GroupedArgs &x) {
       s = encode(&p.tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, x.b, 2, db, sb, box,
                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "b");
       if (s) return s;
-      const uint64_t nb = SK / x.gran_k;
-      const uint64_t dsa[2] = {M, nb}, dsb[2] = {N, nb};
-      // Four scale rows per box: one scale group of the kernel (four k-blocks
-      // at gran_k 128, the four sub-blocks of one k-block at gran_k 32).
-      const uint32_t bsa[2] = {128, 4};
-      const uint32_t bsb[2] = {static_cast<uint32_t>(bn), 4};
-      if ((s = encode(&p.tmSFA, CU_TENSOR_MAP_DATA_TYPE_UINT8, x.sfa, 2, dsa, sa, bsa,
-                      CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE, "sfa")) ||
-          (s = encode(&p.tmSFB, CU_TENSOR_MAP_DATA_TYPE_UINT8, x.sfb, 2, dsb, sb, bsb,
-                      CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE, "sfb")))
-        return s;
+      // The packed scale records are mapped (and the scratch taken) below,
+      // once every other map has been encoded.
     } else {
       const uint64_t da[2] = {M, SK}, sa[1] = {2 * M};
       const uint64_t db[2] = {N, SK}, sb[1] = {2 * N};
@@ -285,7 +293,7 @@ dg_status run_grouped(const GroupedArgs &x) {
     const bool bf = (x.d_dtype == DG_BF16);
     const uint64_t es = bf ? 2 : 4;
     const uint64_t dd[3] = {N, M, G}, sd[2] = {es * N, es * N * M};
-    const uint32_t box[3] = {32, 128, 1};
+    const uint32_t box[3] = {32, 32, 1};
     if ((s = encode(&p.tmD,
                     bf ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, x.d,
                     3, dd, sd, box, bf ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
@@ -297,10 +305,36 @@ dg_status run_grouped(const GroupedArgs &x) {
       return s;
   }
 
+  // ---- FP8 scale records: scratch from the pool, their tensor maps, the pack pass
+  void *scratch = nullptr;
+  cudaError_t e = cudaSuccess;
+  if (sf_bytes > 0) {
+    if ((e = cudaMallocFromPoolAsync(&scratch, sf_bytes, dev->pool, x.stream)) != cudaSuccess)
+      return fail(DG_ERR_CUDA, "%s: scale scratch (%zu bytes): %s", fn, sf_bytes,
+                  cudaGetErrorString(e));
+    dg::bind_scale_pack(pk, scratch, x.sfa, x.sfb);
+    const uint64_t rec[1] = {512};
+    const uint64_t dpa[2] = {128, static_cast<uint64_t>(pk.n_groups) * pk.MC};
+    const uint64_t dpb[2] = {128, static_cast<uint64_t>(pk.n_groups) * pk.NT * pk.CB};
+    const uint32_t bpa[2] = {128, 1}, bpb[2] = {128, static_cast<uint32_t>(pk.CB)};
+    if ((s = encode(&p.tmSFA, CU_TENSOR_MAP_DATA_TYPE_UINT32, pk.sfa_p, 2, dpa, rec, bpa,
+                    CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE, "sfa records")) ||
+        (s = encode(&p.tmSFB, CU_TENSOR_MAP_DATA_TYPE_UINT32, pk.sfb_p, 2, dpb, rec, bpb,
+                    CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE, "sfb records"))) {
+      cudaFreeAsync(scratch, x.stream);
+      return s;
+    }
+    if ((e = dg::launch_pack_scales(pk, x.stream)) != cudaSuccess) {
+      cudaFreeAsync(scratch, x.stream);
+      return fail(DG_ERR_CUDA, "%s: scale pack launch failed: %s", fn, cudaGetErrorString(e));
+    }
+  }
+
   // ---- launch: one persistent CTA pair per two SMs (or per tile when fewer)
   const int pairs = std::min(dev->sms / 2, p.num_tiles);
-  cudaError_t e = x.fp8 ? dg::launch_kgrouped_fp8(p, bn, pairs, x.stream)
-                        : dg::launch_kgrouped_bf16(p, bn, pairs, x.stream);
+  e = x.fp8 ? dg::launch_kgrouped_fp8(p, bn, pairs, x.stream)
+            : dg::launch_kgrouped_bf16(p, bn, pairs, x.stream);
+  if (scratch != nullptr) cudaFreeAsync(scratch, x.stream);   // after the GEMM in stream order
   if (e != cudaSuccess)
     return fail(DG_ERR_CUDA, "%s: launch failed: %s", fn, cudaGetErrorString(e));
   return ok();

@@ -2,18 +2,24 @@
 // callers that cannot allocate device memory.
 //
 // The ordinary entry point allocates one small status record per device with
-// cudaMalloc on its first call; the kernel writes timeouts and ks_dev
-// mismatches there.  Some callers cannot let a library do that: a framework
-// whose caching allocator has already reserved the device memory it is allowed
-// to use, or a thread that must not take the implicit device synchronisation a
-// cudaMalloc can cause.  This variant runs the same kernel with that record
-// placed in a file-scope __device__ array instead, so it allocates nothing.
+// cudaMalloc on its first call (the kernel writes timeouts and ks_dev
+// mismatches there) and takes scratch for the packed scale factors from a
+// memory pool on every call.  Some callers cannot let a library do that: a
+// framework whose caching allocator has already reserved the device memory it
+// is allowed to use, or a thread that must not take the implicit device
+// synchronisation a cudaMalloc can cause.  This variant runs the same kernels
+// with both placed in a file-scope __device__ array instead, so it allocates
+// nothing.
 //
-// Scratch: kScratchBytes (256) bytes, of which one 16-byte status record is
-// used per call, whatever the problem size.  Every GPU that loads the library
-// holds the array until the process exits.  All calls on a device share it:
-// each call clears the record on its stream before the launch, and calls that
-// overlap on the GPU (different streams) race on it.  This entry point never
+// Scratch: kScratchBytes = 256 bytes for the 16-byte status record plus
+// kScaleBytes (32 MiB) for the packed scale records, whose size is
+// (scale groups) x (2 * ceil(M / 256) + ceil(N / BN) * ceil(BN / 128)) x 512
+// bytes, with one scale group per four k-blocks of each expert (gran_k 128) or
+// per k-block (gran_k 32); larger problems are rejected with
+// DG_ERR_UNSUPPORTED.  Every GPU that loads this part of the library holds the
+// array until the process exits.  All calls on a device share it: each call
+// clears the record and rewrites the scale records on its stream before the
+// GEMM, and calls that overlap on the GPU (different streams) race on it.  This entry point never
 // synchronises, so it does not report what the kernel records there; the
 // kernel's waits are still bounded, so a wait that runs out ends the kernel
 // early and leaves D unspecified.
@@ -38,12 +44,15 @@ void set_last_error(const char *msg);   // api.cu
 
 namespace {
 
-constexpr size_t kScratchBytes = 256;
-static_assert(sizeof(dg::DevStatus) <= kScratchBytes, "status record must fit the scratch");
+constexpr size_t kStatusBytes = 256;
+constexpr size_t kScaleBytes = size_t(32) << 20;
+constexpr size_t kScratchBytes = kStatusBytes + kScaleBytes;
+static_assert(sizeof(dg::DevStatus) <= kStatusBytes, "status record must fit the scratch");
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
 thread_local dg::WgradParams t_params;   // reused per thread: no per-call heap allocation
+thread_local dg::PackParams t_pack;
 
 dg_status nfail(dg_status s, const char *fmt, ...) {
   char buf[512];
@@ -59,6 +68,7 @@ struct NoAllocDevice {
   bool ready = false;
   int sms = 0;
   dg::DevStatus *scratch = nullptr;   // device address of g_noalloc_scratch
+  unsigned char *scales = nullptr;    // the packed scale records, kStatusBytes in
 };
 
 constexpr int kMaxDev = 64;
@@ -91,6 +101,7 @@ dg_status setup(NoAllocDevice **out) {
     if (e != cudaSuccess || ptr == nullptr)
       return nfail(DG_ERR_CUDA, "cudaGetSymbolAddress(scratch): %s", cudaGetErrorString(e));
     st.scratch = static_cast<dg::DevStatus *>(ptr);
+    st.scales = static_cast<unsigned char *>(ptr) + kStatusBytes;
     if (n_encode == nullptr) {
       void *fn = nullptr;
       cudaDriverEntryPointQueryResult q{};
@@ -123,7 +134,7 @@ dg_status map_out(CUtensorMap *m, bool bf16, const void *ptr, uint64_t M, uint64
                   uint64_t G, const char *what) {
   const uint64_t es = bf16 ? 2 : 4;
   const cuuint64_t dims[3] = {N, M, G}, strides[2] = {es * N, es * N * M};
-  const cuuint32_t box[3] = {32, 128, 1}, ones[3] = {1, 1, 1};
+  const cuuint32_t box[3] = {32, 32, 1}, ones[3] = {1, 1, 1};
   CUresult r = n_encode(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
                         3, const_cast<void *>(ptr), dims, strides, box, ones,
                         CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -236,25 +247,37 @@ extern "C" dg_status dg_k_grouped_fp8_wgrad_noalloc(
     dg::set_last_error("");
     return DG_OK;
   }
-  const uint64_t SK = sum_k, nb = sum_k / gran_k;
-  const uint32_t rows = 4;   // scale rows per box: one scale group of the kernel
-  if (p.num_mma_tiles > 0 &&
-      ((s = map2d(&p.tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, a, M, SK, M, 128, 128,
-                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "a")) ||
-       (s = map2d(&p.tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, b, N, SK, N, 128, 128,
-                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "b")) ||
-       (s = map2d(&p.tmSFA, CU_TENSOR_MAP_DATA_TYPE_UINT8, sfa, M, nb, M, 128, rows,
-                  CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE, "sfa")) ||
-       (s = map2d(&p.tmSFB, CU_TENSOR_MAP_DATA_TYPE_UINT8, sfb, N, nb, N,
-                  static_cast<uint32_t>(bn), rows, CU_TENSOR_MAP_SWIZZLE_NONE,
-                  CU_TENSOR_MAP_L2_PROMOTION_NONE, "sfb"))))
-    return s;
+  dg::PackParams &pk = t_pack;
+  std::memset(&pk, 0, sizeof(pk));
+  const size_t sf_bytes = (n_mma > 0) ? dg::plan_scale_pack(p, pk, n_mma, gran_k, bn) : 0;
+  if (sf_bytes > kScaleBytes)
+    return nfail(DG_ERR_UNSUPPORTED,
+                 "%s: the packed scale factors need %zu bytes, above this entry point's %zu",
+                 fn, sf_bytes, kScaleBytes);
+  const uint64_t SK = sum_k;
+  if (p.num_mma_tiles > 0) {
+    dg::bind_scale_pack(pk, dev->scales, sfa, sfb);
+    const uint64_t groups = static_cast<uint64_t>(pk.n_groups);
+    if ((s = map2d(&p.tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, a, M, SK, M, 128, 128,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "a")) ||
+        (s = map2d(&p.tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, b, N, SK, N, 128, 128,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "b")) ||
+        (s = map2d(&p.tmSFA, CU_TENSOR_MAP_DATA_TYPE_UINT32, pk.sfa_p, 128, groups * pk.MC, 512,
+                   128, 1, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                   "sfa records")) ||
+        (s = map2d(&p.tmSFB, CU_TENSOR_MAP_DATA_TYPE_UINT32, pk.sfb_p, 128,
+                   groups * pk.NT * pk.CB, 512, 128, static_cast<uint32_t>(pk.CB),
+                   CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE, "sfb records")))
+      return s;
+  }
   if ((s = map_out(&p.tmD, d_dtype == DG_BF16, d, M, N, G, "d"))) return s;
   if (p.out_mode == dg::OUT_F32_C && (s = map_out(&p.tmC, false, c, M, N, G, "c"))) return s;
 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = cudaMemsetAsync(dev->scratch, 0, sizeof(dg::DevStatus), st);
   if (e != cudaSuccess) return nfail(DG_ERR_CUDA, "%s: clearing scratch: %s", fn, cudaGetErrorString(e));
+  if (sf_bytes > 0 && (e = dg::launch_pack_scales(pk, st)) != cudaSuccess)
+    return nfail(DG_ERR_CUDA, "%s: scale pack launch failed: %s", fn, cudaGetErrorString(e));
   e = dg::launch_kgrouped_fp8(p, bn, std::min(dev->sms / 2, p.num_tiles), st);
   if (e != cudaSuccess) return nfail(DG_ERR_CUDA, "%s: launch failed: %s", fn, cudaGetErrorString(e));
   dg::set_last_error("");

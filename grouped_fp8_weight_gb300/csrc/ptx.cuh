@@ -99,6 +99,14 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
                : "memory");
 }
+// 16-byte store into shared memory given by its cluster address (possibly
+// in the peer CTA).
+__device__ __forceinline__ void st_shared_cluster_v4(uint32_t cluster_addr, uint32_t a, uint32_t b,
+                                                     uint32_t c, uint32_t d) {
+  asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(cluster_addr), "r"(a),
+               "r"(b), "r"(c), "r"(d)
+               : "memory");
+}
 // Cluster-wide barrier.  The non-.aligned forms tolerate a warp whose lanes
 // arrive at different times (single-thread roles reaching the end late).
 __device__ __forceinline__ void cluster_sync() {

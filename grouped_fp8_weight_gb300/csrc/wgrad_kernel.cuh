@@ -23,14 +23,15 @@
 //   warp 1      tensor-memory allocation (collective over the pair); in the
 //               even CTA one thread issues tcgen05.cp per scale group and four
 //               tcgen05.mma per stage, committing to both CTAs' barriers.
-//   warps 2..5  epilogue: tensor memory -> registers -> swizzled shared-memory
-//               staging -> TMA store (or TMA reduce-add for in-place D += acc)
-//               of this CTA's 128 rows.
-//   warp 6      FP8: scale warp -- fetches this CTA's scale rows (its 128 rows
-//               of A, all BN columns of B) per group of four UE8M0 rows, up to
-//               four groups ahead, and repacks them into the tensor-memory
-//               scale layout.  BF16 (even CTA): stage gate -- zeroes the token
-//               rows past an expert's slice in both CTAs' last stage.
+//   warps 2..5  epilogue, one warp per tensor-memory lane quadrant (32 rows),
+//               each on its own: tensor memory -> registers -> swizzled
+//               shared-memory staging -> TMA store (or TMA reduce-add for
+//               in-place D += acc) of 32 x 32 boxes.
+//   warp 6      FP8: scale loader -- fetches each scale group's packed
+//               records (written beforehand by the scale pack pass in the
+//               layout tcgen05.cp copies into tensor memory) up to five groups
+//               ahead.  BF16 (even CTA): stage gate -- zeroes the token rows
+//               past an expert's slice in both CTAs' last stage.
 // Two accumulators live in tensor memory, so the epilogue of one tile overlaps
 // the MMAs of the next.
 //
@@ -71,15 +72,17 @@ struct WgradCfg {
   static constexpr int NUM_ACC = 2;
   // FP8 scale groups: four UE8M0 rows (four k-blocks at gran_k 128, the four
   // 32-token sub-blocks of one k-block at gran_k 32), in a ring of SF_SLOTS.
-  static constexpr int SF_SLOTS = kFP8 ? 4 : 0;
+  // FP8 scale groups: four UE8M0 rows (four k-blocks at gran_k 128, the four
+  // 32-token sub-blocks of one k-block at gran_k 32), in a ring of SF_SLOTS.
+  // Each slot holds the group's packed records (UT_A for this CTA's 128 rows
+  // of A, UT_B for the tile's BN columns of B) as tcgen05.cp reads them.
+  static constexpr int SF_SLOTS = kFP8 ? 5 : 0;
   static constexpr int SF_CHUNKS_B = kFP8 ? (kBN + 127) / 128 : 0;
-  static constexpr int SFA_RAW = 512;                   // 4 rows x 128
-  static constexpr int SFB_RAW = ((kBN * 4 + 127) / 128) * 128;
   static constexpr int UT_A = 512;                      // 32 rows x 16 bytes
   static constexpr int UT_B = 512 * SF_CHUNKS_B;
   static constexpr int SF_COLS = 4 + 4 * SF_CHUNKS_B;   // tensor-memory columns per slot
   static constexpr int SF_COL0 = NUM_ACC * kBN;
-  static constexpr int STG_BYTES = 16384;               // 128 rows x 128 bytes
+  static constexpr int WSTG_BYTES = 4096;               // per epilogue warp and buffer: 32 rows x 128 bytes
   static constexpr int TMEM_COLS = 512;
   static_assert(SF_COL0 + SF_SLOTS * SF_COLS <= TMEM_COLS, "tmem budget");
   static_assert(kBN % 32 == 0 && kBN <= 256, "block N");
@@ -87,13 +90,12 @@ struct WgradCfg {
   static constexpr int OFF_B = 0;
   static constexpr int OFF_A = OFF_B + STAGES * B_BYTES;
   static constexpr int OFF_STG = OFF_A + STAGES * A_BYTES;
-  static constexpr int OFF_SFA = OFF_STG + 2 * STG_BYTES;
-  static constexpr int OFF_SFB = OFF_SFA + SF_SLOTS * SFA_RAW;
-  static constexpr int OFF_UTA = OFF_SFB + SF_SLOTS * SFB_RAW;
+  static constexpr int OFF_UTA = OFF_STG + 4 * 2 * WSTG_BYTES;
   static constexpr int OFF_UTB = OFF_UTA + SF_SLOTS * UT_A;
   static constexpr int OFF_BAR = (OFF_UTB + SF_SLOTS * UT_B + 7) / 8 * 8;
-  // barriers: full[S], empty[S], gate[S], accf[2], acce[2], cbar[2], sff/sfr/sfe[SLOTS], drain
-  static constexpr int NUM_BARS = 3 * STAGES + 2 * NUM_ACC + 2 + 3 * SF_SLOTS + 1;
+  // barriers: full[S], empty[S], gate[S], accf[2], acce[2], cbar[4 warps x 2],
+  // sfr/sfe[SLOTS], drain
+  static constexpr int NUM_BARS = 3 * STAGES + 2 * NUM_ACC + 8 + 2 * SF_SLOTS + 1;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;   // + alignment slack
   static_assert(SMEM_BYTES <= 232448, "shared memory");
@@ -131,6 +133,7 @@ __device__ __forceinline__ int interleaved_tile(int t, int n, int R) {
 
 struct TileCoord {
   int expert, k_off, k_len, m0, n0;   // m0: this CTA's first row; n0: the pair's first column
+  int nt, g_off;                      // N-tile index; first packed scale group of the expert
 };
 
 __device__ __forceinline__ TileCoord tile_coord(const WgradParams &p, int u, int bn,
@@ -141,7 +144,7 @@ __device__ __forceinline__ TileCoord tile_coord(const WgradParams &p, int u, int
   const int mt = p.m_fastest ? lt % p.m_tiles : lt / p.n_tiles;
   const int nt = p.m_fastest ? lt / p.m_tiles : lt % p.n_tiles;
   return TileCoord{se.expert, se.k_off, se.k_len, mt * 256 + static_cast<int>(rank) * 128,
-                   nt * bn};
+                   nt * bn, nt, se.g_off};
 }
 
 // Walks the FP8 scale groups of a pair's tiles in order: a group is gs
@@ -198,9 +201,8 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
   uint64_t *gate = bars + 2 * S;   // BF16, even CTA: tail rows masked in both CTAs
   uint64_t *accf = bars + 3 * S;   // accumulator ready (multicast commit)
   uint64_t *acce = accf + 2;       // even CTA: accumulator drained by both epilogues
-  uint64_t *cbar = acce + 2;       // separate-C tile landed
-  uint64_t *sff = cbar + 2;        // scale group landed (this CTA)
-  uint64_t *sfr = sff + NS;        // even CTA: scale group repacked in both CTAs
+  uint64_t *cbar = acce + 2;       // separate-C box landed (per epilogue warp and buffer)
+  uint64_t *sfr = cbar + 8;        // even CTA: both CTAs' records of a scale group landed
   uint64_t *sfe = sfr + NS;        // scale slot free (its tcgen05.cp completed)
   uint64_t *drain = sfe + NS;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Cfg::OFF_MISC);
@@ -216,7 +218,7 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
   // k-blocks covered by one scale group
   const int gs = kFP8 ? (p.gran_k == 128 ? 4 : 1) : 1;
 #ifdef DG_KERNEL_TIMERS
-  unsigned long long tm[4] = {0, 0, 0, 0};
+  unsigned long long tm[7] = {0, 0, 0, 0, 0, 0, 0};
   const unsigned long long t_start = clock64();
 #endif
 
@@ -229,11 +231,10 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&accf[i], 1);
       mbar_init(&acce[i], 8);       // four epilogue warps in each CTA
-      mbar_init(&cbar[i], 1);
     }
+    for (int i = 0; i < 8; ++i) mbar_init(&cbar[i], 1);
     for (int i = 0; i < NS; ++i) {
-      mbar_init(&sff[i], 1);
-      mbar_init(&sfr[i], 2);        // the scale warp of each CTA
+      mbar_init(&sfr[i], 1);
       mbar_init(&sfe[i], 1);
     }
     mbar_init(drain, 1);
@@ -457,98 +458,64 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
         }
       }
     } else {
-      // ---------------------------------------------------------- scale warp
-      // Fetches each scale group of this CTA (TMA, up to SF_SLOTS groups
-      // ahead) and repacks it into the tensor-memory scale layout: for each
-      // 128-row chunk, 32 rows of 16 bytes where row l, word q, byte i holds
-      // scale row i of matrix row 32q + l.
+      // ---------------------------------------------------------- scale loader
+      // Each CTA fetches, per scale group, its packed records (its 128 rows
+      // of A, the tile's BN columns of B) into the group's slot once the
+      // tcgen05.cp of the slot's previous group has completed; both CTAs'
+      // bytes complete on the even CTA's `sfr`.
       if (lane == 0) {
         prefetch_tmap(&p.tmSFA);
         prefetch_tmap(&p.tmSFB);
-      }
-      GroupCursor ic, rc;
-      group_cursor_init(ic, pid, R);
-      group_cursor_init(rc, pid, R);
-      bool have_i = group_cursor_next(ic, p, gs, kBN, R, rank);
-      bool have_r = group_cursor_next(rc, p, gs, kBN, R, rank);
-      const uint32_t sfr_leader = mapa_shared(smem_u32(&sfr[0]), 0);
-      uint32_t ig = 0, rg = 0;
-      bool ok = true;
-      while (ok && have_r) {
-        while (have_i && ig < rg + NS) {
-          const int slot = ig % NS;
+        const uint64_t keep = l2_policy_evict_last();   // B's records serve every M tile
+        const uint32_t sfr_leader = mapa_shared(smem_u32(&sfr[0]), 0);
+        GroupCursor ic;
+        group_cursor_init(ic, pid, R);
+        bool have = group_cursor_next(ic, p, gs, kBN, R, rank);
+        uint32_t ig = 0;
+        bool ok = true;
+        while (ok && have) {
+          const int g = ig % NS;
           DG_T0(w0);
-          ok = mbar_wait(&sfe[slot], ((ig / NS) & 1) ^ 1, abort_flag, lim, p.status, W_PROD_SFE,
+          ok = mbar_wait(&sfe[g], ((ig / NS) & 1) ^ 1, abort_flag, lim, p.status, W_PROD_SFE,
                          ic.t);
-          ok = __all_sync(0xffffffffu, ok);
           DG_TACC(2, w0);
           if (!ok) break;
-          if (lane == 0) {
-            const int row = (ic.tc.k_off + ic.j * 128) / p.gran_k;
-            mbar_arrive_expect_tx(&sff[slot], (128 + kBN) * 4);
-            tma_load_2d(smem + Cfg::OFF_SFA + slot * Cfg::SFA_RAW, &p.tmSFA, &sff[slot],
-                        ic.tc.m0, row);
-            tma_load_2d(smem + Cfg::OFF_SFB + slot * Cfg::SFB_RAW, &p.tmSFB, &sff[slot],
-                        ic.tc.n0, row);
-          }
+          if (leader) mbar_arrive_expect_tx(&sfr[g], 2 * (Cfg::UT_A + Cfg::UT_B));
+          const int grp = ic.tc.g_off + ic.j / gs;
+          tma_load_2d_pair(smem + Cfg::OFF_UTA + g * Cfg::UT_A, &p.tmSFA, sfr_leader + 8 * g, 0,
+                           grp * p.sf_mc + ic.tc.m0 / 128, keep);
+          tma_load_2d_pair(smem + Cfg::OFF_UTB + g * Cfg::UT_B, &p.tmSFB, sfr_leader + 8 * g, 0,
+                           (grp * p.n_tiles + ic.tc.nt) * Cfg::SF_CHUNKS_B, keep);
           ++ig;
-          have_i = group_cursor_next(ic, p, gs, kBN, R, rank);
+          have = group_cursor_next(ic, p, gs, kBN, R, rank);
         }
-        if (!ok) break;
-        const int g = rg % NS;
-        DG_T0(w1);
-        ok = mbar_wait(&sff[g], (rg / NS) & 1, abort_flag, lim, p.status, W_SF_FULL, rc.t);
-        ok = __all_sync(0xffffffffu, ok);
-        DG_TACC(3, w1);
-        if (!ok) break;
-        const uint8_t *ra = smem + Cfg::OFF_SFA + g * Cfg::SFA_RAW;
-        const uint8_t *rb = smem + Cfg::OFF_SFB + g * Cfg::SFB_RAW;
-        uint32_t w[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int m = 32 * q + lane;
-          w[q] = static_cast<uint32_t>(ra[m]) | (static_cast<uint32_t>(ra[128 + m]) << 8) |
-                 (static_cast<uint32_t>(ra[256 + m]) << 16) |
-                 (static_cast<uint32_t>(ra[384 + m]) << 24);
+        // Let every record this CTA requested land before the pair can exit:
+        // the even CTA sees them on `sfr`; its partner sees the slots' copies
+        // complete.
+        for (uint32_t i = (ig > static_cast<uint32_t>(NS) ? ig - NS : 0); i < ig; ++i) {
+          if (leader)
+            mbar_wait(&sfr[i % NS], (i / NS) & 1, abort_flag, lim, p.status, W_PROD_DRAIN,
+                      static_cast<int>(i), false);
+          else
+            mbar_wait(&sfe[i % NS], (i / NS) & 1, abort_flag, lim, p.status, W_PROD_DRAIN,
+                      static_cast<int>(i), false);
         }
-        *reinterpret_cast<uint4 *>(smem + Cfg::OFF_UTA + g * Cfg::UT_A + 16 * lane) =
-            make_uint4(w[0], w[1], w[2], w[3]);
-#pragma unroll
-        for (int c = 0; c < Cfg::SF_CHUNKS_B; ++c) {
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int n = 128 * c + 32 * q + lane;
-            w[q] = (n < kBN) ? static_cast<uint32_t>(rb[n]) |
-                                   (static_cast<uint32_t>(rb[kBN + n]) << 8) |
-                                   (static_cast<uint32_t>(rb[2 * kBN + n]) << 16) |
-                                   (static_cast<uint32_t>(rb[3 * kBN + n]) << 24)
-                             : 0u;
-          }
-          *reinterpret_cast<uint4 *>(smem + Cfg::OFF_UTB + g * Cfg::UT_B + 512 * c +
-                                     16 * lane) = make_uint4(w[0], w[1], w[2], w[3]);
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(sfr_leader + 8 * g);
-        ++rg;
-        have_r = group_cursor_next(rc, p, gs, kBN, R, rank);
       }
-      // Let every scale load this warp started land before the CTA can exit.
-      if (lane == 0)
-        for (uint32_t i = rg; i < ig; ++i)
-          mbar_wait(&sff[i % NS], (i / NS) & 1, abort_flag, lim, p.status, W_PROD_DRAIN,
-                    static_cast<int>(i), false);
     }
   } else {
     // ------------------------------------------------------------ epilogue
+    // Each warp owns one tensor-memory lane quadrant (32 rows of this CTA's
+    // 128) and runs its own pipeline, so the four warps never wait on one
+    // another: tcgen05.ld of 32 columns -> one of its two 4 KB swizzled
+    // staging buffers -> TMA store (or reduce-add) of that 32 x 32 box.
     const int q = warp & 3;               // tensor-memory lane quadrant of this warp
-    const int row = 32 * q + lane;        // tile row owned by this thread
-    const int etid = threadIdx.x - 64;    // 0..127
-    uint32_t tl = 0, nchunk_done = 0;
+    uint32_t tl = 0, nchunk = 0;
     uint32_t cuse[2] = {0, 0};
     constexpr bool kHasC = (kOut == OUT_F32_C);
     const uint64_t stream_out = l2_policy_evict_first();   // D is written once
     const uint32_t acce_leader = mapa_shared(smem_u32(&acce[0]), 0);
+    uint8_t *wstg = smem + Cfg::OFF_STG + q * 2 * Cfg::WSTG_BYTES;
+    uint64_t *wcbar = cbar + 2 * q;
     uint32_t r[32];   // tensor-memory chunk in flight
     for (int t = pid; t < p.num_tiles; t += R) {
       const int u = interleaved_tile(t, p.num_tiles, R);
@@ -557,27 +524,27 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
       const int b = tl & 1;
       if (mma_tile) {
         DG_T0(w0);
-        const bool got =
-            mbar_wait(&accf[b], (tl >> 1) & 1, abort_flag, lim, p.status, W_EPI_ACCF, t);
+        bool got = mbar_wait(&accf[b], (tl >> 1) & 1, abort_flag, lim, p.status, W_EPI_ACCF, t);
         DG_TACC(1, w0);
-        if (!epi_all(got)) break;
+        if (!__all_sync(0xffffffffu, got)) break;
         tc_fence_after();
       }
       const int ncols = min(kBN, p.N - tc.n0);
       const int nch = (ncols + 31) / 32;
+      const int row0 = tc.m0 + 32 * q;    // first output row of this warp's boxes
       const uint32_t tmem_row = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + b * kBN;
       if (mma_tile) tmem_ld_32x32b_x32(tmem_row, r);
       bool ok = true;
-      for (int c = 0; c < nch; ++c, ++nchunk_done) {
-        const int sbuf = nchunk_done & 1;
-        uint8_t *stg = smem + Cfg::OFF_STG + sbuf * Cfg::STG_BYTES;
+      for (int c = 0; c < nch; ++c, ++nchunk) {
+        const int sbuf = nchunk & 1;
+        uint8_t *stg = wstg + sbuf * Cfg::WSTG_BYTES;
         DG_T0(w1);
-        if (etid == 0) bulk_wait_read<1>();    // the store that last used stg is done reading
-        named_bar_sync(1, 128);
+        if (lane == 0) bulk_wait_read<1>();    // the store that last used stg is done reading
+        __syncwarp();
         DG_TACC(2, w1);
-        if (kHasC && etid == 0) {
-          mbar_arrive_expect_tx(&cbar[sbuf], 128 * 128);
-          tma_load_3d(stg, &p.tmC, &cbar[sbuf], tc.n0 + 32 * c, tc.m0, tc.expert);
+        if (kHasC && lane == 0) {
+          mbar_arrive_expect_tx(&wcbar[sbuf], 32 * 128);
+          tma_load_3d(stg, &p.tmC, &wcbar[sbuf], tc.n0 + 32 * c, row0, tc.expert);
         }
         float v[32];
         if (mma_tile) {
@@ -599,15 +566,14 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
           for (int i = 0; i < 32; ++i) v[i] = 0.f;
         }
         if constexpr (kHasC) {
-          ok = mbar_wait(&cbar[sbuf], cuse[sbuf] & 1, abort_flag, lim, p.status, W_EPI_C, t);
+          ok = mbar_wait(&wcbar[sbuf], cuse[sbuf] & 1, abort_flag, lim, p.status, W_EPI_C, t);
           cuse[sbuf]++;
-          ok = epi_all(ok);
+          ok = __all_sync(0xffffffffu, ok);
           if (!ok) break;
-          const uint8_t *rowp = stg + row * 128;
+          const uint8_t *rowp = stg + lane * 128;
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
-            const float4 cv =
-                *reinterpret_cast<const float4 *>(rowp + ((i ^ (row & 7)) << 4));
+            const float4 cv = *reinterpret_cast<const float4 *>(rowp + ((i ^ (lane & 7)) << 4));
             v[4 * i + 0] += cv.x;
             v[4 * i + 1] += cv.y;
             v[4 * i + 2] += cv.z;
@@ -615,7 +581,9 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
           }
         }
         if constexpr (kOut == OUT_BF16) {
-          uint8_t *rowp = stg + row * 64;
+          // 64-byte rows, 64-byte swizzle: 16-byte chunk i of row l sits at
+          // chunk i ^ ((l >> 1) & 3).
+          uint8_t *rowp = stg + lane * 64;
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             uint32_t w[4];
@@ -625,42 +593,42 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
                   __floats2bfloat162_rn(v[8 * i + 2 * h], v[8 * i + 2 * h + 1]);
               w[h] = *reinterpret_cast<const uint32_t *>(&pr);
             }
-            *reinterpret_cast<uint4 *>(rowp + ((i ^ ((row >> 1) & 3)) << 4)) =
+            *reinterpret_cast<uint4 *>(rowp + ((i ^ ((lane >> 1) & 3)) << 4)) =
                 make_uint4(w[0], w[1], w[2], w[3]);
           }
         } else {
-          uint8_t *rowp = stg + row * 128;
+          // 128-byte rows, 128-byte swizzle: chunk i of row l at i ^ (l & 7).
+          uint8_t *rowp = stg + lane * 128;
 #pragma unroll
           for (int i = 0; i < 8; ++i)
-            *reinterpret_cast<float4 *>(rowp + ((i ^ (row & 7)) << 4)) =
+            *reinterpret_cast<float4 *>(rowp + ((i ^ (lane & 7)) << 4)) =
                 make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
         }
         fence_proxy_async_smem();
-        DG_T0(w2);
-        named_bar_sync(1, 128);
-        DG_TACC(3, w2);
-        if (etid == 0) {
+        __syncwarp();
+        if (lane == 0) {
           if constexpr (kOut == OUT_F32_REDUCE)
-            tma_reduce_add_3d_hint(&p.tmD, stg, tc.n0 + 32 * c, tc.m0, tc.expert, stream_out);
+            tma_reduce_add_3d_hint(&p.tmD, stg, tc.n0 + 32 * c, row0, tc.expert, stream_out);
           else
-            tma_store_3d_hint(&p.tmD, stg, tc.n0 + 32 * c, tc.m0, tc.expert, stream_out);
+            tma_store_3d_hint(&p.tmD, stg, tc.n0 + 32 * c, row0, tc.expert, stream_out);
           bulk_commit();
         }
       }
       if (!ok) break;
       if (mma_tile) ++tl;
     }
-    if (etid == 0) bulk_wait<0>();
+    if (lane == 0) bulk_wait<0>();
   }
 
 #ifdef DG_KERNEL_TIMERS
   // Per CTA 32 counters, 8 per role (producer, MMA, warp 6, epilogue warp 2):
-  // the role's wait counters tm[0..3], then its total cycles.
+  // the role's counters tm[0..3], its total cycles, then tm[4..6].
   if (lane == 0 && p.timers != nullptr && (warp <= 2 || warp == 6)) {
     const int role = warp == 0 ? 0 : warp == 1 ? 1 : warp == 6 ? 2 : 3;
     unsigned long long *o = p.timers + blockIdx.x * 32 + role * 8;
     for (int i = 0; i < 4; ++i) o[i] = tm[i];
     o[4] = clock64() - t_start;
+    for (int i = 4; i < 7; ++i) o[i + 1] = tm[i];
   }
 #endif
 

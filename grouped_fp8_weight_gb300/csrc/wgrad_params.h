@@ -18,7 +18,7 @@ struct SchedEntry {
   int expert;
   int k_off;
   int k_len;
-  int pad;
+  int g_off;   // FP8: first packed scale group of this entry
 };
 
 enum OutMode : int {
@@ -31,8 +31,8 @@ enum OutMode : int {
 struct WgradParams {
   CUtensorMap tmA;     // operand A [sum_k, M], 128-byte swizzled tiles
   CUtensorMap tmB;     // operand B [sum_k, N], 128-byte swizzled tiles
-  CUtensorMap tmSFA;   // UE8M0 [sum_k / gran_k, M]   (FP8 only)
-  CUtensorMap tmSFB;   // UE8M0 [sum_k / gran_k, N]   (FP8 only)
+  CUtensorMap tmSFA;   // FP8: packed scale records of A, 512 bytes each (see PackParams)
+  CUtensorMap tmSFB;   // FP8: packed scale records of B, CB x 512 bytes per box
   CUtensorMap tmD;     // output [G, M, N] as 3-D {N, M, G}
   CUtensorMap tmC;     // separate accumulator, same shape (OUT_F32_C only)
   int M, N, G;
@@ -42,6 +42,7 @@ struct WgradParams {
   int gran_k;          // 32 or 128 (FP8)
   int out_mode;
   int m_fastest;       // tile order inside an expert: 1 = M tiles vary fastest
+  int sf_mc;           // FP8: packed A records per scale group (2 * m_tiles)
   uint64_t wait_limit_ns;
   DevStatus *status;
   const int *ks_dev;
@@ -50,6 +51,29 @@ struct WgradParams {
 #endif
   SchedEntry sched[kMaxGroups];
 };
+
+// FP8 scale packing (scale_pack.cu): every scale group the GEMM uses, laid
+// out as the 32-row x 16-byte records tcgen05.cp copies into tensor memory.
+// Group j of schedule entry s (K_e > 0) is record group g_off[s] + j; it covers
+// scale rows row_off[s] + 4j .. + 3, and rows at or past row_end[s] read as 0.
+struct PackParams {
+  const uint8_t *sfa, *sfb;   // [sum_k / gran_k, M] and [sum_k / gran_k, N]
+  uint32_t *sfa_p;            // [n_groups][MC][128 words]
+  uint32_t *sfb_p;            // [n_groups][NT][CB][128 words]
+  int M, N, MC, NT, CB, BN;
+  int n_entries, n_groups;
+  int g_off[kMaxGroups];
+  int row_off[kMaxGroups];
+  int row_end[kMaxGroups];
+};
+
+// Fills pk's plan (and p.sched[i].g_off, p.sf_mc) from the first n_mma
+// schedule entries of p for block width bn; returns the scratch bytes the
+// packed records need (0 when there is no GEMM work).
+size_t plan_scale_pack(WgradParams &p, PackParams &pk, int n_mma, int gran_k, int bn);
+// Points pk at `scratch` (16-byte aligned, plan_scale_pack's size).
+void bind_scale_pack(PackParams &pk, void *scratch, const uint8_t *sfa, const uint8_t *sfb);
+cudaError_t launch_pack_scales(const PackParams &p, cudaStream_t stream);
 
 // Launchers (one translation unit each): `pairs` clusters of two CTAs (capped
 // at the number that fit the GPU at once).  Return the launch error, if any.
