@@ -243,6 +243,7 @@ dg_status run_grouped(const GroupedArgs &x) {
   p.num_mma_tiles = n_mma * p.tiles_per_group;
   p.num_tiles = n_groups * p.tiles_per_group;
   p.gran_k = x.fp8 ? x.gran_k : 0;
+  p.chunk = x.fp8 ? dg::kFp8Chunk : dg::kBf16Chunk;
   // Sweep the smaller operand's tiles fastest: the concurrently running tiles
   // then share the larger operand's slices, and the smaller one stays in L2
   // from one sweep to the next.

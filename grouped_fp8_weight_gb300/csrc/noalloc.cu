@@ -229,6 +229,7 @@ extern "C" dg_status dg_k_grouped_fp8_wgrad_noalloc(
   p.num_mma_tiles = n_mma * p.tiles_per_group;
   p.num_tiles = order_len * p.tiles_per_group;
   p.gran_k = gran_k;
+  p.chunk = dg::kFp8Chunk;
   p.m_fastest = (M <= N) ? 1 : 0;
   p.out_mode = (d_dtype == DG_BF16) ? dg::OUT_BF16
                : (c == nullptr)     ? dg::OUT_F32

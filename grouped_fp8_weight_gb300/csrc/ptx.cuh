@@ -95,9 +95,17 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
   return r;
 }
 // Arrive on an mbarrier given by its cluster address (possibly in the peer CTA).
+// Release at cluster scope: orders all of this thread's prior memory accesses
+// before the arrive, cluster-wide -- on sm_103a this costs thousands of cycles.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
                : "memory");
+}
+// Arrive on an mbarrier given by its cluster address with the default
+// (release, CTA-scope) semantics: enough where what the arrive announces is
+// already complete, e.g. tensor-memory reads the thread has waited for.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 // 16-byte store into shared memory given by its cluster address (possibly
 // in the peer CTA).

@@ -10,11 +10,12 @@
 // MMA thread issues every MMA for both; the operands of one stage are thus
 // loaded once per pair, halving each SM's B traffic.
 //
-// Pairs walk the tile list (expert, 256-row M tile, BN-column N tile) with a
-// stride of the number of pairs.  The host sorts experts longest-first; the
-// list is dealt in rounds taken alternately from its head (long, MMA-heavy
-// tiles) and its tail (short, store-heavy tiles), so a pair alternates the two
-// kinds and the epilogue of one overlaps the MMAs of the next.
+// Pairs own every R-th tile of the list (expert, 256-row M tile, BN-column N
+// tile), which the host sorts longest expert first.  A pair's two tensor-memory
+// accumulators serve as two lanes: lane 0 takes its tiles from the head of its
+// list, lane 1 from the tail, and the MMA stream alternates `chunk` stages of
+// lane 0's (long) tile with the whole of lane 1's (short) tile, so the
+// epilogue drains short tiles while a long one accumulates.
 //
 // Roles per CTA (224 threads):
 //   warp 0      TMA producer (one thread): A/B stages of 128 (FP8) or 64
@@ -32,8 +33,8 @@
 //               layout tcgen05.cp copies into tensor memory) up to five groups
 //               ahead.  BF16 (even CTA): stage gate -- zeroes the token rows
 //               past an expert's slice in both CTAs' last stage.
-// Two accumulators live in tensor memory, so the epilogue of one tile overlaps
-// the MMAs of the next.
+// Two accumulators live in tensor memory (the two lanes), so the epilogue of
+// one tile overlaps the MMAs of others.
 //
 // Operands are MN-major (the token axis is K and is the slow axis in memory):
 // an operand tile for one stage is BK token rows x 128-byte swizzle atoms.
@@ -123,14 +124,6 @@ __device__ __forceinline__ bool epi_all(bool ok) {
   return r != 0;
 }
 
-// Position t of a pair's walk -> index into the longest-first tile list:
-// rounds of R tiles alternate between the head and the tail of the list.
-__device__ __forceinline__ int interleaved_tile(int t, int n, int R) {
-  const int r = t / R;
-  const int q = (r >> 1) * R + (t - r * R);
-  return (r & 1) ? n - 1 - q : q;
-}
-
 struct TileCoord {
   int expert, k_off, k_len, m0, n0;   // m0: this CTA's first row; n0: the pair's first column
   int nt, g_off;                      // N-tile index; first packed scale group of the expert
@@ -147,33 +140,73 @@ __device__ __forceinline__ TileCoord tile_coord(const WgradParams &p, int u, int
                    nt * bn, nt, se.g_off};
 }
 
-// Walks the FP8 scale groups of a pair's tiles in order: a group is gs
-// consecutive k-blocks of one tile.
-struct GroupCursor {
-  int t, j, nk;
-  TileCoord tc;
+// ---------------------------------------------------------------- schedule
+// A pair owns the tiles u = pid + i * R (i = 0, 1, ...) of the longest-first
+// tile list.  Its two accumulator buffers work as two lanes: lane 0 takes
+// tiles from the head of its list (long, MMA-heavy) and lane 1 from the tail
+// (short or output-only, store-heavy).  The MMA stream alternates between the
+// lanes: `chunk` stages of lane 0's tile, then all of lane 1's tile, and so
+// on, so that while a long tile accumulates the epilogue drains a stream of
+// short ones.  Every role walks the same sequence of chunks.
+struct Chunk {
+  int u;        // tile
+  int j0, j1;   // its stages [j0, j1) (BK tokens each)
+  int nk;       // stages of the whole tile; 0 = output-only tile
+  int lane;     // accumulator buffer
 };
 
-__device__ __forceinline__ void group_cursor_init(GroupCursor &c, int pid, int R) {
-  c.t = pid - R;
-  c.j = 0;
-  c.nk = 0;
+struct LaneSched {
+  int head, tail;   // list positions not yet taken: [head, tail]
+  int u0, nk0, j0;  // lane 0: tile (-1: none), its stages, next stage
+  int u1, nk1, j1;  // lane 1
+  int turn;
+};
+
+__device__ __forceinline__ void lane_init(LaneSched &L, const WgradParams &p, int pid, int R) {
+  L.head = 0;
+  L.tail = (p.num_tiles - pid + R - 1) / R - 1;
+  L.u0 = L.u1 = -1;
+  L.nk0 = L.nk1 = L.j0 = L.j1 = 0;
+  L.turn = 0;
 }
 
-__device__ __forceinline__ bool group_cursor_next(GroupCursor &c, const WgradParams &p, int gs,
-                                                  int bn, int R, uint32_t rank) {
-  c.j += gs;
-  while (c.j >= c.nk) {
-    c.t += R;
-    if (c.t >= p.num_tiles) return false;
-    const int u = interleaved_tile(c.t, p.num_tiles, R);
-    c.j = 0;
-    c.nk = 0;
-    if (u >= p.num_mma_tiles) continue;
-    c.tc = tile_coord(p, u, bn, rank);
-    c.nk = c.tc.k_len / 128;
+// One lane's turn: a chunk of its current tile, taking the next tile from its
+// end of the list first if it has none.  Returns false if the lane has no
+// tile and the list is used up.
+__device__ __forceinline__ bool lane_turn(LaneSched &L, const WgradParams &p, int pid, int R,
+                                          int bk, int l, int &u, int &nk, int &j, Chunk &c) {
+  if (u < 0) {
+    if (L.head > L.tail) return false;
+    const int i = (l == 0) ? L.head++ : L.tail--;
+    u = pid + i * R;
+    nk = (u < p.num_mma_tiles) ? (p.sched[u / p.tiles_per_group].k_len + bk - 1) / bk : 0;
+    j = 0;
+    if (nk == 0) {   // output-only tile: a completion without MMAs
+      c = Chunk{u, 0, 0, 0, l};
+      u = -1;
+      return true;
+    }
   }
+  const int rem = nk - j;
+  const int len = (l == 0) ? min(p.chunk, rem) : rem;
+  c = Chunk{u, j, j + len, nk, l};
+  j += len;
+  if (j == nk) u = -1;
   return true;
+}
+
+__device__ __forceinline__ bool lane_next(LaneSched &L, const WgradParams &p, int pid, int R,
+                                          int bk, Chunk &c) {
+  const int first = L.turn;
+  L.turn ^= 1;
+  if (first == 0) {
+    if (lane_turn(L, p, pid, R, bk, 0, L.u0, L.nk0, L.j0, c)) return true;
+    L.turn = 0;
+    return lane_turn(L, p, pid, R, bk, 1, L.u1, L.nk1, L.j1, c);
+  }
+  if (lane_turn(L, p, pid, R, bk, 1, L.u1, L.nk1, L.j1, c)) return true;
+  L.turn = 1;
+  return lane_turn(L, p, pid, R, bk, 0, L.u0, L.nk0, L.j0, c);
 }
 
 #ifdef DG_KERNEL_TIMERS
@@ -260,16 +293,18 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
       int s = 0;
       uint32_t ph = 0, armed = 0;
       bool ok = true;
-      for (int t = pid; ok && t < p.num_tiles; t += R) {
-        const int u = interleaved_tile(t, p.num_tiles, R);
-        if (u >= p.num_mma_tiles) continue;
-        const TileCoord tc = tile_coord(p, u, kBN, rank);
-        if (leader && p.ks_dev != nullptr && tc.m0 == 0 && tc.n0 == 0 &&
+      LaneSched L;
+      lane_init(L, p, pid, R);
+      Chunk ch;
+      while (ok && lane_next(L, p, pid, R, Cfg::BK, ch)) {
+        if (ch.nk == 0) continue;
+        const TileCoord tc = tile_coord(p, ch.u, kBN, rank);
+        const int t = ch.u;
+        if (leader && ch.j0 == 0 && p.ks_dev != nullptr && tc.m0 == 0 && tc.n0 == 0 &&
             p.ks_dev[tc.expert] != tc.k_len)
           atomicCAS(&p.status->code, DEV_OK, DEV_KS_MISMATCH);
-        const int nk = (tc.k_len + Cfg::BK - 1) / Cfg::BK;
         const int nb = tc.n0 + static_cast<int>(rank) * Cfg::BN_CTA;   // this CTA's B columns
-        for (int j = 0; j < nk; ++j) {
+        for (int j = ch.j0; j < ch.j1; ++j) {
           const int k = tc.k_off + j * Cfg::BK;
           DG_T0(w1);
           ok = mbar_wait(&empty[s], ph ^ 1, abort_flag, lim, p.status, W_PROD_EMPTY, t);
@@ -306,7 +341,7 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
     // One thread; per stage only constant-offset descriptor updates and the
     // four MMAs, so that issue keeps ahead of the tensor pipe.
     if (lane == 0 && leader) {
-      int s = 0, g = 0, tl = 0;
+      int s = 0, g = 0;
       uint32_t ph = 0, gph = 0, it = 0;
       uint32_t sfa_t = 0, sfb_t = 0;
       bool ok = true;
@@ -320,27 +355,26 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
       const uint64_t uta_desc0 = smem_desc(smem_u32(smem + Cfg::OFF_UTA), 0, 128, 0);
       const uint64_t utb_desc0 = smem_desc(smem_u32(smem + Cfg::OFF_UTB), 0, 128, 0);
       uint64_t a_desc = a_desc0, b_desc = b_desc0;
-      int q = pid;   // position of this pair's tile within the current head/tail round
-      for (int i = 0; ok; ++i) {
-        const int t = pid + i * R;
-        if (t >= p.num_tiles) break;
-        const int u = (i & 1) ? p.num_tiles - 1 - q : q;
-        if (i & 1) q += R;
-        if (u >= p.num_mma_tiles) continue;
-        const int k_len = p.sched[u / p.tiles_per_group].k_len;
-        const int nk = (k_len + Cfg::BK - 1) / Cfg::BK;
-        const int b = tl & 1;
-        DG_T0(w0);
-        ok = mbar_wait(&acce[b], ((tl >> 1) & 1) ^ 1, abort_flag, lim, p.status, W_MMA_ACCE, t);
-        DG_TACC(1, w0);
-        if (!ok) break;
-        tc_fence_after();
+      uint32_t uses[2] = {0, 0};   // tiles completed per accumulator buffer
+      LaneSched L;
+      lane_init(L, p, pid, R);
+      Chunk ch;
+      while (ok && lane_next(L, p, pid, R, Cfg::BK, ch)) {
+        if (ch.nk == 0) continue;
+        const int t = ch.u;
+        const int b = ch.lane;
+        if (ch.j0 == 0) {
+          // the buffer's previous tile has been drained by both epilogues
+          DG_T0(w0);
+          ok = mbar_wait(&acce[b], (uses[b] & 1) ^ 1, abort_flag, lim, p.status, W_MMA_ACCE, t);
+          DG_TACC(1, w0);
+          if (!ok) break;
+          tc_fence_after();
+        }
         const uint32_t d_tmem = tmem_base + b * kBN;
-        int jg = 0;   // k-blocks left in the current scale group
-        for (int j = 0; j < nk; ++j) {
+        for (int j = ch.j0; j < ch.j1; ++j) {
           if constexpr (kFP8) {
-            if (jg == 0) {
-              jg = gs;
+            if (j % gs == 0) {
               DG_T0(w1);
               ok = mbar_wait(&sfr[g], gph, abort_flag, lim, p.status, W_MMA_SFR, t);
               DG_TACC(2, w1);
@@ -357,7 +391,6 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
               mma_commit_pair(&sfe[g], 0x3);
               if (++g == NS) { g = 0; gph ^= 1; }
             }
-            --jg;
           }
           DG_T0(w2);
           // Keep at most two stages queued in the tensor pipe: sleep on the
@@ -402,8 +435,10 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
           }
         }
         if (!ok) break;
-        mma_commit_pair(&accf[b], 0x3);
-        ++tl;
+        if (ch.j1 == ch.nk) {
+          mma_commit_pair(&accf[b], 0x3);
+          ++uses[b];
+        }
       }
       // Drain: every tcgen05 op issued here completes before tensor memory
       // is released.
@@ -421,13 +456,15 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
         int s = 0;
         uint32_t ph = 0;
         bool ok = true;
-        for (int t = pid; ok && t < p.num_tiles; t += R) {
-          const int u = interleaved_tile(t, p.num_tiles, R);
-          if (u >= p.num_mma_tiles) continue;
-          const int k_len = p.sched[u / p.tiles_per_group].k_len;
-          const int nk = (k_len + Cfg::BK - 1) / Cfg::BK;
-          const int tail = k_len - (nk - 1) * Cfg::BK;
-          for (int j = 0; j < nk; ++j) {
+        LaneSched L;
+        lane_init(L, p, pid, R);
+        Chunk ch;
+        while (ok && lane_next(L, p, pid, R, Cfg::BK, ch)) {
+          if (ch.nk == 0) continue;
+          const int t = ch.u;
+          const int nk = ch.nk;
+          const int tail = p.sched[ch.u / p.tiles_per_group].k_len - (nk - 1) * Cfg::BK;
+          for (int j = ch.j0; j < ch.j1; ++j) {
             ok = mbar_wait(&full[s], ph, abort_flag, lim, p.status, W_SF_FULL, t);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
@@ -468,26 +505,39 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
         prefetch_tmap(&p.tmSFB);
         const uint64_t keep = l2_policy_evict_last();   // B's records serve every M tile
         const uint32_t sfr_leader = mapa_shared(smem_u32(&sfr[0]), 0);
-        GroupCursor ic;
-        group_cursor_init(ic, pid, R);
-        bool have = group_cursor_next(ic, p, gs, kBN, R, rank);
+        LaneSched L;
+        lane_init(L, p, pid, R);
+        Chunk ch;
+        TileCoord tc{};
+        int j = 0;          // next k-block of the current chunk
+        bool have = false;  // a chunk with k-blocks left is current
         uint32_t ig = 0;
         bool ok = true;
-        while (ok && have) {
+        while (ok) {
+          // next scale group: a k-block j with j % gs == 0 (chunks start on
+          // group boundaries)
+          while (!have || j >= ch.j1) {
+            have = lane_next(L, p, pid, R, Cfg::BK, ch);
+            if (!have) break;
+            if (ch.nk == 0) { have = false; continue; }
+            tc = tile_coord(p, ch.u, kBN, rank);
+            j = ch.j0;
+          }
+          if (!have) break;
           const int g = ig % NS;
           DG_T0(w0);
           ok = mbar_wait(&sfe[g], ((ig / NS) & 1) ^ 1, abort_flag, lim, p.status, W_PROD_SFE,
-                         ic.t);
+                         ch.u);
           DG_TACC(2, w0);
           if (!ok) break;
           if (leader) mbar_arrive_expect_tx(&sfr[g], 2 * (Cfg::UT_A + Cfg::UT_B));
-          const int grp = ic.tc.g_off + ic.j / gs;
+          const int grp = tc.g_off + j / gs;
           tma_load_2d_pair(smem + Cfg::OFF_UTA + g * Cfg::UT_A, &p.tmSFA, sfr_leader + 8 * g, 0,
-                           grp * p.sf_mc + ic.tc.m0 / 128, keep);
+                           grp * p.sf_mc + tc.m0 / 128, keep);
           tma_load_2d_pair(smem + Cfg::OFF_UTB + g * Cfg::UT_B, &p.tmSFB, sfr_leader + 8 * g, 0,
-                           (grp * p.n_tiles + ic.tc.nt) * Cfg::SF_CHUNKS_B, keep);
+                           (grp * p.n_tiles + tc.nt) * Cfg::SF_CHUNKS_B, keep);
           ++ig;
-          have = group_cursor_next(ic, p, gs, kBN, R, rank);
+          j += gs;
         }
         // Let every record this CTA requested land before the pair can exit:
         // the even CTA sees them on `sfr`; its partner sees the slots' copies
@@ -509,7 +559,7 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
     // another: tcgen05.ld of 32 columns -> one of its two 4 KB swizzled
     // staging buffers -> TMA store (or reduce-add) of that 32 x 32 box.
     const int q = warp & 3;               // tensor-memory lane quadrant of this warp
-    uint32_t tl = 0, nchunk = 0;
+    uint32_t uses[2] = {0, 0}, nchunk = 0;
     uint32_t cuse[2] = {0, 0};
     constexpr bool kHasC = (kOut == OUT_F32_C);
     const uint64_t stream_out = l2_policy_evict_first();   // D is written once
@@ -517,14 +567,18 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
     uint8_t *wstg = smem + Cfg::OFF_STG + q * 2 * Cfg::WSTG_BYTES;
     uint64_t *wcbar = cbar + 2 * q;
     uint32_t r[32];   // tensor-memory chunk in flight
-    for (int t = pid; t < p.num_tiles; t += R) {
-      const int u = interleaved_tile(t, p.num_tiles, R);
-      const TileCoord tc = tile_coord(p, u, kBN, rank);
-      const bool mma_tile = u < p.num_mma_tiles;
-      const int b = tl & 1;
+    LaneSched L;
+    lane_init(L, p, pid, R);
+    Chunk ch;
+    while (lane_next(L, p, pid, R, Cfg::BK, ch)) {
+      if (ch.nk > 0 && ch.j1 != ch.nk) continue;   // only tile completions
+      const int t = ch.u;
+      const TileCoord tc = tile_coord(p, ch.u, kBN, rank);
+      const bool mma_tile = ch.nk > 0;
+      const int b = ch.lane;
       if (mma_tile) {
         DG_T0(w0);
-        bool got = mbar_wait(&accf[b], (tl >> 1) & 1, abort_flag, lim, p.status, W_EPI_ACCF, t);
+        bool got = mbar_wait(&accf[b], uses[b] & 1, abort_flag, lim, p.status, W_EPI_ACCF, t);
         DG_TACC(1, w0);
         if (!__all_sync(0xffffffffu, got)) break;
         tc_fence_after();
@@ -557,9 +611,12 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
           if (c + 1 < nch) {
             tmem_ld_32x32b_x32(tmem_row + 32 * (c + 1), r);
           } else {
+            // Every read of this buffer has completed (tcgen05.wait::ld above);
+            // the tcgen05 fence orders them before the release, so a CTA-scope
+            // arrive suffices (a cluster-scope release costs thousands of cycles).
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(acce_leader + 8 * b);
+            if (lane == 0) mbar_arrive_remote(acce_leader + 8 * b);
           }
         } else {
 #pragma unroll
@@ -615,7 +672,7 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
         }
       }
       if (!ok) break;
-      if (mma_tile) ++tl;
+      if (mma_tile) ++uses[b];
     }
     if (lane == 0) bulk_wait<0>();
   }

@@ -43,6 +43,7 @@ struct WgradParams {
   int out_mode;
   int m_fastest;       // tile order inside an expert: 1 = M tiles vary fastest
   int sf_mc;           // FP8: packed A records per scale group (2 * m_tiles)
+  int chunk;           // stages of a lane-0 tile per turn (FP8: a multiple of 4)
   uint64_t wait_limit_ns;
   DevStatus *status;
   const int *ks_dev;
@@ -87,6 +88,10 @@ cudaError_t launch_quant_colblock(const void *x, int64_t T, int C, void *q, uint
 // Tile shape: a CTA pair covers 256 rows of M (128 per CTA) and block_n
 // columns of N.
 constexpr int kPairM = 256;
+// Stages of a long tile issued per turn before the MMA stream switches to the
+// other accumulator's tile (FP8 stages are 128 tokens, BF16 64).
+constexpr int kFp8Chunk = 12;
+constexpr int kBf16Chunk = 24;
 int fp8_pick_block_n(int N);
 int bf16_pick_block_n(int N);
 
