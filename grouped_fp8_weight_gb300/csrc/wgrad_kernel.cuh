@@ -84,6 +84,7 @@ struct WgradCfg {
   static constexpr int SF_COLS = 4 + 4 * SF_CHUNKS_B;   // tensor-memory columns per slot
   static constexpr int SF_COL0 = NUM_ACC * kBN;
   static constexpr int WSTG_BYTES = 4096;               // per epilogue warp and buffer: 32 rows x 128 bytes
+  static constexpr int EPI_BUFS = 2;                    // staging buffers per epilogue warp
   static constexpr int TMEM_COLS = 512;
   static_assert(SF_COL0 + SF_SLOTS * SF_COLS <= TMEM_COLS, "tmem budget");
   static_assert(kBN % 32 == 0 && kBN <= 256, "block N");
@@ -91,7 +92,7 @@ struct WgradCfg {
   static constexpr int OFF_B = 0;
   static constexpr int OFF_A = OFF_B + STAGES * B_BYTES;
   static constexpr int OFF_STG = OFF_A + STAGES * A_BYTES;
-  static constexpr int OFF_UTA = OFF_STG + 4 * 2 * WSTG_BYTES;
+  static constexpr int OFF_UTA = OFF_STG + 4 * EPI_BUFS * WSTG_BYTES;
   static constexpr int OFF_UTB = OFF_UTA + SF_SLOTS * UT_A;
   static constexpr int OFF_BAR = (OFF_UTB + SF_SLOTS * UT_B + 7) / 8 * 8;
   // barriers: full[S], empty[S], gate[S], accf[2], acce[2], cbar[4 warps x 2],
@@ -342,7 +343,7 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
     // four MMAs, so that issue keeps ahead of the tensor pipe.
     if (lane == 0 && leader) {
       int s = 0, g = 0;
-      uint32_t ph = 0, gph = 0, it = 0;
+      uint32_t ph = 0, gph = 0;
       uint32_t sfa_t = 0, sfb_t = 0;
       bool ok = true;
       constexpr uint32_t kIdescBase =
@@ -393,15 +394,6 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
             }
           }
           DG_T0(w2);
-          // Keep at most two stages queued in the tensor pipe: sleep on the
-          // completion of stage it-2 rather than stall in tcgen05.mma issue
-          // (a stalled issue also holds back the epilogue warp that shares
-          // this warp's scheduler).
-          if (it >= 2) {
-            const uint32_t pit = it - 2;
-            ok = mbar_wait(&empty[pit % S], (pit / S) & 1, abort_flag, lim, p.status, W_MMA_FULL, t);
-            if (!ok) break;
-          }
           // FP8 stages are complete once both CTAs' bytes land; BF16 stages
           // once warp 6 has also masked an expert's tail rows.
           ok = mbar_wait(kFP8 ? &full[s] : &gate[s], ph, abort_flag, lim, p.status, W_MMA_FULL, t);
@@ -423,7 +415,6 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
             }
           }
           mma_commit_pair(&empty[s], 0x3);
-          ++it;
           if (++s == S) {
             s = 0;
             ph ^= 1;
@@ -556,7 +547,7 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
     // ------------------------------------------------------------ epilogue
     // Each warp owns one tensor-memory lane quadrant (32 rows of this CTA's
     // 128) and runs its own pipeline, so the four warps never wait on one
-    // another: tcgen05.ld of 32 columns -> one of its two 4 KB swizzled
+    // another: tcgen05.ld of 32 columns -> one of its EPI_BUFS 4 KB swizzled
     // staging buffers -> TMA store (or reduce-add) of that 32 x 32 box.
     const int q = warp & 3;               // tensor-memory lane quadrant of this warp
     uint32_t uses[2] = {0, 0}, nchunk = 0;
@@ -564,7 +555,7 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
     constexpr bool kHasC = (kOut == OUT_F32_C);
     const uint64_t stream_out = l2_policy_evict_first();   // D is written once
     const uint32_t acce_leader = mapa_shared(smem_u32(&acce[0]), 0);
-    uint8_t *wstg = smem + Cfg::OFF_STG + q * 2 * Cfg::WSTG_BYTES;
+    uint8_t *wstg = smem + Cfg::OFF_STG + q * Cfg::EPI_BUFS * Cfg::WSTG_BYTES;
     uint64_t *wcbar = cbar + 2 * q;
     uint32_t r[32];   // tensor-memory chunk in flight
     LaneSched L;
@@ -590,10 +581,10 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
       if (mma_tile) tmem_ld_32x32b_x32(tmem_row, r);
       bool ok = true;
       for (int c = 0; c < nch; ++c, ++nchunk) {
-        const int sbuf = nchunk & 1;
+        const int sbuf = static_cast<int>(nchunk % Cfg::EPI_BUFS);
         uint8_t *stg = wstg + sbuf * Cfg::WSTG_BYTES;
         DG_T0(w1);
-        if (lane == 0) bulk_wait_read<1>();    // the store that last used stg is done reading
+        if (lane == 0) bulk_wait_read<Cfg::EPI_BUFS - 1>();   // the store that last used stg is done reading
         __syncwarp();
         DG_TACC(2, w1);
         if (kHasC && lane == 0) {
