@@ -271,10 +271,12 @@ dg_status run_grouped(const GroupedArgs &x) {
       const uint64_t da[2] = {M, SK}, sa[1] = {M};
       const uint64_t db[2] = {N, SK}, sb[1] = {N};
       const uint32_t box[2] = {128, 128};
+      // B: one box per CTA covers its bn / 2 columns (<= one 128-byte atom)
+      const uint32_t boxb[2] = {static_cast<uint32_t>(std::min(128, bn / 2)), 128};
       if ((s = encode(&p.tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, x.a, 2, da, sa, box,
                       CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "a")))
         return s;
-      s = encode(&p.tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, x.b, 2, db, sb, box,
+      s = encode(&p.tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, x.b, 2, db, sb, boxb,
                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "b");
       if (s) return s;
       // The packed scale records are mapped (and the scratch taken) below,
@@ -283,9 +285,10 @@ dg_status run_grouped(const GroupedArgs &x) {
       const uint64_t da[2] = {M, SK}, sa[1] = {2 * M};
       const uint64_t db[2] = {N, SK}, sb[1] = {2 * N};
       const uint32_t box[2] = {64, 64};
+      const uint32_t boxb[2] = {static_cast<uint32_t>(std::min(64, bn / 2)), 64};
       if ((s = encode(&p.tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x.a, 2, da, sa, box,
                       CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "a")) ||
-          (s = encode(&p.tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x.b, 2, db, sb, box,
+          (s = encode(&p.tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x.b, 2, db, sb, boxb,
                       CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "b")))
         return s;
     }
@@ -294,15 +297,15 @@ dg_status run_grouped(const GroupedArgs &x) {
     const bool bf = (x.d_dtype == DG_BF16);
     const uint64_t es = bf ? 2 : 4;
     const uint64_t dd[3] = {N, M, G}, sd[2] = {es * N, es * N * M};
-    const uint32_t box[3] = {32, 32, 1};
+    const uint32_t box[3] = {dg::kEpiCols, 32, 1};
     if ((s = encode(&p.tmD,
                     bf ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, x.d,
-                    3, dd, sd, box, bf ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
+                    3, dd, sd, box, dg::epi_swizzle(bf ? 2 : 4),
                     CU_TENSOR_MAP_L2_PROMOTION_NONE, "d")))
       return s;
     if (p.out_mode == dg::OUT_F32_C &&
         (s = encode(&p.tmC, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, x.c, 3, dd, sd, box,
-                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE, "c")))
+                    dg::epi_swizzle(4), CU_TENSOR_MAP_L2_PROMOTION_NONE, "c")))
       return s;
   }
 

@@ -134,11 +134,10 @@ dg_status map_out(CUtensorMap *m, bool bf16, const void *ptr, uint64_t M, uint64
                   uint64_t G, const char *what) {
   const uint64_t es = bf16 ? 2 : 4;
   const cuuint64_t dims[3] = {N, M, G}, strides[2] = {es * N, es * N * M};
-  const cuuint32_t box[3] = {32, 32, 1}, ones[3] = {1, 1, 1};
+  const cuuint32_t box[3] = {dg::kEpiCols, 32, 1}, ones[3] = {1, 1, 1};
   CUresult r = n_encode(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
                         3, const_cast<void *>(ptr), dims, strides, box, ones,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        bf16 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, dg::epi_swizzle(bf16 ? 2 : 4),
                         CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return nfail(DG_ERR_CUDA, "tensor map for %s failed (%d)", what, (int)r);
   return DG_OK;
@@ -261,7 +260,8 @@ extern "C" dg_status dg_k_grouped_fp8_wgrad_noalloc(
     const uint64_t groups = static_cast<uint64_t>(pk.n_groups);
     if ((s = map2d(&p.tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, a, M, SK, M, 128, 128,
                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "a")) ||
-        (s = map2d(&p.tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, b, N, SK, N, 128, 128,
+        (s = map2d(&p.tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, b, N, SK, N,
+                   static_cast<uint32_t>(std::min(128, bn / 2)), 128,
                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "b")) ||
         (s = map2d(&p.tmSFA, CU_TENSOR_MAP_DATA_TYPE_UINT32, pk.sfa_p, 128, groups * pk.MC, 512,
                    128, 1, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,

@@ -27,7 +27,7 @@
 //   warps 2..5  epilogue, one warp per tensor-memory lane quadrant (32 rows),
 //               each on its own: tensor memory -> registers -> swizzled
 //               shared-memory staging -> TMA store (or TMA reduce-add for
-//               in-place D += acc) of 32 x 32 boxes.
+//               in-place D += acc) of 32-row x kEpiCols boxes.
 //   warp 6      FP8: scale loader -- fetches each scale group's packed
 //               records (written beforehand by the scale pack pass in the
 //               layout tcgen05.cp copies into tensor memory) up to five groups
@@ -63,6 +63,11 @@ struct WgradCfg {
   static constexpr int ATOM_BYTES = BK * 128;           // BK rows x 128 bytes
   static constexpr int A_BYTES = A_ATOMS * ATOM_BYTES;
   static constexpr int B_BYTES = B_ATOMS * ATOM_BYTES;
+  // Bytes a stage's B loads bring in: each box is min(ATOM, BN_CTA) columns
+  // wide, so a CTA's 112-column half of a 224-wide tile is loaded exactly
+  // (its 128-byte swizzled rows keep their 128-byte pitch in shared memory).
+  static constexpr int B_BOX_COLS = BN_CTA < ATOM ? BN_CTA : ATOM;
+  static constexpr int B_LOAD_BYTES = B_ATOMS * BK * B_BOX_COLS * ELEM;
   static constexpr int KSTEP_BYTES = MMA_K * 128;
   // Descriptor strides: SBO = 1024 (8 token rows x 128 B) between K groups,
   // LBO = ATOM_BYTES between 128-byte atoms along M/N.  A single-atom operand
@@ -83,7 +88,8 @@ struct WgradCfg {
   static constexpr int UT_B = 512 * SF_CHUNKS_B;
   static constexpr int SF_COLS = 4 + 4 * SF_CHUNKS_B;   // tensor-memory columns per slot
   static constexpr int SF_COL0 = NUM_ACC * kBN;
-  static constexpr int WSTG_BYTES = 4096;               // per epilogue warp and buffer: 32 rows x 128 bytes
+  static constexpr int EC = kEpiCols;                   // output columns per epilogue chunk
+  static constexpr int WSTG_BYTES = 32 * EC * 4;        // per epilogue warp and buffer: 32 FP32 rows
   static constexpr int EPI_BUFS = 2;                    // staging buffers per epilogue warp
   static constexpr int TMEM_COLS = 512;
   static_assert(SF_COL0 + SF_SLOTS * SF_COLS <= TMEM_COLS, "tmem budget");
@@ -210,6 +216,14 @@ __device__ __forceinline__ bool lane_next(LaneSched &L, const WgradParams &p, in
   return lane_turn(L, p, pid, R, bk, 0, L.u0, L.nk0, L.j0, c);
 }
 
+// 16-byte chunk i of staging row `row` (rows of RB = 32, 64 or 128 bytes) under
+// the TMA swizzle of that width: the chunk index is XORed with address bits
+// 7.. of the row start.
+template <int RB>
+__device__ __forceinline__ int swz_chunk(int i, int row) {
+  return i ^ (((row * RB) >> 7) & (RB / 16 - 1));
+}
+
 #ifdef DG_KERNEL_TIMERS
 #define DG_T0(v) const unsigned long long v = clock64()
 #define DG_TACC(slot, v) (tm[slot] += clock64() - (v))
@@ -289,7 +303,7 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
     if (lane == 0) {
       prefetch_tmap(&p.tmA);
       prefetch_tmap(&p.tmB);
-      const uint32_t tx = 2 * (Cfg::A_BYTES + Cfg::B_BYTES);   // both CTAs' bytes
+      const uint32_t tx = 2 * (Cfg::A_BYTES + Cfg::B_LOAD_BYTES);   // both CTAs' bytes
       const uint64_t keep = l2_policy_evict_last();   // operands are re-read by other tiles
       int s = 0;
       uint32_t ph = 0, armed = 0;
@@ -547,8 +561,8 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
     // ------------------------------------------------------------ epilogue
     // Each warp owns one tensor-memory lane quadrant (32 rows of this CTA's
     // 128) and runs its own pipeline, so the four warps never wait on one
-    // another: tcgen05.ld of 32 columns -> one of its EPI_BUFS 4 KB swizzled
-    // staging buffers -> TMA store (or reduce-add) of that 32 x 32 box.
+    // another: tcgen05.ld of EC columns -> one of its EPI_BUFS swizzled
+    // staging buffers -> TMA store (or reduce-add) of that 32-row box.
     const int q = warp & 3;               // tensor-memory lane quadrant of this warp
     uint32_t uses[2] = {0, 0}, nchunk = 0;
     uint32_t cuse[2] = {0, 0};
@@ -557,7 +571,8 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
     const uint32_t acce_leader = mapa_shared(smem_u32(&acce[0]), 0);
     uint8_t *wstg = smem + Cfg::OFF_STG + q * Cfg::EPI_BUFS * Cfg::WSTG_BYTES;
     uint64_t *wcbar = cbar + 2 * q;
-    uint32_t r[32];   // tensor-memory chunk in flight
+    constexpr int EC = Cfg::EC;
+    uint32_t r[EC];   // tensor-memory chunk in flight
     LaneSched L;
     lane_init(L, p, pid, R);
     Chunk ch;
@@ -575,10 +590,10 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
         tc_fence_after();
       }
       const int ncols = min(kBN, p.N - tc.n0);
-      const int nch = (ncols + 31) / 32;
+      const int nch = (ncols + EC - 1) / EC;
       const int row0 = tc.m0 + 32 * q;    // first output row of this warp's boxes
       const uint32_t tmem_row = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + b * kBN;
-      if (mma_tile) tmem_ld_32x32b_x32(tmem_row, r);
+      if (mma_tile) tmem_ld_row<EC>(tmem_row, r);
       bool ok = true;
       for (int c = 0; c < nch; ++c, ++nchunk) {
         const int sbuf = static_cast<int>(nchunk % Cfg::EPI_BUFS);
@@ -588,19 +603,19 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
         __syncwarp();
         DG_TACC(2, w1);
         if (kHasC && lane == 0) {
-          mbar_arrive_expect_tx(&wcbar[sbuf], 32 * 128);
-          tma_load_3d(stg, &p.tmC, &wcbar[sbuf], tc.n0 + 32 * c, row0, tc.expert);
+          mbar_arrive_expect_tx(&wcbar[sbuf], 32 * EC * 4);
+          tma_load_3d(stg, &p.tmC, &wcbar[sbuf], tc.n0 + EC * c, row0, tc.expert);
         }
-        float v[32];
+        float v[EC];
         if (mma_tile) {
           // Chunk c was requested one iteration earlier; request chunk c + 1
           // now so that it streams in while this one is staged.
           tmem_wait_ld();
-          tmem_reg_fence(r);
+          tmem_reg_fence_n<EC>(r);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+          for (int i = 0; i < EC; ++i) v[i] = __uint_as_float(r[i]);
           if (c + 1 < nch) {
-            tmem_ld_32x32b_x32(tmem_row + 32 * (c + 1), r);
+            tmem_ld_row<EC>(tmem_row + EC * (c + 1), r);
           } else {
             // Every read of this buffer has completed (tcgen05.wait::ld above);
             // the tcgen05 fence orders them before the release, so a CTA-scope
@@ -611,17 +626,17 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
           }
         } else {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = 0.f;
+          for (int i = 0; i < EC; ++i) v[i] = 0.f;
         }
         if constexpr (kHasC) {
           ok = mbar_wait(&wcbar[sbuf], cuse[sbuf] & 1, abort_flag, lim, p.status, W_EPI_C, t);
           cuse[sbuf]++;
           ok = __all_sync(0xffffffffu, ok);
           if (!ok) break;
-          const uint8_t *rowp = stg + lane * 128;
+          const uint8_t *rowp = stg + lane * (EC * 4);
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const float4 cv = *reinterpret_cast<const float4 *>(rowp + ((i ^ (lane & 7)) << 4));
+          for (int i = 0; i < EC / 4; ++i) {
+            const float4 cv = *reinterpret_cast<const float4 *>(rowp + (swz_chunk<EC * 4>(i, lane) << 4));
             v[4 * i + 0] += cv.x;
             v[4 * i + 1] += cv.y;
             v[4 * i + 2] += cv.z;
@@ -629,11 +644,9 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
           }
         }
         if constexpr (kOut == OUT_BF16) {
-          // 64-byte rows, 64-byte swizzle: 16-byte chunk i of row l sits at
-          // chunk i ^ ((l >> 1) & 3).
-          uint8_t *rowp = stg + lane * 64;
+          uint8_t *rowp = stg + lane * (EC * 2);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
+          for (int i = 0; i < EC / 8; ++i) {
             uint32_t w[4];
 #pragma unroll
             for (int h = 0; h < 4; ++h) {
@@ -641,24 +654,23 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
                   __floats2bfloat162_rn(v[8 * i + 2 * h], v[8 * i + 2 * h + 1]);
               w[h] = *reinterpret_cast<const uint32_t *>(&pr);
             }
-            *reinterpret_cast<uint4 *>(rowp + ((i ^ ((lane >> 1) & 3)) << 4)) =
+            *reinterpret_cast<uint4 *>(rowp + (swz_chunk<EC * 2>(i, lane) << 4)) =
                 make_uint4(w[0], w[1], w[2], w[3]);
           }
         } else {
-          // 128-byte rows, 128-byte swizzle: chunk i of row l at i ^ (l & 7).
-          uint8_t *rowp = stg + lane * 128;
+          uint8_t *rowp = stg + lane * (EC * 4);
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            *reinterpret_cast<float4 *>(rowp + ((i ^ (lane & 7)) << 4)) =
+          for (int i = 0; i < EC / 4; ++i)
+            *reinterpret_cast<float4 *>(rowp + (swz_chunk<EC * 4>(i, lane) << 4)) =
                 make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
         }
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
           if constexpr (kOut == OUT_F32_REDUCE)
-            tma_reduce_add_3d_hint(&p.tmD, stg, tc.n0 + 32 * c, row0, tc.expert, stream_out);
+            tma_reduce_add_3d_hint(&p.tmD, stg, tc.n0 + EC * c, row0, tc.expert, stream_out);
           else
-            tma_store_3d_hint(&p.tmD, stg, tc.n0 + 32 * c, row0, tc.expert, stream_out);
+            tma_store_3d_hint(&p.tmD, stg, tc.n0 + EC * c, row0, tc.expert, stream_out);
           bulk_commit();
         }
       }

@@ -91,6 +91,15 @@ constexpr int kPairM = 256;
 // Stages of a long tile issued per turn before the MMA stream switches to the
 // other accumulator's tile (FP8 stages are 128 tokens, BF16 64).
 constexpr int kFp8Chunk = 12;
+// Epilogue chunk: output columns per staged TMA store box (32 rows high).
+constexpr int kEpiCols = 32;
+// Staging row of kEpiCols elements of `bytes` each is stored with the TMA
+// swizzle of its width (32, 64 or 128 bytes).
+inline CUtensorMapSwizzle epi_swizzle(int elem_bytes) {
+  const int row = kEpiCols * elem_bytes;
+  return row >= 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                    : row == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
+}
 constexpr int kBf16Chunk = 24;
 int fp8_pick_block_n(int N);
 int bf16_pick_block_n(int N);
