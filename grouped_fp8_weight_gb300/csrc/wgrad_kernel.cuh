@@ -57,6 +57,7 @@ struct WgradCfg {
   static constexpr int ATOM = 128 / ELEM;               // elements per swizzle row
   static constexpr int MMA_K = kFP8 ? 32 : 16;          // K of one tcgen05.mma
   static constexpr int KSTEPS = BK / MMA_K;             // 4
+  static constexpr int ROT_UNIT = kFP8 ? 8 : 16;        // k-loop rotation step (stages)
   static constexpr int BN_CTA = kBN / 2;                // B columns held per CTA
   static constexpr int A_ATOMS = BM / ATOM;
   static constexpr int B_ATOMS = (BN_CTA + ATOM - 1) / ATOM;
@@ -133,7 +134,7 @@ __device__ __forceinline__ bool epi_all(bool ok) {
 
 struct TileCoord {
   int expert, k_off, k_len, m0, n0;   // m0: this CTA's first row; n0: the pair's first column
-  int nt, g_off;                      // N-tile index; first packed scale group of the expert
+  int mt, nt, g_off;                  // M- and N-tile index; first packed scale group of the expert
 };
 
 __device__ __forceinline__ TileCoord tile_coord(const WgradParams &p, int u, int bn,
@@ -144,7 +145,18 @@ __device__ __forceinline__ TileCoord tile_coord(const WgradParams &p, int u, int
   const int mt = p.m_fastest ? lt % p.m_tiles : lt / p.n_tiles;
   const int nt = p.m_fastest ? lt / p.m_tiles : lt % p.n_tiles;
   return TileCoord{se.expert, se.k_off, se.k_len, mt * 256 + static_cast<int>(rank) * 128,
-                   nt * bn, nt, se.g_off};
+                   nt * bn, mt, nt, se.g_off};
+}
+
+// Rotation of a tile's k loop, in stages.  Tiles running at the same time that
+// share an operand slice (same expert, same M tile or same N tile) start their
+// k loops `unit` stages apart, so each k-block of the slice is first read (from
+// HBM) by one of them and found in L2 by the others, instead of all of them
+// waiting on the same HBM fetch.  `unit` is a multiple of the scale-group size,
+// so scale groups stay whole.
+__device__ __forceinline__ int tile_rot(int mt, int nt, int nk, int unit) {
+  const int nu = nk / unit;
+  return nu >= 2 ? unit * ((mt + nt) % nu) : 0;
 }
 
 // ---------------------------------------------------------------- schedule
@@ -319,8 +331,11 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
             p.ks_dev[tc.expert] != tc.k_len)
           atomicCAS(&p.status->code, DEV_OK, DEV_KS_MISMATCH);
         const int nb = tc.n0 + static_cast<int>(rank) * Cfg::BN_CTA;   // this CTA's B columns
+        const int rot = tile_rot(tc.mt, tc.nt, ch.nk, Cfg::ROT_UNIT);
         for (int j = ch.j0; j < ch.j1; ++j) {
-          const int k = tc.k_off + j * Cfg::BK;
+          int jj = j + rot;   // stage of the tile's k range loaded at position j
+          if (jj >= ch.nk) jj -= ch.nk;
+          const int k = tc.k_off + jj * Cfg::BK;
           DG_T0(w1);
           ok = mbar_wait(&empty[s], ph ^ 1, abort_flag, lim, p.status, W_PROD_EMPTY, t);
           DG_TACC(0, w1);
@@ -387,9 +402,13 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
           tc_fence_after();
         }
         const uint32_t d_tmem = tmem_base + b * kBN;
+        const TileCoord tcm = tile_coord(p, ch.u, kBN, 0);
+        const int rot = tile_rot(tcm.mt, tcm.nt, ch.nk, Cfg::ROT_UNIT);
         for (int j = ch.j0; j < ch.j1; ++j) {
+          int jj = j + rot;   // k-block of this position
+          if (jj >= ch.nk) jj -= ch.nk;
           if constexpr (kFP8) {
-            if (j % gs == 0) {
+            if (jj % gs == 0) {
               DG_T0(w1);
               ok = mbar_wait(&sfr[g], gph, abort_flag, lim, p.status, W_MMA_SFR, t);
               DG_TACC(2, w1);
@@ -416,7 +435,7 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
           tc_fence_after();
           // gran_k 128: byte j%4 of each scale word holds this k-block's
           // scale; gran_k 32: byte ks holds this 32-token sub-block's.
-          const uint32_t idesc_j = kIdescBase | ((gs == 4) ? (static_cast<uint32_t>(j & 3) * 0x20000010u) : 0u);
+          const uint32_t idesc_j = kIdescBase | ((gs == 4) ? (static_cast<uint32_t>(jj & 3) * 0x20000010u) : 0u);
 #pragma unroll
           for (int ks = 0; ks < Cfg::KSTEPS; ++ks) {
             const uint64_t ad = a_desc + static_cast<uint64_t>(ks * (Cfg::KSTEP_BYTES >> 4));
@@ -469,11 +488,15 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
           const int t = ch.u;
           const int nk = ch.nk;
           const int tail = p.sched[ch.u / p.tiles_per_group].k_len - (nk - 1) * Cfg::BK;
+          const TileCoord tcg = tile_coord(p, ch.u, kBN, 0);
+          const int rot = tile_rot(tcg.mt, tcg.nt, nk, Cfg::ROT_UNIT);
           for (int j = ch.j0; j < ch.j1; ++j) {
+            int jj = j + rot;
+            if (jj >= nk) jj -= nk;
             ok = mbar_wait(&full[s], ph, abort_flag, lim, p.status, W_SF_FULL, t);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
-            if (j == nk - 1 && tail < Cfg::BK) {
+            if (jj == nk - 1 && tail < Cfg::BK) {
               const uint32_t sa = smem_u32(smem + Cfg::OFF_A + s * Cfg::A_BYTES);
               const uint32_t sb = smem_u32(smem + Cfg::OFF_B + s * Cfg::B_BYTES);
               const int per_atom = (Cfg::BK - tail) * 8;   // 16-byte chunks per atom
@@ -514,21 +537,28 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
         lane_init(L, p, pid, R);
         Chunk ch;
         TileCoord tc{};
-        int j = 0;          // next k-block of the current chunk
-        bool have = false;  // a chunk with k-blocks left is current
+        int j = 0, rot = 0, jj = 0;   // position in the current chunk, its k-block
+        bool have = false;            // a chunk with positions left is current
         uint32_t ig = 0;
         bool ok = true;
         while (ok) {
-          // next scale group: a k-block j with j % gs == 0 (chunks start on
-          // group boundaries)
-          while (!have || j >= ch.j1) {
-            have = lane_next(L, p, pid, R, Cfg::BK, ch);
-            if (!have) break;
-            if (ch.nk == 0) { have = false; continue; }
-            tc = tile_coord(p, ch.u, kBN, rank);
-            j = ch.j0;
+          // next scale group: the next position whose k-block starts a group
+          bool found = false;
+          while (!found) {
+            if (!have || j >= ch.j1) {
+              have = lane_next(L, p, pid, R, Cfg::BK, ch);
+              if (!have) break;
+              if (ch.nk == 0) { have = false; continue; }
+              tc = tile_coord(p, ch.u, kBN, rank);
+              rot = tile_rot(tc.mt, tc.nt, ch.nk, Cfg::ROT_UNIT);
+              j = ch.j0;
+              continue;
+            }
+            jj = j + rot;
+            if (jj >= ch.nk) jj -= ch.nk;
+            if (jj % gs == 0) found = true; else ++j;
           }
-          if (!have) break;
+          if (!found) break;
           const int g = ig % NS;
           DG_T0(w0);
           ok = mbar_wait(&sfe[g], ((ig / NS) & 1) ^ 1, abort_flag, lim, p.status, W_PROD_SFE,
@@ -536,13 +566,13 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
           DG_TACC(2, w0);
           if (!ok) break;
           if (leader) mbar_arrive_expect_tx(&sfr[g], 2 * (Cfg::UT_A + Cfg::UT_B));
-          const int grp = tc.g_off + j / gs;
+          const int grp = tc.g_off + jj / gs;
           tma_load_2d_pair(smem + Cfg::OFF_UTA + g * Cfg::UT_A, &p.tmSFA, sfr_leader + 8 * g, 0,
                            grp * p.sf_mc + tc.m0 / 128, keep);
           tma_load_2d_pair(smem + Cfg::OFF_UTB + g * Cfg::UT_B, &p.tmSFB, sfr_leader + 8 * g, 0,
                            (grp * p.n_tiles + tc.nt) * Cfg::SF_CHUNKS_B, keep);
           ++ig;
-          j += gs;
+          ++j;
         }
         // Let every record this CTA requested land before the pair can exit:
         // the even CTA sees them on `sfr`; its partner sees the slots' copies
