@@ -90,7 +90,7 @@ cudaError_t launch_quant_colblock(const void *x, int64_t T, int C, void *q, uint
 constexpr int kPairM = 256;
 // Stages of a long tile issued per turn before the MMA stream switches to the
 // other accumulator's tile (FP8 stages are 128 tokens, BF16 64).
-constexpr int kFp8Chunk = 12;
+constexpr int kFp8Chunk = 40;
 // Epilogue chunk: output columns per staged TMA store box (32 rows high).
 constexpr int kEpiCols = 32;
 // Staging row of kEpiCols elements of `bytes` each is stored with the TMA
@@ -100,7 +100,7 @@ inline CUtensorMapSwizzle epi_swizzle(int elem_bytes) {
   return row >= 128 ? CU_TENSOR_MAP_SWIZZLE_128B
                     : row == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
 }
-constexpr int kBf16Chunk = 24;
+constexpr int kBf16Chunk = 80;
 int fp8_pick_block_n(int N);
 int bf16_pick_block_n(int N);
 
