@@ -148,15 +148,28 @@ __device__ __forceinline__ TileCoord tile_coord(const WgradParams &p, int u, int
                    nt * bn, mt, nt, se.g_off};
 }
 
-// Rotation of a tile's k loop, in stages.  Tiles running at the same time that
-// share an operand slice (same expert, same M tile or same N tile) start their
-// k loops `unit` stages apart, so each k-block of the slice is first read (from
-// HBM) by one of them and found in L2 by the others, instead of all of them
-// waiting on the same HBM fetch.  `unit` is a multiple of the scale-group size,
-// so scale groups stay whole.
-__device__ __forceinline__ int tile_rot(int mt, int nt, int nk, int unit) {
-  const int nu = nk / unit;
-  return nu >= 2 ? unit * ((mt + nt) % nu) : 0;
+// Rotation of a tile's k loop.  Tiles running at the same time that share an
+// operand slice (same expert, same M tile or same N tile) start their k loops
+// `unit` stages apart, so each k-block of the slice is first read (from HBM)
+// by one of them and found in L2 by the others, instead of all of them
+// waiting on the same HBM fetch.  Only the first F = nk rounded down to a
+// multiple of 4 stages rotate; a last partial scale group stays at the end.
+// With `unit` a multiple of 4, every scale group is visited whole and starts at
+// a position that is a multiple of 4, as in the unrotated loop, so lane
+// chunks (multiples of 4 stages) always begin with a new group.
+struct KRot {
+  int rot, F;
+};
+__device__ __forceinline__ KRot tile_rot(int mt, int nt, int nk, int unit) {
+  const int F = nk & ~3;
+  const int nu = F / unit;
+  return KRot{nu >= 2 ? unit * ((mt + nt) % nu) : 0, F};
+}
+// Stage of the tile's k range visited at loop position j.
+__device__ __forceinline__ int rot_stage(int j, KRot r) {
+  if (j >= r.F) return j;
+  const int x = j + r.rot;
+  return x < r.F ? x : x - r.F;
 }
 
 // ---------------------------------------------------------------- schedule
@@ -331,10 +344,9 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
             p.ks_dev[tc.expert] != tc.k_len)
           atomicCAS(&p.status->code, DEV_OK, DEV_KS_MISMATCH);
         const int nb = tc.n0 + static_cast<int>(rank) * Cfg::BN_CTA;   // this CTA's B columns
-        const int rot = tile_rot(tc.mt, tc.nt, ch.nk, Cfg::ROT_UNIT);
+        const KRot rot = tile_rot(tc.mt, tc.nt, ch.nk, Cfg::ROT_UNIT);
         for (int j = ch.j0; j < ch.j1; ++j) {
-          int jj = j + rot;   // stage of the tile's k range loaded at position j
-          if (jj >= ch.nk) jj -= ch.nk;
+          const int jj = rot_stage(j, rot);   // stage of the tile's k range at position j
           const int k = tc.k_off + jj * Cfg::BK;
           DG_T0(w1);
           ok = mbar_wait(&empty[s], ph ^ 1, abort_flag, lim, p.status, W_PROD_EMPTY, t);
@@ -403,10 +415,9 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
         }
         const uint32_t d_tmem = tmem_base + b * kBN;
         const TileCoord tcm = tile_coord(p, ch.u, kBN, 0);
-        const int rot = tile_rot(tcm.mt, tcm.nt, ch.nk, Cfg::ROT_UNIT);
+        const KRot rot = tile_rot(tcm.mt, tcm.nt, ch.nk, Cfg::ROT_UNIT);
         for (int j = ch.j0; j < ch.j1; ++j) {
-          int jj = j + rot;   // k-block of this position
-          if (jj >= ch.nk) jj -= ch.nk;
+          const int jj = rot_stage(j, rot);   // k-block of this position
           if constexpr (kFP8) {
             if (jj % gs == 0) {
               DG_T0(w1);
@@ -489,10 +500,9 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
           const int nk = ch.nk;
           const int tail = p.sched[ch.u / p.tiles_per_group].k_len - (nk - 1) * Cfg::BK;
           const TileCoord tcg = tile_coord(p, ch.u, kBN, 0);
-          const int rot = tile_rot(tcg.mt, tcg.nt, nk, Cfg::ROT_UNIT);
+          const KRot rot = tile_rot(tcg.mt, tcg.nt, nk, Cfg::ROT_UNIT);
           for (int j = ch.j0; j < ch.j1; ++j) {
-            int jj = j + rot;
-            if (jj >= nk) jj -= nk;
+            const int jj = rot_stage(j, rot);
             ok = mbar_wait(&full[s], ph, abort_flag, lim, p.status, W_SF_FULL, t);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
@@ -537,7 +547,8 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
         lane_init(L, p, pid, R);
         Chunk ch;
         TileCoord tc{};
-        int j = 0, rot = 0, jj = 0;   // position in the current chunk, its k-block
+        int j = 0, jj = 0;            // position in the current chunk, its k-block
+        KRot rot{0, 0};
         bool have = false;            // a chunk with positions left is current
         uint32_t ig = 0;
         bool ok = true;
@@ -554,8 +565,7 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
               j = ch.j0;
               continue;
             }
-            jj = j + rot;
-            if (jj >= ch.nk) jj -= ch.nk;
+            jj = rot_stage(j, rot);
             if (jj % gs == 0) found = true; else ++j;
           }
           if (!found) break;

@@ -19,9 +19,13 @@
  *    DEVICE pointer on the current CUDA device; ks_host is a HOST pointer.
  *  - All matrices are dense row-major with the last index contiguous (no
  *    padding between rows).  Device pointers must be 16-byte aligned.
- *  - The caller owns every buffer.  The library allocates nothing per call;
- *    the first call on a device allocates one small status word for that
- *    device, kept until process exit.
+ *  - The caller owns every buffer.  The first call on a device allocates one
+ *    small status word for that device, kept until process exit.  Each FP8
+ *    GEMM call also takes scratch for its packed scale factors (below) from a
+ *    memory pool the library creates per device: allocated and freed in
+ *    stream order on `stream` (cudaMallocFromPoolAsync / cudaFreeAsync), so
+ *    calls on different streams never share it; the pool keeps freed blocks
+ *    for reuse.  The BF16 GEMM and the cast allocate nothing per call.
  *  - Work is enqueued on `stream` (NULL = legacy default stream) and runs
  *    asynchronously.  ks_host is read during the call only; device buffers
  *    must stay valid until the enqueued work completes.
@@ -96,9 +100,17 @@ typedef enum {
  *           kernel to confirm the host copy; a mismatch is recorded as
  *           DG_ERR_INVALID_ARG in the status word (see dg_sync_check).
  *   gran_k  32 or 128: tokens per scale block ("FP8 Implementation Example").
+ * Work enqueued: a scale-packing pass, then the GEMM.  The pass rewrites every
+ * group of four scale rows (four 128-token blocks at gran_k 128, the four
+ * 32-token blocks of one 128-token block at gran_k 32) of each expert into
+ * 512-byte records laid out as the tensor core reads scales, so the GEMM loads
+ * them with TMA.  Scratch: (scale groups) x (2 * ceil(M / 256) +
+ * ceil(N / BN) * ceil(BN / 128)) x 512 bytes, BN = 224 if N % 224 == 0 else
+ * 128 -- about 3.9 MB for G = 32, M = 4096, N = 7168, sum_k = 32768.
  * Errors: DG_ERR_INVALID_ARG for any violated condition above (including
  * NULL pointers where data is needed and misaligned pointers),
- * DG_ERR_UNSUPPORTED off sm_103, DG_ERR_CUDA on a failed launch.
+ * DG_ERR_UNSUPPORTED off sm_103, DG_ERR_CUDA on a failed launch or scratch
+ * allocation.
  */
 dg_status dg_k_grouped_fp8_wgrad(const void *a, const uint8_t *sfa,
                                  const void *b, const uint8_t *sfb,
@@ -161,23 +173,27 @@ dg_status dg_quant_transpose_fp8(const void *x, int64_t T, int C,
  * addition of this library.
  *
  * The ordinary call allocates a 16-byte status record per device (cudaMalloc)
- * on its first use.  A caller whose device memory is owned by its own caching
- * allocator, or that must not take the device synchronisation cudaMalloc can
- * cause, cannot accept that.  This entry point computes exactly what
- * dg_k_grouped_fp8_wgrad computes, with the same arguments and errors, and
- * allocates nothing: the kernel's status record lives in a 256-byte
- * file-scope device array of the library (every GPU that loads the library
- * holds it until the process exits).
+ * on its first use and takes stream-ordered scratch for the packed scale
+ * factors on every call.  A caller whose device memory is owned by its own
+ * caching allocator, or that must not take the device synchronisation
+ * cudaMalloc can cause, cannot accept that.  This entry point computes exactly
+ * what dg_k_grouped_fp8_wgrad computes, with the same arguments and errors,
+ * and allocates nothing: the status record and the packed scale records live
+ * in one file-scope device array of the library, 256 bytes + 32 MiB (every GPU
+ * that loads this part of the library holds it until the process exits).
  *  - The first call on a device does the set-up (device queries, the
  *    array's device address via cudaGetSymbolAddress); make that first call
  *    before any stream capture.
- *  - Each call clears the record on `stream` before its launch; calls that
- *    overlap on the GPU (on different streams) share the array and race on it.
+ *  - Each call clears the record and rewrites the scale records on `stream`
+ *    before its GEMM; calls that overlap on the GPU (on different streams)
+ *    share the array and race on it.
  *  - It never synchronises, so device-side timeouts and ks_dev mismatches are
  *    not reported (waits stay bounded: the kernel ends early, D unspecified).
- *  - The record needs the same 16 bytes for every problem size; sizes above
- *    the kernel's limits (G > DG_MAX_GROUPS, sum_k >= 2^31 - 256) are rejected
- *    with DG_ERR_UNSUPPORTED and a message.
+ *  - Limits: the packed scale records must fit 32 MiB (their size is given
+ *    under dg_k_grouped_fp8_wgrad; G = 64, M = 4096, N = 7168,
+ *    sum_k = 131072 needs 14 MB); larger problems, and sizes above the
+ *    kernel's own limits (G > DG_MAX_GROUPS, sum_k >= 2^31 - 256), are
+ *    rejected with DG_ERR_UNSUPPORTED and a message.
  */
 dg_status dg_k_grouped_fp8_wgrad_noalloc(const void *a, const uint8_t *sfa,
                                          const void *b, const uint8_t *sfb,

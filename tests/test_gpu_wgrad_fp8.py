@@ -73,6 +73,23 @@ def test_long_expert_many_stages():
     assert_close(d, D, S, what="long")
 
 
+@pytest.mark.parametrize("gran_k", [128, 32])
+def test_lanes_and_rotated_k_loops(gran_k):
+    """Several tiles per CTA pair: long experts (82, 41 k-blocks) are split into
+    lane chunks interleaved with short and output-only tiles, and their k loops
+    are rotated; every expert checked on sampled rows x all N."""
+    ks = [128 * 82, 128 * 41, 128 * 13, 0, 128 * 2, 128]
+    M, N = 2048, 1792
+    qa, sa, qb, sb = _case(ks, M, N, 21, gran_k, scale_noise=True)
+    d = run_fp8(qa, sa, qb, sb, ks, gran_k)
+    rows = np.sort(np.random.default_rng(21).choice(M, 24, replace=False))
+    part = oracle.kgrouped_fp8_wgrad_rows(qa, sa, qb, sb, ks, rows, gran_k)
+    dr = d[:, torch.from_numpy(rows).to(DEV)].double().cpu().numpy()
+    for e, (De, Se) in part.items():
+        assert_close(dr[e], De, Se, what=f"lanes expert {e}")
+    assert torch.count_nonzero(d[3]).item() == 0
+
+
 def test_integer_valued_is_bit_exact():
     """E4M3 integers in [-8, 8] with unit scales: every partial sum is an
     integer below 2^24, so the FP32 result is exact."""
