@@ -31,8 +31,9 @@
 //   warp 6      FP8: scale loader -- fetches each scale group's packed
 //               records (written beforehand by the scale pack pass in the
 //               layout tcgen05.cp copies into tensor memory) up to five groups
-//               ahead.  BF16 (even CTA): stage gate -- zeroes the token rows
-//               past an expert's slice in both CTAs' last stage.
+//               ahead.  BF16: stage gate -- each CTA zeroes the token rows
+//               past an expert's slice in its own tiles of that expert's last
+//               stage.
 // Two accumulators live in tensor memory (the two lanes), so the epilogue of
 // one tile overlaps the MMAs of others.
 //
@@ -102,9 +103,9 @@ struct WgradCfg {
   static constexpr int OFF_UTA = OFF_STG + 4 * EPI_BUFS * WSTG_BYTES;
   static constexpr int OFF_UTB = OFF_UTA + SF_SLOTS * UT_A;
   static constexpr int OFF_BAR = (OFF_UTB + SF_SLOTS * UT_B + 7) / 8 * 8;
-  // barriers: full[S], empty[S], gate[S], accf[2], acce[2], cbar[4 warps x 2],
-  // sfr/sfe[SLOTS], drain
-  static constexpr int NUM_BARS = 3 * STAGES + 2 * NUM_ACC + 8 + 2 * SF_SLOTS + 1;
+  // barriers: full[S], empty[S], gate[S], tfull[S], accf[2], acce[2],
+  // cbar[4 warps x 2], sfr/sfe[SLOTS], drain
+  static constexpr int NUM_BARS = 4 * STAGES + 2 * NUM_ACC + 8 + 2 * SF_SLOTS + 1;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;   // + alignment slack
   static_assert(SMEM_BYTES <= 232448, "shared memory");
@@ -272,7 +273,8 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
   uint64_t *full = bars;           // even CTA: both CTAs' stage bytes landed
   uint64_t *empty = bars + S;      // stage consumed by the pair's MMAs
   uint64_t *gate = bars + 2 * S;   // BF16, even CTA: tail rows masked in both CTAs
-  uint64_t *accf = bars + 3 * S;   // accumulator ready (multicast commit)
+  uint64_t *tfull = bars + 3 * S;  // BF16, odd CTA: its bytes of an expert's last stage landed
+  uint64_t *accf = bars + 4 * S;   // accumulator ready (multicast commit)
   uint64_t *acce = accf + 2;       // even CTA: accumulator drained by both epilogues
   uint64_t *cbar = acce + 2;       // separate-C box landed (per epilogue warp and buffer)
   uint64_t *sfr = cbar + 8;        // even CTA: both CTAs' records of a scale group landed
@@ -299,7 +301,8 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
     for (int i = 0; i < S; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], 1);
-      mbar_init(&gate[i], 1);
+      mbar_init(&gate[i], 2);       // BF16: the stage gate of each CTA
+      mbar_init(&tfull[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&accf[i], 1);
@@ -352,17 +355,35 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
           ok = mbar_wait(&empty[s], ph ^ 1, abort_flag, lim, p.status, W_PROD_EMPTY, t);
           DG_TACC(0, w1);
           if (!ok) break;
-          if (leader) mbar_arrive_expect_tx(&full[s], tx);
-          const uint32_t fbar = mapa_shared(smem_u32(&full[s]), 0);
+          // BF16: the odd CTA's bytes of an expert's last, partial stage
+          // complete on its own `tfull`, so that its gate can mask the rows
+          // past the slice once they land; every other stage of both CTAs
+          // completes on the even CTA's `full`.
+          const bool tail_stage = !kFP8 && jj == ch.nk - 1 && tc.k_len - jj * Cfg::BK < Cfg::BK;
+          if (leader) mbar_arrive_expect_tx(&full[s], tail_stage ? tx / 2 : tx);
           uint8_t *sa = smem + Cfg::OFF_A + s * Cfg::A_BYTES;
           uint8_t *sb = smem + Cfg::OFF_B + s * Cfg::B_BYTES;
+          if (tail_stage && !leader) {
+            mbar_arrive_expect_tx(&tfull[s], tx / 2);
 #pragma unroll
-          for (int a = 0; a < Cfg::A_ATOMS; ++a)
-            tma_load_2d_pair(sa + a * Cfg::ATOM_BYTES, &p.tmA, fbar, tc.m0 + a * Cfg::ATOM, k,
-                             keep);
+            for (int a = 0; a < Cfg::A_ATOMS; ++a)
+              tma_load_2d_hint(sa + a * Cfg::ATOM_BYTES, &p.tmA, &tfull[s], tc.m0 + a * Cfg::ATOM,
+                               k, keep);
 #pragma unroll
-          for (int b = 0; b < Cfg::B_ATOMS; ++b)
-            tma_load_2d_pair(sb + b * Cfg::ATOM_BYTES, &p.tmB, fbar, nb + b * Cfg::ATOM, k, keep);
+            for (int b = 0; b < Cfg::B_ATOMS; ++b)
+              tma_load_2d_hint(sb + b * Cfg::ATOM_BYTES, &p.tmB, &tfull[s], nb + b * Cfg::ATOM, k,
+                               keep);
+          } else {
+            const uint32_t fbar = mapa_shared(smem_u32(&full[s]), 0);
+#pragma unroll
+            for (int a = 0; a < Cfg::A_ATOMS; ++a)
+              tma_load_2d_pair(sa + a * Cfg::ATOM_BYTES, &p.tmA, fbar, tc.m0 + a * Cfg::ATOM, k,
+                               keep);
+#pragma unroll
+            for (int b = 0; b < Cfg::B_ATOMS; ++b)
+              tma_load_2d_pair(sb + b * Cfg::ATOM_BYTES, &p.tmB, fbar, nb + b * Cfg::ATOM, k,
+                               keep);
+          }
           ++armed;
           if (++s == S) { s = 0; ph ^= 1; }
         }
@@ -483,14 +504,19 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
   } else if (warp == 6) {
     if constexpr (!kFP8) {
       // ---------------------------------------------------------- BF16 stage gate
-      // In the even CTA, every stage passes through here in order.  An
-      // expert's last stage may run past its slice: those token rows of both
-      // operands, in both CTAs, are zeroed so they add nothing (row k of an
-      // atom is bytes [k*128, k*128 + 128)).
-      if (leader) {
+      // Every stage passes through here in order, in both CTAs.  An expert's
+      // last stage may run past its slice: each CTA zeroes those token rows of
+      // its own operand tiles (row k of an atom is bytes [k*128, k*128 + 128))
+      // once they have landed, makes the writes visible to the tensor core
+      // (CTA-scope proxy fence) and arrives on the even CTA's `gate`.  The
+      // odd CTA's other stages need no work: it arrives once the stage's slot
+      // is free, well before their data land on the even CTA's `full`.
+      {
         int s = 0;
         uint32_t ph = 0;
+        uint32_t tph = 0;   // odd CTA: phase bit of each slot's `tfull` (advances on tail stages only)
         bool ok = true;
+        const uint32_t gate_leader = mapa_shared(smem_u32(&gate[0]), 0);
         LaneSched L;
         lane_init(L, p, pid, R);
         Chunk ch;
@@ -503,31 +529,40 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
           const KRot rot = tile_rot(tcg.mt, tcg.nt, nk, Cfg::ROT_UNIT);
           for (int j = ch.j0; j < ch.j1; ++j) {
             const int jj = rot_stage(j, rot);
-            ok = mbar_wait(&full[s], ph, abort_flag, lim, p.status, W_SF_FULL, t);
+            const bool tail_stage = (jj == nk - 1 && tail < Cfg::BK);
+            // the slot's previous use has been consumed (keeps gate phases in order)
+            ok = mbar_wait(&empty[s], ph ^ 1, abort_flag, lim, p.status, W_SF_FULL, t);
+            if (ok && leader)
+              ok = mbar_wait(&full[s], ph, abort_flag, lim, p.status, W_SF_FULL, t);
+            if (ok && !leader && tail_stage) {
+              ok = mbar_wait(&tfull[s], (tph >> s) & 1, abort_flag, lim, p.status, W_SF_FULL, t);
+              tph ^= 1u << s;
+            }
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
-            if (jj == nk - 1 && tail < Cfg::BK) {
-              const uint32_t sa = smem_u32(smem + Cfg::OFF_A + s * Cfg::A_BYTES);
-              const uint32_t sb = smem_u32(smem + Cfg::OFF_B + s * Cfg::B_BYTES);
+            if (tail_stage) {
+              uint8_t *sa = smem + Cfg::OFF_A + s * Cfg::A_BYTES;
+              uint8_t *sb = smem + Cfg::OFF_B + s * Cfg::B_BYTES;
               const int per_atom = (Cfg::BK - tail) * 8;   // 16-byte chunks per atom
               const int n_chunks = per_atom * (Cfg::A_ATOMS + Cfg::B_ATOMS);
-              for (int i = lane; i < 2 * n_chunks; i += 32) {
-                const int cta = i / n_chunks;
-                const int ii = i - cta * n_chunks;
-                const int atom = ii / per_atom;
-                const int r = ii - atom * per_atom;
-                const uint32_t base = atom < Cfg::A_ATOMS
-                                          ? sa + atom * Cfg::ATOM_BYTES
-                                          : sb + (atom - Cfg::A_ATOMS) * Cfg::ATOM_BYTES;
-                const uint32_t addr = mapa_shared(base + tail * 128 + r * 16, cta);
-                asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(addr),
-                             "r"(0u)
-                             : "memory");
+              for (int i = lane; i < n_chunks; i += 32) {
+                const int atom = i / per_atom;
+                const int r = i - atom * per_atom;
+                uint8_t *base = atom < Cfg::A_ATOMS ? sa + atom * Cfg::ATOM_BYTES
+                                                    : sb + (atom - Cfg::A_ATOMS) * Cfg::ATOM_BYTES;
+                *reinterpret_cast<uint4 *>(base + tail * 128 + r * 16) = make_uint4(0, 0, 0, 0);
               }
-              asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
+              fence_proxy_async_smem();
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(&gate[s]);
+            if (lane == 0) {
+              if (leader)
+                mbar_arrive(&gate[s]);
+              else if (tail_stage)
+                mbar_arrive_cluster(gate_leader + 8 * s);   // publishes the zeroed rows
+              else
+                mbar_arrive_remote(gate_leader + 8 * s);
+            }
             if (++s == S) { s = 0; ph ^= 1; }
           }
         }
