@@ -196,6 +196,23 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(value: float, ws: int, device) -> float:
+    """Largest `value` over the ranks of the default process group (the
+    slowest replica sets the job's time); `value` itself when ws == 1."""
+    if ws <= 1:
+        return value
+    import torch.distributed as tdist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(flops_per_replica: float, ws: int, ms_max: float) -> float:
+    """Whole-job TFLOP/s: every rank runs one replica of the workload (weak
+    scaling), all finishing within ms_max."""
+    return ws * flops_per_replica / (ms_max * 1e-3) / 1e12
+
+
 def run_reference(args):
     """Reference arm: the CPU oracle, timed on a bounded sample of the workload
     per step (all experts x 8 seeded rows of M x 64 seeded columns of N)."""
@@ -287,14 +304,9 @@ def run_ours(args):
         torch.cuda.synchronize()
         barrier()
     dg.dg_sync_check()
-    ms_max = ms
-    if ws > 1:
-        import torch.distributed as tdist
-        t = torch.tensor([ms], device=dev)
-        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
-        ms_max = float(t.item())
+    ms_max = max_over_ranks(ms, ws, dev)
     flops = w.flops
-    value = ws * flops / (ms_max * 1e-3) / 1e12
+    value = job_throughput(flops, ws, ms_max)
 
     # ---- roofline of the GEMM kernel (the only kernel of the step)
     alg = algorithmic_bytes(w, ks)
