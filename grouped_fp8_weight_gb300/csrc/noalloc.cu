@@ -191,10 +191,8 @@ extern "C" dg_status dg_k_grouped_fp8_wgrad_noalloc(
                     !al16(a) || !al16(b) || !al16(sfa) || !al16(sfb)))
     return nfail(DG_ERR_INVALID_ARG, "%s: a, b, sfa, sfb must be 16-byte aligned device pointers",
                  fn);
-  NoAllocDevice *dev = nullptr;
-  dg_status s = setup(&dev);
-  if (s != DG_OK) return s;
-
+  // The schedule and the size check need no device: an over-size problem is
+  // rejected before any CUDA call.
   dg::WgradParams &p = t_params;
   std::memset(&p, 0, sizeof(p));
   // Longest experts first; then experts that only need their output written.
@@ -241,12 +239,7 @@ extern "C" dg_status dg_k_grouped_fp8_wgrad_noalloc(
     if (end != env && v > 0) ms = v;
   }
   p.wait_limit_ns = static_cast<uint64_t>(ms) * 1000000ull;
-  p.status = dev->scratch;
   p.ks_dev = ks_dev;
-  if (p.num_tiles == 0) {
-    dg::set_last_error("");
-    return DG_OK;
-  }
   dg::PackParams &pk = t_pack;
   std::memset(&pk, 0, sizeof(pk));
   const size_t sf_bytes = (n_mma > 0) ? dg::plan_scale_pack(p, pk, n_mma, gran_k, bn) : 0;
@@ -254,6 +247,14 @@ extern "C" dg_status dg_k_grouped_fp8_wgrad_noalloc(
     return nfail(DG_ERR_UNSUPPORTED,
                  "%s: the packed scale factors need %zu bytes, above this entry point's %zu",
                  fn, sf_bytes, kScaleBytes);
+  NoAllocDevice *dev = nullptr;
+  dg_status s = setup(&dev);
+  if (s != DG_OK) return s;
+  p.status = dev->scratch;
+  if (p.num_tiles == 0) {
+    dg::set_last_error("");
+    return DG_OK;
+  }
   const uint64_t SK = sum_k;
   if (p.num_mma_tiles > 0) {
     dg::bind_scale_pack(pk, dev->scales, sfa, sfb);

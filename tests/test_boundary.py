@@ -84,6 +84,18 @@ def test_fp8_empty_problem_is_ok_without_device(L):
     assert L.dg_last_error().decode() == ""
 
 
+def test_noalloc_rejects_oversize_scale_records_without_device(L):
+    """The allocation-free entry point keeps the packed scale records in a
+    32 MiB static array: a problem needing more is refused before any CUDA
+    call.  G = 8 experts of 16384 tokens at gran_k 32 on 4096 x 7168 needs
+    (8 * 128 groups) x (32 + 64 records) x 512 B = 48 MiB."""
+    ks = [16384] * 8
+    st = L.dg_k_grouped_fp8_wgrad_noalloc(FAKE, FAKE, FAKE, FAKE, FAKE, B.DG_F32, None, 8, 4096,
+                                          7168, sum(ks), _ks(ks), FAKE, 32, None)
+    assert st == B.DG_ERR_UNSUPPORTED
+    assert "packed scale factors need" in L.dg_last_error().decode()
+
+
 def _bf16(L, **kw):
     a = dict(a=FAKE, b=FAKE, d=FAKE, dt=B.DG_F32, c=None, G=2, M=64, N=72, sk=7, ks=[3, 4],
              ksd=FAKE)
