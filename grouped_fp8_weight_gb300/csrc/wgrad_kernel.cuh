@@ -80,8 +80,6 @@ struct WgradCfg {
   static constexpr int NUM_ACC = 2;
   // FP8 scale groups: four UE8M0 rows (four k-blocks at gran_k 128, the four
   // 32-token sub-blocks of one k-block at gran_k 32), in a ring of SF_SLOTS.
-  // FP8 scale groups: four UE8M0 rows (four k-blocks at gran_k 128, the four
-  // 32-token sub-blocks of one k-block at gran_k 32), in a ring of SF_SLOTS.
   // Each slot holds the group's packed records (UT_A for this CTA's 128 rows
   // of A, UT_B for the tile's BN columns of B) as tcgen05.cp reads them.
   static constexpr int SF_SLOTS = kFP8 ? 5 : 0;
@@ -117,21 +115,6 @@ constexpr int kWgradThreads = 224;
 enum : int { W_PROD_EMPTY = 0x01, W_PROD_DRAIN = 0x02, W_PROD_SFE = 0x03, W_MMA_ACCE = 0x11,
              W_MMA_FULL = 0x12, W_MMA_DRAIN = 0x13, W_MMA_SFR = 0x14, W_EPI_ACCF = 0x21,
              W_EPI_C = 0x22, W_SF_FULL = 0x31 };
-
-// AND-reduce a predicate over the 128 epilogue threads (named barrier 1), so
-// that all four epilogue warps take the same branch.
-__device__ __forceinline__ bool epi_all(bool ok) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\t"
-      "setp.ne.u32 p, %1, 0;\n\t"
-      "bar.red.and.pred q, 1, 128, p;\n\t"
-      "selp.u32 %0, 1, 0, q;\n\t}"
-      : "=r"(r)
-      : "r"(static_cast<uint32_t>(ok))
-      : "memory");
-  return r != 0;
-}
 
 struct TileCoord {
   int expert, k_off, k_len, m0, n0;   // m0: this CTA's first row; n0: the pair's first column
