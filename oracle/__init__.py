@@ -12,7 +12,10 @@ Modules
            UE8M0 power-of-two scale byte.
 ``quant``  the column-block quantiser: one UE8M0 scale per column per
            ``gran_k``-token block, values cast to E4M3 (the transpose + cast
-           step a weight-gradient GEMM needs).
+           step a weight-gradient GEMM needs); the forward pass's 1 x 128
+           row-tile cast and its exact dequantisation (re-quantising stored
+           FP8 activations); the MoE token layout (its plan from top-k
+           routing, and the row gather with zero padding rows).
 ``wgrad``  the K-grouped GEMM ``D[e] = C[e] + A_e^T B_e`` with per-block
            scales, in float64, plus the tolerance budget ``S = sum |a b s|``.
 
@@ -21,7 +24,10 @@ against something other than itself (a library cast, exact rational
 arithmetic, closed forms, invariants).  No function is "parity unpinned".
 """
 from .e4m3 import e4m3_decode, e4m3_encode, ue8m0_to_float, E4M3_MAX  # noqa: F401
-from .quant import scale_exponent, quant_colblock  # noqa: F401
+from .quant import (  # noqa: F401
+    scale_exponent, quant_colblock, quant_rowtile, dequant_rowtile, requant_colblock,
+    gather_rows, moe_layout_cast, moe_layout_plan,
+)
 from .wgrad import (  # noqa: F401
     dequant_colblock, kgrouped_fp8_wgrad, kgrouped_bf16_wgrad,
     kgrouped_fp8_wgrad_rows, kgrouped_bf16_wgrad_rows, expert_offsets,
