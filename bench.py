@@ -12,6 +12,8 @@ The same JSON line also carries:
                 fraction against the FP8 peak (2 x measured BF16);
   pipeline      the cast-inclusive step (BF16 dY, X -> dg_quant_transpose_fp8
                 x2 -> GEMM) on the same shapes, and the cast's own roofline;
+  casts         the re-quantisation of stored FP8 operands and the cast fused
+                with the MoE layout, each against the HBM roofline;
   e2e           the same metric through the C ABI with pinned host buffers:
                 H2D of the step's operands and D2H of the result D in the
                 timed region;
@@ -169,6 +171,67 @@ def time_events(fn, steps, stream):
     end.record(stream)
     end.synchronize()
     return start.elapsed_time(end) / steps
+
+
+def moe_layout_rows(ks, t_tok: int, seed: int) -> np.ndarray:
+    """Source token of every row of the expert layout: expert e's K_e rows take
+    K_e distinct tokens of t_tok, drawn at random and kept in token order."""
+    rng = np.random.default_rng(seed)
+    rows = [np.sort(rng.choice(t_tok, size=k, replace=False)) for k in ks if k > 0]
+    return np.concatenate(rows).astype(np.int32)
+
+
+def measure_casts(w, ks, dev, stream, pk, steps):
+    """The two other casts of the path on the workload's operand shapes, each
+    against the HBM roofline: re-quantising stored FP8 (1 x 128 tiles, random
+    codes and scale bytes) of dY [sum_k, M] and X [sum_k, N]; and the BF16
+    cast of X fused with the MoE layout (each expert's rows gathered from
+    sum_k / 2 tokens)."""
+    import grouped_fp8_weight_gb300 as dg
+    gen = torch.Generator(device=dev).manual_seed(w.seed + 100)
+    out = {}
+    bufs = []
+    for C in (w.M, w.N):
+        q_in = torch.randint(0, 256, (w.sum_k, C), generator=gen, device=dev, dtype=torch.uint8)
+        q_in[(q_in & 0x7F) == 0x7F] = 0x7E
+        sf_in = torch.randint(110, 140, (w.sum_k, C // 128), generator=gen, device=dev,
+                              dtype=torch.uint8)
+        bufs.append((q_in, sf_in, torch.empty_like(q_in),
+                     torch.empty(w.sum_k // 128, C, dtype=torch.uint8, device=dev)))
+
+    def requant():
+        for q_in, sf_in, q, sf in bufs:
+            dg.dg_requant_transpose_fp8(q_in, sf_in, q, sf)
+
+    for _ in range(3):
+        requant()
+    ms = time_events(requant, steps, stream)
+    nb = sum(w.sum_k * C * 2 + 2 * w.sum_k * C // 128 for C in (w.M, w.N))
+    out["requant"] = {"ms": ms, "kernel": "requant_tm_kernel<128> (e4m3 1x128 source, token-major)",
+                      "launches_per_step": 2, "bound": "hbm",
+                      "achieved": nb / (ms * 1e-3) / 1e9, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                      "frac": nb / (ms * 1e-3) / 1e9 / pk["hbm_gbs"], "algorithmic_bytes": nb}
+    del bufs
+
+    t_tok = w.sum_k // 2
+    src = torch.from_numpy(moe_layout_rows(ks, t_tok, w.seed + 101)).to(dev)
+    x = torch.randn(t_tok, w.N, generator=gen, device=dev).to(torch.bfloat16)
+    q = torch.empty(w.sum_k, w.N, dtype=torch.uint8, device=dev)
+    sf = torch.empty(w.sum_k // 128, w.N, dtype=torch.uint8, device=dev)
+
+    def layout_cast():
+        dg.dg_quant_moe_layout_fp8(x, src, q, sf)
+
+    for _ in range(3):
+        layout_cast()
+    ms = time_events(layout_cast, steps, stream)
+    nb = w.sum_k * w.N * 3 + w.sum_k * 4 + (w.sum_k // 128) * w.N
+    out["moe_layout"] = {"ms": ms, "kernel": "cast_colblock_kernel<128, token, bf16, gather>",
+                         "launches_per_step": 1, "source_tokens": t_tok, "rows": w.sum_k,
+                         "bound": "hbm", "achieved": nb / (ms * 1e-3) / 1e9,
+                         "peak": pk["hbm_gbs"], "unit": "GB/s",
+                         "frac": nb / (ms * 1e-3) / 1e9 / pk["hbm_gbs"], "algorithmic_bytes": nb}
+    return out
 
 
 def cpu_oracle_sample(w, ks, qa, sa, qb, sb, n_rows=16):
@@ -359,6 +422,9 @@ def run_ours(args):
                     "algorithmic_bytes": cast_bytes}}
     dg.dg_sync_check()
 
+    casts = measure_casts(w, ks, dev, stream, pk, max(5, args.steps // 4))
+    dg.dg_sync_check()
+
     # ---- end to end through the C ABI with pinned host buffers
     h_qa, h_sa = qa.cpu().pin_memory(), sa.cpu().pin_memory()
     h_qb, h_sb = qb.cpu().pin_memory(), sb.cpu().pin_memory()
@@ -392,7 +458,8 @@ def run_ours(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "e4m3 x e4m3 -> f32", "data": "synthetic",
             "config": workload_config(w, ks), "fp8_peak_frac": tflops / fp8_peak,
-            "roofline": roof, "pipeline": pipeline, "e2e": e2e, "cpu_baseline": cpu,
+            "roofline": roof, "pipeline": pipeline, "casts": casts, "e2e": e2e,
+            "cpu_baseline": cpu,
             "clocks": clk.summary(),
             # per step: the scale-packing pass and the GEMM kernel
             "gpu_launches": 2 * args.steps}

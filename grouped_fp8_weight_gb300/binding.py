@@ -33,6 +33,9 @@ SIGNATURES = {
                                             _I64, _IP, _IP, _I, _VP]),
     "dg_k_grouped_bf16_wgrad": (_I, [_VP, _VP, _VP, _I, _FP, _I, _I, _I, _I64, _IP, _IP, _VP]),
     "dg_quant_transpose_fp8": (_I, [_VP, _I64, _I, _VP, _U8P, _I, _I, _VP]),
+    "dg_requant_transpose_fp8": (_I, [_VP, _U8P, _I64, _I, _VP, _U8P, _I, _I, _VP]),
+    "dg_quant_moe_layout_fp8": (_I, [_VP, _U8P, _I64, _I, _IP, _I64, _VP, _U8P, _I, _I, _VP]),
+    "dg_moe_layout_plan": (_I, [_IP, _I64, _I, _I, _I, _IP, _IP, _IP, _I64, _VP]),
     "dg_last_error": (ctypes.c_char_p, []),
     "dg_sync_check": (_I, [_VP]),
     "dg_version": (_I, []),
@@ -157,6 +160,79 @@ def dg_quant_transpose_fp8(x, q, sf, layout: str = "token", gran_k: int = 128, s
     _check(lib().dg_quant_transpose_fp8(
         _dptr(x), T, C, _dptr(q8), _dptr(sf),
         DG_TOKEN_MAJOR if layout == "token" else DG_CHANNEL_MAJOR, gran_k, _stream(stream)))
+
+
+def _layout(layout):
+    if layout not in ("token", "channel"):
+        raise ValueError("layout must be 'token' or 'channel'")
+    return DG_TOKEN_MAJOR if layout == "token" else DG_CHANNEL_MAJOR
+
+
+def _check_out(q8, sf, T, C, layout, gran_k):
+    _need(q8, torch.uint8, "q", 2)
+    _need(sf, torch.uint8, "sf", 2)
+    want = (T, C) if layout == "token" else (C, T)
+    if tuple(q8.shape) != want or tuple(sf.shape) != (T // gran_k, C):
+        raise ValueError("q / sf shapes do not match the output rows")
+
+
+def dg_requant_transpose_fp8(q_in, sf_in, q, sf, layout: str = "token", gran_k: int = 128,
+                             stream=None):
+    """Stored E4M3 q_in [T, C] with 1 x 128 scales sf_in [T, C/128] (UE8M0) ->
+    column-block E4M3 q ([T, C] or [C, T]) and sf [T/gran_k, C]."""
+    qi = q_in.view(torch.uint8) if q_in.dtype != torch.uint8 else q_in
+    _need(qi, torch.uint8, "q_in", 2)
+    _need(sf_in, torch.uint8, "sf_in", 2)
+    T, C = qi.shape
+    if tuple(sf_in.shape) != (T, C // 128):
+        raise ValueError("sf_in must be [T, C / 128]")
+    q8 = q.view(torch.uint8) if q.dtype != torch.uint8 else q
+    _check_out(q8, sf, T, C, layout, gran_k)
+    _check(lib().dg_requant_transpose_fp8(
+        _dptr(qi), _dptr(sf_in), T, C, _dptr(q8), _dptr(sf), _layout(layout), gran_k,
+        _stream(stream)))
+
+
+def dg_quant_moe_layout_fp8(x, src_rows, q, sf, x_sf=None, layout: str = "token",
+                            gran_k: int = 128, stream=None):
+    """Column-block cast of the MoE-layout rows x[src_rows] (-1: a zero row).
+    x: bf16 [T_src, C], or E4M3 codes [T_src, C] with x_sf uint8 [T_src, C/128];
+    src_rows: int32 CUDA tensor [T]; q ([T, C] or [C, T]), sf [T/gran_k, C]."""
+    if x_sf is None:
+        _need(x, torch.bfloat16, "x", 2)
+        xp = x
+    else:
+        xp = x.view(torch.uint8) if x.dtype != torch.uint8 else x
+        _need(xp, torch.uint8, "x", 2)
+        _need(x_sf, torch.uint8, "x_sf", 2)
+        if tuple(x_sf.shape) != (xp.shape[0], xp.shape[1] // 128):
+            raise ValueError("x_sf must be [T_src, C / 128]")
+    _need(src_rows, torch.int32, "src_rows", 1)
+    T_src, C = xp.shape
+    T = src_rows.numel()
+    q8 = q.view(torch.uint8) if q.dtype != torch.uint8 else q
+    _check_out(q8, sf, T, C, layout, gran_k)
+    _check(lib().dg_quant_moe_layout_fp8(
+        _dptr(xp), _dptr(x_sf), T_src, C, _dptr(src_rows), T, _dptr(q8), _dptr(sf),
+        _layout(layout), gran_k, _stream(stream)))
+
+
+def dg_moe_layout_plan(topk_idx, G: int, align: int = 128, with_pairs: bool = False,
+                       stream=None):
+    """The MoE token layout from routing topk_idx (int32 CUDA [T_tok, topk],
+    -1 = unused slot).  Returns device tensors (ks [G], src_rows [cap], and
+    pair_rows [cap] if with_pairs), cap = T_tok * topk + G * (align - 1); rows
+    past the layout's end are -1 (the layout has ks.sum() rows)."""
+    _need(topk_idx, torch.int32, "topk_idx", 2)
+    T_tok, topk = topk_idx.shape
+    cap = T_tok * topk + G * (align - 1)
+    dev = topk_idx.device
+    ks = torch.empty(G, dtype=torch.int32, device=dev)
+    src = torch.empty(cap, dtype=torch.int32, device=dev)
+    pair = torch.empty(cap, dtype=torch.int32, device=dev) if with_pairs else None
+    _check(lib().dg_moe_layout_plan(_dptr(topk_idx), T_tok, topk, G, align, _dptr(ks),
+                                    _dptr(src), _dptr(pair), cap, _stream(stream)))
+    return (ks, src, pair) if with_pairs else (ks, src)
 
 
 def dg_last_error() -> str:

@@ -344,6 +344,44 @@ dg_status run_grouped(const GroupedArgs &x) {
   return ok();
 }
 
+// Validation and launch shared by the three column-block casts.  a.x_sf set:
+// E4M3 source with 1 x 128 scales (C a multiple of 128); a.src_rows set: MoE
+// layout gather from T_src source rows.
+dg_status run_cast(const char *fn, dg::CastArgs a, dg_layout q_layout, int gran_k,
+                   cudaStream_t stream) {
+  const bool fp8 = (a.x_sf != nullptr);
+  if (gran_k != 32 && gran_k != 128)
+    return fail(DG_ERR_INVALID_ARG, "%s: gran_k = %d (must be 32 or 128)", fn, gran_k);
+  if (q_layout != DG_TOKEN_MAJOR && q_layout != DG_CHANNEL_MAJOR)
+    return fail(DG_ERR_INVALID_ARG, "%s: unknown layout %d", fn, (int)q_layout);
+  if (a.T < 0 || a.T % gran_k)
+    return fail(DG_ERR_INVALID_ARG, "%s: T = %lld must be a non-negative multiple of gran_k",
+                fn, (long long)a.T);
+  const int cmult = fp8 ? 128 : 16;
+  if (a.C <= 0 || a.C % cmult)
+    return fail(DG_ERR_INVALID_ARG, "%s: C = %d must be a positive multiple of %d", fn, a.C,
+                cmult);
+  if ((a.C + 255) / 256 > 65535) return fail(DG_ERR_UNSUPPORTED, "%s: C too large", fn);
+  if ((a.T + 127) / 128 > 0x7FFFFFFFll) return fail(DG_ERR_UNSUPPORTED, "%s: T too large", fn);
+  if (a.src_rows != nullptr && a.T_src > 0x7FFFFFFFll)
+    return fail(DG_ERR_UNSUPPORTED, "%s: T_src above 2^31 - 1 (int32 row indices)", fn);
+  if (a.T == 0) return ok();
+  const bool need_x = (a.src_rows == nullptr) || a.T_src > 0;
+  if ((need_x && (a.x == nullptr || !aligned16(a.x))) || a.q == nullptr || a.sf == nullptr ||
+      !aligned16(a.q) || !aligned16(a.sf) || (fp8 && need_x && !aligned16(a.x_sf)) ||
+      (a.src_rows != nullptr && !aligned16(a.src_rows)))
+    return fail(DG_ERR_INVALID_ARG, "%s: device pointers must be non-NULL and 16-byte aligned",
+                fn);
+  DeviceState *dev = nullptr;
+  dg_status s = device_state(&dev);
+  if (s != DG_OK) return s;
+  a.status = dev->status;
+  cudaError_t e = dg::launch_cast_colblock(a, q_layout == DG_CHANNEL_MAJOR, gran_k, stream);
+  if (e != cudaSuccess)
+    return fail(DG_ERR_CUDA, "%s: launch failed: %s", fn, cudaGetErrorString(e));
+  return ok();
+}
+
 }  // namespace
 
 namespace dg {
@@ -372,27 +410,68 @@ dg_status dg_k_grouped_bf16_wgrad(const void *a, const void *b, void *d, dg_dtyp
 
 dg_status dg_quant_transpose_fp8(const void *x, int64_t T, int C, void *q, uint8_t *sf,
                                  dg_layout q_layout, int gran_k, dg_stream_t stream) {
-  const char *fn = "dg_quant_transpose_fp8";
-  if (gran_k != 32 && gran_k != 128)
-    return fail(DG_ERR_INVALID_ARG, "%s: gran_k = %d (must be 32 or 128)", fn, gran_k);
-  if (q_layout != DG_TOKEN_MAJOR && q_layout != DG_CHANNEL_MAJOR)
-    return fail(DG_ERR_INVALID_ARG, "%s: unknown layout %d", fn, (int)q_layout);
-  if (T < 0 || T % gran_k)
-    return fail(DG_ERR_INVALID_ARG, "%s: T = %lld must be a non-negative multiple of gran_k",
-                fn, (long long)T);
-  if (C <= 0 || C % 16)
-    return fail(DG_ERR_INVALID_ARG, "%s: C = %d must be a positive multiple of 16", fn, C);
-  if ((C + 255) / 256 > 65535) return fail(DG_ERR_UNSUPPORTED, "%s: C too large", fn);
-  if ((T + 127) / 128 > 0x7FFFFFFFll) return fail(DG_ERR_UNSUPPORTED, "%s: T too large", fn);
-  if (T == 0) return ok();
-  if (x == nullptr || q == nullptr || sf == nullptr || !aligned16(x) || !aligned16(q) ||
-      !aligned16(sf))
-    return fail(DG_ERR_INVALID_ARG, "%s: x, q, sf must be 16-byte aligned device pointers", fn);
+  dg::CastArgs a{x, nullptr, nullptr, T, T, C, static_cast<uint8_t *>(q), sf, nullptr};
+  return run_cast("dg_quant_transpose_fp8", a, q_layout, gran_k,
+                  reinterpret_cast<cudaStream_t>(stream));
+}
+
+dg_status dg_requant_transpose_fp8(const void *q_in, const uint8_t *sf_in, int64_t T, int C,
+                                   void *q, uint8_t *sf, dg_layout q_layout, int gran_k,
+                                   dg_stream_t stream) {
+  const char *fn = "dg_requant_transpose_fp8";
+  if (T > 0 && sf_in == nullptr)
+    return fail(DG_ERR_INVALID_ARG, "%s: sf_in is required", fn);
+  dg::CastArgs a{q_in, sf_in, nullptr, T, T, C, static_cast<uint8_t *>(q), sf, nullptr};
+  return run_cast(fn, a, q_layout, gran_k, reinterpret_cast<cudaStream_t>(stream));
+}
+
+dg_status dg_quant_moe_layout_fp8(const void *x, const uint8_t *x_sf, int64_t T_src, int C,
+                                  const int *src_rows, int64_t T, void *q, uint8_t *sf,
+                                  dg_layout q_layout, int gran_k, dg_stream_t stream) {
+  const char *fn = "dg_quant_moe_layout_fp8";
+  if (T_src < 0) return fail(DG_ERR_INVALID_ARG, "%s: T_src < 0", fn);
+  if (T > 0 && src_rows == nullptr)
+    return fail(DG_ERR_INVALID_ARG, "%s: src_rows is required", fn);
+  dg::CastArgs a{x, x_sf, src_rows, T_src, T, C, static_cast<uint8_t *>(q), sf, nullptr};
+  return run_cast(fn, a, q_layout, gran_k, reinterpret_cast<cudaStream_t>(stream));
+}
+
+dg_status dg_moe_layout_plan(const int *topk_idx, int64_t T_tok, int topk, int G, int align,
+                             int *ks, int *src_rows, int *pair_rows, int64_t cap,
+                             dg_stream_t stream) {
+  const char *fn = "dg_moe_layout_plan";
+  if (T_tok < 0 || topk < 1)
+    return fail(DG_ERR_INVALID_ARG, "%s: T_tok = %lld, topk = %d", fn, (long long)T_tok, topk);
+  if (G < 1 || G > DG_MAX_GROUPS)
+    return fail(G < 1 ? DG_ERR_INVALID_ARG : DG_ERR_UNSUPPORTED, "%s: G = %d (1..%d)", fn, G,
+                DG_MAX_GROUPS);
+  if (align < 1 || align > 65536)
+    return fail(DG_ERR_INVALID_ARG, "%s: align = %d (1..65536)", fn, align);
+  const int64_t n = T_tok * static_cast<int64_t>(topk);
+  const int64_t need = n + static_cast<int64_t>(G) * (align - 1);
+  if (T_tok > 0x7FFFFFFFll || need > 0x7FFFFFFFll)
+    return fail(DG_ERR_UNSUPPORTED, "%s: layout rows above 2^31 - 1", fn);
+  if (cap < need)
+    return fail(DG_ERR_INVALID_ARG, "%s: cap = %lld < T_tok * topk + G * (align - 1) = %lld",
+                fn, (long long)cap, (long long)need);
+  if (ks == nullptr || src_rows == nullptr || !aligned16(ks) || !aligned16(src_rows) ||
+      (n > 0 && (topk_idx == nullptr || !aligned16(topk_idx))) ||
+      (pair_rows != nullptr && !aligned16(pair_rows)))
+    return fail(DG_ERR_INVALID_ARG, "%s: device pointers must be non-NULL and 16-byte aligned",
+                fn);
   DeviceState *dev = nullptr;
   dg_status s = device_state(&dev);
   if (s != DG_OK) return s;
-  cudaError_t e = dg::launch_quant_colblock(x, T, C, q, sf, q_layout == DG_CHANNEL_MAJOR, gran_k,
-                                            reinterpret_cast<cudaStream_t>(stream));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  void *scratch = nullptr;
+  cudaError_t e =
+      cudaMallocFromPoolAsync(&scratch, dg::moe_plan_scratch_bytes(n, G), dev->pool, st);
+  if (e != cudaSuccess)
+    return fail(DG_ERR_CUDA, "%s: scratch: %s", fn, cudaGetErrorString(e));
+  dg::MoePlanArgs a{topk_idx, n, topk, G, align, ks, src_rows, pair_rows, cap, scratch,
+                    dev->status};
+  e = dg::launch_moe_layout_plan(a, dev->sms, st);
+  cudaFreeAsync(scratch, st);   // after the plan's kernels in stream order
   if (e != cudaSuccess)
     return fail(DG_ERR_CUDA, "%s: launch failed: %s", fn, cudaGetErrorString(e));
   return ok();
@@ -415,6 +494,10 @@ dg_status dg_sync_check(dg_stream_t stream) {
   if (st.code == dg::DEV_TIMEOUT)
     return fail(DG_ERR_TIMEOUT, "device wait timed out (site 0x%x, block %d, detail %d)",
                 st.where, st.block, st.detail);
+  if (st.code == dg::DEV_BAD_ROW)
+    return fail(DG_ERR_INVALID_ARG, "a src_rows entry lies outside [-1, T_src)");
+  if (st.code == dg::DEV_BAD_ROUTE)
+    return fail(DG_ERR_INVALID_ARG, "a topk_idx entry lies outside [-1, G)");
   return fail(DG_ERR_INVALID_ARG, "ks_dev does not match ks_host");
 }
 

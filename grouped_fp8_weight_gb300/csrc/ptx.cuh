@@ -46,7 +46,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 }
 
 // Status words a kernel may record (first writer wins), read back by the host.
-enum : int { DEV_OK = 0, DEV_KS_MISMATCH = 1, DEV_TIMEOUT = 4 };
+enum : int { DEV_OK = 0, DEV_KS_MISMATCH = 1, DEV_BAD_ROW = 2, DEV_BAD_ROUTE = 3, DEV_TIMEOUT = 4 };
 
 struct DevStatus {
   int code;      // DEV_* (0 = fine)

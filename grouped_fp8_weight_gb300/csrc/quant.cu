@@ -1,19 +1,30 @@
-// Column-block FP8 cast (with optional physical transpose) for sm_103a.
+// Column-block FP8 casts (with optional physical transpose and MoE-layout row
+// gather) for sm_103a.
 //
-// For every gran_k-token block and column of a BF16 matrix x[T, C]:
+// For every gran_k-token block and column of a matrix x[T, C]:
 //   amax = max |x|, e = clamp(ceil(log2(amax / 448)), -127, 127),
 //   sf = e + 127 (UE8M0), q = E4M3 round-to-nearest-even of x * 2^-e.
 //
-// HBM-bound: 2 bytes read and 1 (+1/gran_k) written per element.  One CTA
-// covers 128 tokens x 256 channels (64 KiB of input).  Each thread loads 16
-// rows x 16 bytes with independent vector loads, reduces |x| with packed
-// 16-bit maxima on the BF16 bit patterns (exact: non-negative floats order like
-// their bit patterns), combines the eight warps' partial maxima in shared
+// Sources:
+//   BF16       x[T, C] as stored.
+//   E4M3 tiles the forward pass's stored activations: codes [T, C] with one
+//              UE8M0 scale per token per 128 channels (x = e4m3 * 2^(b - 127));
+//              dequantised exactly in registers, then cast by columns.
+// Optional row gather (the MoE layout): output row t takes source row
+// src_rows[t], or zeros where src_rows[t] == -1 (an expert's padding).
+//
+// HBM-bound: BF16 source 2 bytes read and 1 (+1/gran_k) written per element,
+// E4M3 source 1 (+1/128) read.  One CTA covers 128 tokens x 256 channels.
+// Each thread loads 16 rows x 8 channels with independent vector loads,
+// reduces |x| (BF16: packed 16-bit maxima on the bit patterns, exact because
+// non-negative floats order like their bit patterns; E4M3: float maxima of
+// the dequantised values), combines the eight warps' partial maxima in shared
 // memory, and converts with the hardware's saturating RNE E4M3 conversion.
 // The channel-major variant transposes 4x4 byte blocks in registers and
 // stages the tile in a swizzled shared-memory buffer so that both the shared
 // stores and the 128-byte global row stores are conflict-free and coalesced.
 #include <cstdint>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "wgrad_params.h"
@@ -36,11 +47,50 @@ __device__ __forceinline__ int scale_exp_from_bf16(uint32_t h) {
   return max(-127, min(127, e));
 }
 
+// Exact ceil(log2(amax / 448)) from the float32 bit pattern of a = amax * 2^-8
+// (the E4M3 source keeps its dequantised values scaled by 2^-8 so that every
+// one is finite and exact in float32).  amax / 448 = a / 1.75, so with
+// a = f * 2^q (f in [1, 2)) the result is q + (f > 1.75).  Subnormal a (its
+// mantissa m, a = m * 2^-149) takes q from m's top bit.
+__device__ __forceinline__ int scale_exp_from_f32_shifted(uint32_t bits) {
+  const int ef = static_cast<int>((bits >> 23) & 0xFF);
+  const uint32_t mant = bits & 0x7FFFFFu;
+  int e;
+  if (ef != 0) {
+    e = ef - 127 + (mant > 0x600000u ? 1 : 0);
+  } else if (mant == 0) {
+    e = -127;
+  } else {
+    const int p = 31 - __clz(static_cast<int>(mant));
+    e = p - 149 + (4u * mant > (7u << p) ? 1 : 0);
+  }
+  return max(-127, min(127, e));
+}
+
+// 2^(b - 135) as a float (normal for b >= 9, subnormal below): the factor
+// that takes an E4M3 value to its dequantised value times 2^-8.
+__device__ __forceinline__ float pow2_b_minus_135(uint32_t b) {
+  return b >= 9 ? __uint_as_float((b - 8) << 23) : __uint_as_float(1u << (b + 14));
+}
+
 // Two floats -> two E4M3 bytes (lo in the low byte), RNE, saturating.
 __device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
   uint16_t r;
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
   return static_cast<uint32_t>(r);
+}
+
+// Two E4M3 bytes (lo in the low byte) -> two exact floats.  kFresh: decode
+// again instead of reusing an earlier decode of the same bytes (which would
+// keep every decoded value of the tile live in registers).
+template <bool kFresh = false>
+__device__ __forceinline__ float2 e4m3x2_to_f32(uint32_t two) {
+  uint32_t h;
+  if constexpr (kFresh)
+    asm volatile("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(static_cast<uint16_t>(two & 0xFFFFu)));
+  else
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(static_cast<uint16_t>(two & 0xFFFFu)));
+  return __half22float2(*reinterpret_cast<const __half2 *>(&h));
 }
 
 __device__ __forceinline__ uint32_t quant_word(uint32_t w, float m_lo, float m_hi) {
@@ -49,84 +99,208 @@ __device__ __forceinline__ uint32_t quant_word(uint32_t w, float m_lo, float m_h
   return cvt_e4m3x2(lo, hi);
 }
 
-template <int kGran, bool kChannel>
-__global__ void __launch_bounds__(256, 2)
-    quant_colblock_kernel(const uint16_t *__restrict__ x, int64_t T, int C,
-                          uint8_t *__restrict__ q, uint8_t *__restrict__ sf) {
-  __shared__ uint4 red[8][32];
+// Eight E4M3 source codes of one row (dequantised, times 2^-8 = the factor
+// p) quantised with per-column factors 2^sh, sh = 135 - b (b = the column's
+// new scale byte): ma = 2^min(sh, 127), and, only where sh > 127 (kBig),
+// a second factor 2^(sh - 127) so that every factor stays representable.
+// Every product is exact.
+template <bool kBig>
+__device__ __forceinline__ uint2 requant8(uint2 c, float p, const float *ma, const uint32_t *sfw) {
+  uint32_t out[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const uint32_t w = h ? c.y : c.x;
+    const float2 a = e4m3x2_to_f32<true>(w);
+    const float2 b = e4m3x2_to_f32<true>(w >> 16);
+    const int k = 4 * h;
+    float y[4] = {a.x * p * ma[k], a.y * p * ma[k + 1], b.x * p * ma[k + 2], b.y * p * ma[k + 3]};
+    if constexpr (kBig) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int bo = static_cast<int>((sfw[h] >> (8 * j)) & 0xFFu);
+        y[j] *= __uint_as_float(static_cast<uint32_t>(max(8 - bo, 0) + 127) << 23);
+      }
+    }
+    out[h] = cvt_e4m3x2(y[0], y[1]) | (cvt_e4m3x2(y[2], y[3]) << 16);
+  }
+  return make_uint2(out[0], out[1]);
+}
+
+// Source row of output row t (-1: not read).  Gather: src_rows[t]; an entry
+// outside [-1, T_src) is not read and is recorded in the status word.
+template <bool kGather>
+__device__ __forceinline__ int64_t source_row(const CastArgs &a, int64_t t, bool in, int lane) {
+  if constexpr (kGather) {
+    const int s = in ? __ldg(a.src_rows + t) : -1;
+    if (s < -1 || s >= a.T_src) {
+      if (lane == 0) atomicCAS(&a.status->code, DEV_OK, DEV_BAD_ROW);
+      return -1;
+    }
+    return s;
+  } else {
+    return in ? t : -1;
+  }
+}
+
+// The factor taking row i's E4M3 values to their dequantised values x 2^-8.
+__device__ __forceinline__ float row_factor(const uint32_t (&sbw)[4], int i) {
+  return pow2_b_minus_135((sbw[i >> 2] >> (8 * (i & 3))) & 0xFFu);
+}
+
+template <bool kBig>
+__device__ __forceinline__ void requant_rows(uint2 (&o)[16], const uint2 (&v8)[16],
+                                             const uint32_t (&sbw)[4], const float (&ma)[8],
+                                             const uint32_t (&sfw)[2]) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i) o[i] = requant8<kBig>(v8[i], row_factor(sbw, i), ma, sfw);
+}
+
+template <int kGran, bool kChannel, bool kFp8Src, bool kGather>
+__global__ void __launch_bounds__(256, 2) cast_colblock_kernel(const CastArgs a) {
+  __shared__ uint4 red[8][32][kFp8Src ? 2 : 1];
   __shared__ __align__(16) uint8_t tq[kChannel ? kTileC * kTileT : 16];
   const int w = threadIdx.x >> 5;
   const int l = threadIdx.x & 31;
   const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kTileT;
+  const int C = a.C;
   const int c0 = blockIdx.y * kTileC;
   const int col = c0 + 8 * l;
   const bool col_ok = col < C;
 
-  uint4 v[16];
-#pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const int64_t t = t0 + 16 * w + i;
-    if (col_ok && t < T)
-      v[i] = __ldcs(reinterpret_cast<const uint4 *>(x + t * C + col));
-    else
-      v[i] = make_uint4(0, 0, 0, 0);
-  }
+  // ---- loads and column maxima
+  uint4 v[kFp8Src ? 1 : 16];
+  uint2 v8[kFp8Src ? 16 : 1];
+  uint32_t sbw[4] = {0, 0, 0, 0};   // E4M3 source: scale byte of row i in byte i % 4 of word i / 4
   uint32_t m[4] = {0, 0, 0, 0};
+  float fm[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  if constexpr (!kFp8Src) {
+    const uint16_t *x = static_cast<const uint16_t *>(a.x);
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    m[0] = __vmaxu2(m[0], v[i].x & 0x7FFF7FFFu);
-    m[1] = __vmaxu2(m[1], v[i].y & 0x7FFF7FFFu);
-    m[2] = __vmaxu2(m[2], v[i].z & 0x7FFF7FFFu);
-    m[3] = __vmaxu2(m[3], v[i].w & 0x7FFF7FFFu);
+    for (int i = 0; i < 16; ++i) {
+      const int64_t t = t0 + 16 * w + i;
+      const int64_t r = source_row<kGather>(a, t, col_ok && t < a.T, l);
+      v[i] = r >= 0 ? __ldcs(reinterpret_cast<const uint4 *>(x + r * C + col))
+                    : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      m[0] = __vmaxu2(m[0], v[i].x & 0x7FFF7FFFu);
+      m[1] = __vmaxu2(m[1], v[i].y & 0x7FFF7FFFu);
+      m[2] = __vmaxu2(m[2], v[i].z & 0x7FFF7FFFu);
+      m[3] = __vmaxu2(m[3], v[i].w & 0x7FFF7FFFu);
+    }
+    red[w][l][0] = make_uint4(m[0], m[1], m[2], m[3]);
+  } else {
+    // Rows not read hold code 0 (value 0 at any scale).
+    const uint8_t *x = static_cast<const uint8_t *>(a.x);
+    const int tiles = C / 128;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int64_t t = t0 + 16 * w + i;
+      const int64_t r = source_row<kGather>(a, t, col_ok && t < a.T, l);
+      v8[i] = r >= 0 ? __ldcs(reinterpret_cast<const uint2 *>(x + r * C + col)) : make_uint2(0, 0);
+      const uint32_t b = r >= 0 ? __ldg(a.x_sf + r * tiles + col / 128) : 0u;
+      sbw[i >> 2] |= b << (8 * (i & 3));
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float p = pow2_b_minus_135((sbw[i >> 2] >> (8 * (i & 3))) & 0xFFu);
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        const float2 f = e4m3x2_to_f32((h & 2 ? v8[i].y : v8[i].x) >> (16 * (h & 1)));
+        fm[2 * h] = fmaxf(fm[2 * h], fabsf(f.x * p));
+        fm[2 * h + 1] = fmaxf(fm[2 * h + 1], fabsf(f.y * p));
+      }
+    }
+    red[w][l][0] = make_uint4(__float_as_uint(fm[0]), __float_as_uint(fm[1]),
+                              __float_as_uint(fm[2]), __float_as_uint(fm[3]));
+    red[w][l][kFp8Src ? 1 : 0] = make_uint4(__float_as_uint(fm[4]), __float_as_uint(fm[5]),
+                                            __float_as_uint(fm[6]), __float_as_uint(fm[7]));
   }
-  red[w][l] = make_uint4(m[0], m[1], m[2], m[3]);
   __syncthreads();
-  uint4 a;
-  if constexpr (kGran == 128) {
-    a = red[0][l];
+
+  // ---- block maxima -> scale exponents and quantisation factors
+  // (non-negative float bit patterns order like the floats: integer maxima)
+  constexpr int kWarps = (kGran == 128) ? 8 : 2;
+  const int w0 = (kGran == 128) ? 0 : (w & ~1);
+  float mul[8], ma[8];
+  uint32_t sfw[2] = {0, 0};
+  bool big = false;   // E4M3 source: a column needs the second factor (sh > 127)
+  if constexpr (!kFp8Src) {
+    uint4 r = red[w0][l][0];
 #pragma unroll
-    for (int ww = 1; ww < 8; ++ww) {
-      const uint4 r = red[ww][l];
-      a.x = __vmaxu2(a.x, r.x);
-      a.y = __vmaxu2(a.y, r.y);
-      a.z = __vmaxu2(a.z, r.z);
-      a.w = __vmaxu2(a.w, r.w);
+    for (int ww = 1; ww < kWarps; ++ww) {
+      const uint4 o = red[w0 + ww][l][0];
+      r.x = __vmaxu2(r.x, o.x);
+      r.y = __vmaxu2(r.y, o.y);
+      r.z = __vmaxu2(r.z, o.z);
+      r.w = __vmaxu2(r.w, o.w);
+    }
+    const uint32_t aw[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int e = scale_exp_from_bf16((aw[k] >> (16 * h)) & 0xFFFFu);
+        mul[2 * k + h] = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+        sfw[k >> 1] |= static_cast<uint32_t>(e + 127) << (8 * (2 * (k & 1) + h));
+      }
     }
   } else {
-    const uint4 r0 = red[w & ~1][l], r1 = red[w | 1][l];
-    a = make_uint4(__vmaxu2(r0.x, r1.x), __vmaxu2(r0.y, r1.y), __vmaxu2(r0.z, r1.z),
-                   __vmaxu2(r0.w, r1.w));
-  }
-  const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
-  float mul[8];
-  uint32_t sfw[2] = {0, 0};
+    uint32_t ab[8];
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
+    for (int j = 0; j < 2; ++j) {
+      uint4 r = red[w0][l][j];
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int e = scale_exp_from_bf16((aw[k] >> (16 * h)) & 0xFFFFu);
-      mul[2 * k + h] = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
-      sfw[k >> 1] |= static_cast<uint32_t>(e + 127) << (8 * (2 * (k & 1) + h));
+      for (int ww = 1; ww < kWarps; ++ww) {
+        const uint4 o = red[w0 + ww][l][j];
+        r.x = max(r.x, o.x);
+        r.y = max(r.y, o.y);
+        r.z = max(r.z, o.z);
+        r.w = max(r.w, o.w);
+      }
+      ab[4 * j] = r.x;
+      ab[4 * j + 1] = r.y;
+      ab[4 * j + 2] = r.z;
+      ab[4 * j + 3] = r.w;
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int e = scale_exp_from_f32_shifted(ab[k]);
+      const int sh = 8 - e;   // y = (x * 2^-8) * 2^sh, sh in [-119, 135]
+      ma[k] = __uint_as_float(static_cast<uint32_t>(min(sh, 127) + 127) << 23);
+      big |= sh > 127;
+      sfw[k >> 2] |= static_cast<uint32_t>(e + 127) << (8 * (k & 3));
     }
   }
   if (col_ok) {
     if constexpr (kGran == 128) {
       if (w == 0)
-        *reinterpret_cast<uint2 *>(sf + (t0 / 128) * C + col) = make_uint2(sfw[0], sfw[1]);
+        *reinterpret_cast<uint2 *>(a.sf + (t0 / 128) * C + col) = make_uint2(sfw[0], sfw[1]);
     } else {
       const int64_t tb = t0 + 16 * w;
-      if ((w & 1) == 0 && tb < T)
-        *reinterpret_cast<uint2 *>(sf + (tb / 32) * C + col) = make_uint2(sfw[0], sfw[1]);
+      if ((w & 1) == 0 && tb < a.T)
+        *reinterpret_cast<uint2 *>(a.sf + (tb / 32) * C + col) = make_uint2(sfw[0], sfw[1]);
     }
   }
 
+  // ---- quantise and store (rows past T are not written; gathered padding
+  // rows are zeros)
+  uint8_t *q = a.q;
+  const int64_t T = a.T;
   uint2 o[16];
+  if constexpr (!kFp8Src) {
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    o[i].x = quant_word(v[i].x, mul[0], mul[1]) | (quant_word(v[i].y, mul[2], mul[3]) << 16);
-    o[i].y = quant_word(v[i].z, mul[4], mul[5]) | (quant_word(v[i].w, mul[6], mul[7]) << 16);
+    for (int i = 0; i < 16; ++i)
+      o[i] = make_uint2(
+          quant_word(v[i].x, mul[0], mul[1]) | (quant_word(v[i].y, mul[2], mul[3]) << 16),
+          quant_word(v[i].z, mul[4], mul[5]) | (quant_word(v[i].w, mul[6], mul[7]) << 16));
+  } else {
+    if (big)
+      requant_rows<true>(o, v8, sbw, ma, sfw);
+    else
+      requant_rows<false>(o, v8, sbw, ma, sfw);
   }
-
   if constexpr (!kChannel) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
@@ -179,26 +353,179 @@ __global__ void __launch_bounds__(256, 2)
   }
 }
 
-}  // namespace
+// Re-quantisation into the token-major layout (the TN GEMM's operand): one
+// CTA covers 128 tokens x 512 channels, each thread 16 rows x 16 channels
+// with 16-byte loads, so that two CTAs per SM keep as many bytes in flight as
+// the BF16 cast does.  A thread's 16 channels lie in one 128-channel tile of
+// the source scales.  After the maxima the codes wait in shared memory (64 KB)
+// instead of registers, and the quantise pass streams them row by row.
+constexpr int kRqTileC = 512;
+constexpr int kRqSmem = kTileT * kRqTileC + 8 * 32 * 64;   // codes + per-warp maxima
 
-cudaError_t launch_quant_colblock(const void *x, int64_t T, int C, void *q, uint8_t *sf,
-                                  int channel_major, int gran_k, cudaStream_t stream) {
-  const dim3 grid(static_cast<unsigned>((T + kTileT - 1) / kTileT),
-                  static_cast<unsigned>((C + kTileC - 1) / kTileC));
-  const auto *xp = static_cast<const uint16_t *>(x);
-  auto *qp = static_cast<uint8_t *>(q);
+template <int kGran, bool kGather>
+__global__ void __launch_bounds__(256, 2) requant_tm_kernel(const CastArgs a) {
+  extern __shared__ __align__(16) uint8_t rq_smem[];
+  uint4 *tile = reinterpret_cast<uint4 *>(rq_smem);                         // [128][32] x 16 B
+  uint4 (*red)[32][4] = reinterpret_cast<uint4 (*)[32][4]>(rq_smem + kTileT * kRqTileC);
+  const int w = threadIdx.x >> 5;
+  const int l = threadIdx.x & 31;
+  const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kTileT;
+  const int C = a.C;
+  const int col = blockIdx.y * kRqTileC + 16 * l;
+  const bool col_ok = col < C;
+  const uint8_t *x = static_cast<const uint8_t *>(a.x);
+  const int tiles = C / 128;
+
+  uint32_t sbw[4] = {0, 0, 0, 0};   // scale byte of row i in byte i % 4 of word i / 4
+  float fm[16];
+#pragma unroll
+  for (int k = 0; k < 16; ++k) fm[k] = 0.f;
+  {
+    uint4 v[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int64_t t = t0 + 16 * w + i;
+      const int64_t r = source_row<kGather>(a, t, col_ok && t < a.T, l);
+      v[i] = r >= 0 ? __ldcs(reinterpret_cast<const uint4 *>(x + r * C + col))
+                    : make_uint4(0, 0, 0, 0);
+      const uint32_t b = r >= 0 ? __ldg(a.x_sf + r * tiles + col / 128) : 0u;
+      sbw[i >> 2] |= b << (8 * (i & 3));
+    }
+    // column maxima of |x| * 2^-8 (exact floats; rows not read hold code 0)
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float p = row_factor(sbw, i);
+      const uint32_t wd[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+      for (int h = 0; h < 8; ++h) {
+        const float2 f = e4m3x2_to_f32(wd[h >> 1] >> (16 * (h & 1)));
+        fm[2 * h] = fmaxf(fm[2 * h], fabsf(f.x * p));
+        fm[2 * h + 1] = fmaxf(fm[2 * h + 1], fabsf(f.y * p));
+      }
+      tile[(16 * w + i) * 32 + l] = v[i];
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    red[w][l][j] = make_uint4(__float_as_uint(fm[4 * j]), __float_as_uint(fm[4 * j + 1]),
+                              __float_as_uint(fm[4 * j + 2]), __float_as_uint(fm[4 * j + 3]));
+  __syncthreads();
+
+  // Block maxima (float bit patterns of non-negative values: integer maxima).
+  constexpr int kWarps = (kGran == 128) ? 8 : 2;
+  const int w0 = (kGran == 128) ? 0 : (w & ~1);
+  float ma[16];
+  uint32_t sfw[4] = {0, 0, 0, 0};
+  bool big = false;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    uint4 r = red[w0][l][j];
+#pragma unroll
+    for (int ww = 1; ww < kWarps; ++ww) {
+      const uint4 o = red[w0 + ww][l][j];
+      r.x = max(r.x, o.x);
+      r.y = max(r.y, o.y);
+      r.z = max(r.z, o.z);
+      r.w = max(r.w, o.w);
+    }
+    const uint32_t ab[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int e = scale_exp_from_f32_shifted(ab[u]);
+      const int sh = 8 - e;
+      ma[4 * j + u] = __uint_as_float(static_cast<uint32_t>(min(sh, 127) + 127) << 23);
+      big |= sh > 127;
+      sfw[j] |= static_cast<uint32_t>(e + 127) << (8 * u);
+    }
+  }
+  if (col_ok) {
+    if constexpr (kGran == 128) {
+      if (w == 0)
+        *reinterpret_cast<uint4 *>(a.sf + (t0 / 128) * C + col) =
+            make_uint4(sfw[0], sfw[1], sfw[2], sfw[3]);
+    } else {
+      const int64_t tb = t0 + 16 * w;
+      if ((w & 1) == 0 && tb < a.T)
+        *reinterpret_cast<uint4 *>(a.sf + (tb / 32) * C + col) =
+            make_uint4(sfw[0], sfw[1], sfw[2], sfw[3]);
+    }
+  }
+
+  // quantise and store, one row at a time from shared memory
+  const float ma_lo[8] = {ma[0], ma[1], ma[2], ma[3], ma[4], ma[5], ma[6], ma[7]};
+  const float ma_hi[8] = {ma[8], ma[9], ma[10], ma[11], ma[12], ma[13], ma[14], ma[15]};
+  const uint32_t sf_lo[2] = {sfw[0], sfw[1]}, sf_hi[2] = {sfw[2], sfw[3]};
+#pragma unroll 4
+  for (int i = 0; i < 16; ++i) {
+    const uint4 c = tile[(16 * w + i) * 32 + l];
+    const float p = pow2_b_minus_135((sbw[i >> 2] >> (8 * (i & 3))) & 0xFFu);
+    uint2 lo, hi;
+    if (big) {
+      lo = requant8<true>(make_uint2(c.x, c.y), p, ma_lo, sf_lo);
+      hi = requant8<true>(make_uint2(c.z, c.w), p, ma_hi, sf_hi);
+    } else {
+      lo = requant8<false>(make_uint2(c.x, c.y), p, ma_lo, sf_lo);
+      hi = requant8<false>(make_uint2(c.z, c.w), p, ma_hi, sf_hi);
+    }
+    const int64_t t = t0 + 16 * w + i;
+    if (col_ok && t < a.T)
+      __stcs(reinterpret_cast<uint4 *>(a.q + t * C + col), make_uint4(lo.x, lo.y, hi.x, hi.y));
+  }
+}
+
+template <bool kFp8Src, bool kGather>
+cudaError_t launch_src(const CastArgs &a, int channel_major, int gran_k, cudaStream_t stream) {
+  const dim3 grid(static_cast<unsigned>((a.T + kTileT - 1) / kTileT),
+                  static_cast<unsigned>((a.C + kTileC - 1) / kTileC));
   if (gran_k == 128) {
     if (channel_major)
-      quant_colblock_kernel<128, true><<<grid, 256, 0, stream>>>(xp, T, C, qp, sf);
+      cast_colblock_kernel<128, true, kFp8Src, kGather><<<grid, 256, 0, stream>>>(a);
     else
-      quant_colblock_kernel<128, false><<<grid, 256, 0, stream>>>(xp, T, C, qp, sf);
+      cast_colblock_kernel<128, false, kFp8Src, kGather><<<grid, 256, 0, stream>>>(a);
   } else {
     if (channel_major)
-      quant_colblock_kernel<32, true><<<grid, 256, 0, stream>>>(xp, T, C, qp, sf);
+      cast_colblock_kernel<32, true, kFp8Src, kGather><<<grid, 256, 0, stream>>>(a);
     else
-      quant_colblock_kernel<32, false><<<grid, 256, 0, stream>>>(xp, T, C, qp, sf);
+      cast_colblock_kernel<32, false, kFp8Src, kGather><<<grid, 256, 0, stream>>>(a);
   }
   return cudaGetLastError();
+}
+
+template <bool kGather>
+cudaError_t launch_requant_tm(const CastArgs &a, int gran_k, cudaStream_t stream) {
+  const dim3 grid(static_cast<unsigned>((a.T + kTileT - 1) / kTileT),
+                  static_cast<unsigned>((a.C + kRqTileC - 1) / kRqTileC));
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(requant_tm_kernel<128, kGather>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kRqSmem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(requant_tm_kernel<32, kGather>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, kRqSmem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  if (gran_k == 128)
+    requant_tm_kernel<128, kGather><<<grid, 256, kRqSmem, stream>>>(a);
+  else
+    requant_tm_kernel<32, kGather><<<grid, 256, kRqSmem, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_cast_colblock(const CastArgs &a, int channel_major, int gran_k,
+                                 cudaStream_t stream) {
+  const bool fp8 = (a.x_sf != nullptr);
+  const bool gather = (a.src_rows != nullptr);
+  if (fp8 && !channel_major)
+    return gather ? launch_requant_tm<true>(a, gran_k, stream)
+                  : launch_requant_tm<false>(a, gran_k, stream);
+  if (fp8)
+    return gather ? launch_src<true, true>(a, channel_major, gran_k, stream)
+                  : launch_src<true, false>(a, channel_major, gran_k, stream);
+  return gather ? launch_src<false, true>(a, channel_major, gran_k, stream)
+                : launch_src<false, false>(a, channel_major, gran_k, stream);
 }
 
 }  // namespace dg

@@ -82,8 +82,34 @@ cudaError_t launch_kgrouped_fp8(const WgradParams &p, int block_n, int pairs,
                                 cudaStream_t stream);
 cudaError_t launch_kgrouped_bf16(const WgradParams &p, int block_n, int pairs,
                                  cudaStream_t stream);
-cudaError_t launch_quant_colblock(const void *x, int64_t T, int C, void *q, uint8_t *sf,
-                                  int channel_major, int gran_k, cudaStream_t stream);
+// Column-block casts (quant.cu).  x is BF16 [T_src, C], or, with x_sf set,
+// E4M3 codes [T_src, C] with one UE8M0 scale per token per 128 channels
+// (x_sf [T_src, C / 128]).  With src_rows set, output row t takes source row
+// src_rows[t] (-1: a row of zeros); otherwise row t (T_src == T).
+struct CastArgs {
+  const void *x;
+  const uint8_t *x_sf;
+  const int *src_rows;
+  int64_t T_src, T;
+  int C;
+  uint8_t *q, *sf;
+  DevStatus *status;   // records DEV_BAD_ROW for a src_rows entry outside [-1, T_src)
+};
+cudaError_t launch_cast_colblock(const CastArgs &a, int channel_major, int gran_k,
+                                 cudaStream_t stream);
+
+// MoE layout plan (moe_layout.cu) from routing idx[n] (n = tokens x topk).
+struct MoePlanArgs {
+  const int *idx;
+  int64_t n;
+  int topk, G, align;
+  int *ks, *src_rows, *pair_rows;   // pair_rows may be null
+  int64_t cap;                      // rows of src_rows / pair_rows
+  void *scratch;                    // moe_plan_scratch_bytes(n, G), 16-byte aligned
+  DevStatus *status;                // records DEV_BAD_ROUTE for an entry outside [-1, G)
+};
+size_t moe_plan_scratch_bytes(int64_t n, int G);
+cudaError_t launch_moe_layout_plan(const MoePlanArgs &a, int sms, cudaStream_t stream);
 
 // Tile shape: a CTA pair covers 256 rows of M (128 per CTA) and block_n
 // columns of N.

@@ -15,7 +15,8 @@
  *
  * Conventions shared by every entry point
  * ---------------------------------------
- *  - Every pointer argument named a, b, sfa, sfb, d, c, x, q, sf, ks_dev is a
+ *  - Every pointer argument named a, b, sfa, sfb, d, c, x, x_sf, q_in, sf_in,
+ *    src_rows, pair_rows, topk_idx, ks, q, sf, ks_dev is a
  *    DEVICE pointer on the current CUDA device; ks_host is a HOST pointer.
  *  - All matrices are dense row-major with the last index contiguous (no
  *    padding between rows).  Device pointers must be 16-byte aligned.
@@ -25,7 +26,8 @@
  *    memory pool the library creates per device: allocated and freed in
  *    stream order on `stream` (cudaMallocFromPoolAsync / cudaFreeAsync), so
  *    calls on different streams never share it; the pool keeps freed blocks
- *    for reuse.  The BF16 GEMM and the cast allocate nothing per call.
+ *    for reuse.  dg_moe_layout_plan takes its counters from the same pool.
+ *    The BF16 GEMM and the casts allocate nothing per call.
  *  - Work is enqueued on `stream` (NULL = legacy default stream) and runs
  *    asynchronously.  ks_host is read during the call only; device buffers
  *    must stay valid until the enqueued work completes.
@@ -168,6 +170,110 @@ dg_status dg_quant_transpose_fp8(const void *x, int64_t T, int C,
                                  dg_stream_t stream);
 
 /*
+ * dg_requant_transpose_fp8 -- re-quantise stored FP8 activations for the
+ * weight gradient: from the forward pass's 1 x 128 tiles (one scale per token
+ * per 128 channels) to column blocks (one scale per channel per gran_k
+ * tokens), with the same cast as dg_quant_transpose_fp8 applied to the
+ * exactly dequantised values:
+ *
+ *   x[t, c] = E4M3(q_in[t, c]) * 2^(sf_in[t, c / 128] - 127)
+ *   (q, sf) = dg_quant_transpose_fp8 of x
+ *
+ * Source: "Is DeepGEMM directly applicable to backward in training?" (hxdtest,
+ * 4 May 2025, quoting the DeepSeek-V3 workflow: forward activations are
+ * stored as 1x128 FP8 tiles; the backward pass reads them out, dequantises,
+ * transposes and re-quantises them into 128x1 tiles; TheTinyTeddy, 12 Mar
+ * 2025: the FP8 weight-gradient GEMM lets activations be stored in FP8).  The
+ * pages do not give the stored scales' format; here they are UE8M0 bytes (the
+ * SM100 format of "UE8M0 Format in DeepGEMM").
+ *
+ *   q_in      E4M3 codes [T, C] (token-major, as the forward pass stored them).
+ *   sf_in     UE8M0 bytes [T, C / 128]; bytes 0..254 (255 is NaN: unsupported).
+ *   T         non-negative multiple of gran_k.
+ *   C         positive multiple of 128.
+ *   q, sf, q_layout, gran_k   as for dg_quant_transpose_fp8.
+ * Every dequantised value is exact in the kernel (it works on x * 2^-8, which
+ * is finite and exact in FP32 for every code and scale byte), so the result is
+ * bit-identical to the definition above.  Errors as for dg_quant_transpose_fp8.
+ */
+dg_status dg_requant_transpose_fp8(const void *q_in, const uint8_t *sf_in,
+                                   int64_t T, int C,
+                                   void *q, uint8_t *sf,
+                                   dg_layout q_layout, int gran_k,
+                                   dg_stream_t stream);
+
+/*
+ * dg_quant_moe_layout_fp8 -- the column-block cast fused with the MoE token
+ * layout: output row t is source row src_rows[t], or a row of zeros where
+ * src_rows[t] == -1 (padding an expert's slice up to whole 128-token blocks),
+ * then cast as by dg_quant_transpose_fp8 (BF16 source) or
+ * dg_requant_transpose_fp8 (stored FP8 source).
+ *
+ * Source: "Is DeepGEMM directly applicable to backward in training?"
+ * (LyricZhao, 26 Feb 2025: weight-gradient support needs utility kernels with
+ * the cast fused with the MoE layout; NiuMa, 18 Mar 2025: the FP8 weight
+ * gradient needs each expert's token count to be a multiple of 128).
+ *
+ *   x         x_sf == NULL: BF16 [T_src, C].  Otherwise E4M3 codes [T_src, C]
+ *             with x_sf UE8M0 [T_src, C / 128] (1 x 128 tiles, as for
+ *             dg_requant_transpose_fp8; C then a multiple of 128).
+ *   T_src     source rows (>= 0, < 2^31).
+ *   src_rows  device int32 [T]: source row of each output row, or -1.  An
+ *             entry outside [-1, T_src) gives a zero row and is recorded as
+ *             DG_ERR_INVALID_ARG in the device status word (dg_sync_check).
+ *   T         output rows: a non-negative multiple of gran_k (each expert's
+ *             slice is a whole number of blocks).
+ *   q, sf, q_layout, gran_k   as for dg_quant_transpose_fp8, over the T output
+ *             rows.
+ * Errors as for dg_quant_transpose_fp8.
+ */
+dg_status dg_quant_moe_layout_fp8(const void *x, const uint8_t *x_sf,
+                                  int64_t T_src, int C,
+                                  const int *src_rows, int64_t T,
+                                  void *q, uint8_t *sf,
+                                  dg_layout q_layout, int gran_k,
+                                  dg_stream_t stream);
+
+/*
+ * dg_moe_layout_plan -- the MoE token layout that dg_quant_moe_layout_fp8 and
+ * the K-grouped GEMMs consume, built on the device from top-k routing.
+ *
+ * Expert e's slice holds its routing pairs (t, j) (topk_idx[t, j] == e) in the
+ * order of the pair index t * topk + j, then -1 padding rows up to a multiple
+ * of `align`; the slices follow in expert order.  ks[e] is the slice's padded
+ * length, so ks feeds the GEMM's ks_dev directly (and, copied to the host, its
+ * ks_host).  Deterministic: the same routing always gives the same layout.
+ *
+ * Source: "Is DeepGEMM directly applicable to backward in training?"
+ * (LyricZhao, 26 Feb 2025: casts fused with the MoE layout; NiuMa, 18 Mar
+ * 2025: the FP8 weight gradient needs each expert's token count to be a
+ * multiple of 128, which padding provides).
+ *
+ *   topk_idx   device int32 [T_tok, topk]: the expert of each (token, slot),
+ *              or -1 for an unused slot.  An entry outside [-1, G) is skipped
+ *              and recorded as DG_ERR_INVALID_ARG in the device status word
+ *              (dg_sync_check).
+ *   T_tok      tokens (>= 0);  topk >= 1;  T_tok * topk + G * (align - 1) < 2^31.
+ *   G          experts, 1 <= G <= DG_MAX_GROUPS.
+ *   align      slice length multiple, 1..65536 (128 for the FP8 GEMM).
+ *   ks         device int32 [G] out.
+ *   src_rows   device int32 [cap] out: the source token t of each row, -1 on
+ *              padding and on every row past the layout's end.
+ *   pair_rows  device int32 [cap] out, or NULL: the pair index t * topk + j of
+ *              each row (for operands stored per routed pair), -1 likewise.
+ *   cap        rows of src_rows / pair_rows; at least T_tok * topk +
+ *              G * (align - 1), the largest layout any routing can give.
+ * Scratch: (ceil(T_tok * topk / 4096) + 1) * G int32 counters from the
+ * library's stream-ordered pool.  Errors: DG_ERR_INVALID_ARG (arguments,
+ * cap too small, NULL or misaligned pointers), DG_ERR_UNSUPPORTED (G above
+ * DG_MAX_GROUPS, sizes above the limit), DG_ERR_CUDA.
+ */
+dg_status dg_moe_layout_plan(const int *topk_idx, int64_t T_tok, int topk,
+                             int G, int align,
+                             int *ks, int *src_rows, int *pair_rows,
+                             int64_t cap, dg_stream_t stream);
+
+/*
  * dg_k_grouped_fp8_wgrad_noalloc -- dg_k_grouped_fp8_wgrad for callers that
  * cannot allocate device memory.  The pages have no counterpart: this is an
  * addition of this library.
@@ -208,7 +314,8 @@ const char *dg_last_error(void);
 /*
  * Synchronise `stream`, then read and clear the current device's status word.
  * Returns DG_ERR_TIMEOUT if a kernel gave up on a bounded wait,
- * DG_ERR_INVALID_ARG if a kernel found ks_dev different from ks_host,
+ * DG_ERR_INVALID_ARG if a kernel found ks_dev different from ks_host, a
+ * src_rows entry or a topk_idx entry out of range,
  * DG_ERR_CUDA if the synchronisation failed, else DG_OK.
  */
 dg_status dg_sync_check(dg_stream_t stream);

@@ -140,6 +140,74 @@ def test_quant_zero_tokens_is_ok(L):
     assert _quant(L, T=0) == B.DG_OK
 
 
+def _requant(L, **kw):
+    a = dict(q_in=FAKE, sf_in=FAKE, T=256, C=256, q=FAKE, sf=FAKE, lay=B.DG_TOKEN_MAJOR, g=128)
+    a.update(kw)
+    return L.dg_requant_transpose_fp8(a["q_in"], a["sf_in"], a["T"], a["C"], a["q"], a["sf"],
+                                      a["lay"], a["g"], None)
+
+
+@pytest.mark.parametrize("kw,why", [
+    (dict(C=64), "multiple of 128"),
+    (dict(T=96), "multiple of gran_k"),
+    (dict(sf_in=None), "sf_in is required"),
+    (dict(q_in=MIS), "16-byte aligned"),
+    (dict(g=64), "gran_k = 64"),
+])
+def test_requant_invalid_arguments(L, kw, why):
+    assert _requant(L, **kw) == B.DG_ERR_INVALID_ARG
+    assert why in L.dg_last_error().decode()
+
+
+def _moe(L, **kw):
+    a = dict(x=FAKE, x_sf=None, Ts=300, C=64, src=FAKE, T=256, q=FAKE, sf=FAKE,
+             lay=B.DG_TOKEN_MAJOR, g=128)
+    a.update(kw)
+    return L.dg_quant_moe_layout_fp8(a["x"], a["x_sf"], a["Ts"], a["C"], a["src"], a["T"],
+                                     a["q"], a["sf"], a["lay"], a["g"], None)
+
+
+@pytest.mark.parametrize("kw,why", [
+    (dict(src=None), "src_rows is required"),
+    (dict(Ts=-1), "T_src < 0"),
+    (dict(x_sf=FAKE), "multiple of 128"),          # FP8 source needs C % 128 == 0
+    (dict(T=130), "multiple of gran_k"),
+    (dict(src=MIS), "16-byte aligned"),
+    (dict(Ts=2 ** 31), "T_src above"),
+])
+def test_moe_layout_invalid_arguments(L, kw, why):
+    st = _moe(L, **kw)
+    assert st in (B.DG_ERR_INVALID_ARG, B.DG_ERR_UNSUPPORTED)
+    assert why in L.dg_last_error().decode()
+
+
+def test_casts_zero_rows_are_ok(L):
+    assert _requant(L, T=0, sf_in=None) == B.DG_OK
+    assert _moe(L, T=0, src=None) == B.DG_OK
+
+
+def _plan(L, **kw):
+    a = dict(idx=FAKE, T=100, k=2, G=8, al=128, ks=FAKE, src=FAKE, pair=None, cap=200 + 8 * 127)
+    a.update(kw)
+    return L.dg_moe_layout_plan(a["idx"], a["T"], a["k"], a["G"], a["al"], a["ks"], a["src"],
+                                a["pair"], a["cap"], None)
+
+
+@pytest.mark.parametrize("kw,why,st", [
+    (dict(cap=200 + 8 * 127 - 1), "cap = ", B.DG_ERR_INVALID_ARG),
+    (dict(G=0), "G = 0", B.DG_ERR_INVALID_ARG),
+    (dict(G=B.DG_MAX_GROUPS + 1, cap=10 ** 6), "G = 1025", B.DG_ERR_UNSUPPORTED),
+    (dict(k=0), "topk = 0", B.DG_ERR_INVALID_ARG),
+    (dict(al=0), "align = 0", B.DG_ERR_INVALID_ARG),
+    (dict(src=MIS), "16-byte aligned", B.DG_ERR_INVALID_ARG),
+    (dict(idx=None), "16-byte aligned", B.DG_ERR_INVALID_ARG),
+    (dict(T=2 ** 30, k=2, cap=2 ** 32), "above 2^31", B.DG_ERR_UNSUPPORTED),
+])
+def test_moe_plan_invalid_arguments(L, kw, why, st):
+    assert _plan(L, **kw) == st
+    assert why in L.dg_last_error().decode()
+
+
 def test_binding_raises_when_library_missing(monkeypatch, tmp_path):
     monkeypatch.setattr(B, "LIB_PATH", str(tmp_path / "missing.so"))
     monkeypatch.setattr(B, "_lib", None)
