@@ -16,6 +16,8 @@ Modules
            row-tile cast and its exact dequantisation (re-quantising stored
            FP8 activations); the MoE token layout (its plan from top-k
            routing, and the row gather with zero padding rows).
+``swiglu`` the SwiGLU backward of a MoE expert (dh = [dg | du] and the
+           recomputed activation a), cast by columns.
 ``wgrad``  the K-grouped GEMM ``D[e] = C[e] + A_e^T B_e`` with per-block
            scales, in float64, plus the tolerance budget ``S = sum |a b s|``.
 
@@ -28,6 +30,7 @@ from .quant import (  # noqa: F401
     scale_exponent, quant_colblock, quant_rowtile, dequant_rowtile, requant_colblock,
     gather_rows, moe_layout_cast, moe_layout_plan,
 )
+from .swiglu import sigmoid, swiglu_backward, swiglu_backward_cast  # noqa: F401
 from .wgrad import (  # noqa: F401
     dequant_colblock, kgrouped_fp8_wgrad, kgrouped_bf16_wgrad,
     kgrouped_fp8_wgrad_rows, kgrouped_bf16_wgrad_rows, expert_offsets,
