@@ -12,8 +12,11 @@ The same JSON line also carries:
                 fraction against the FP8 peak (2 x measured BF16);
   pipeline      the cast-inclusive step (BF16 dY, X -> dg_quant_transpose_fp8
                 x2 -> GEMM) on the same shapes, and the cast's own roofline;
-  casts         the re-quantisation of stored FP8 operands and the cast fused
-                with the MoE layout, each against the HBM roofline;
+  nt            the same GEMM with K-major operands (dg_k_grouped_fp8_wgrad_nt)
+                fed by the channel-major cast;
+  casts         the re-quantisation of stored FP8 operands, the cast fused
+                with the MoE layout and the cast fused with the SwiGLU
+                backward, each against the HBM roofline;
   e2e           the same metric through the C ABI with pinned host buffers:
                 H2D of the step's operands and D2H of the result D in the
                 timed region;
@@ -182,11 +185,12 @@ def moe_layout_rows(ks, t_tok: int, seed: int) -> np.ndarray:
 
 
 def measure_casts(w, ks, dev, stream, pk, steps):
-    """The two other casts of the path on the workload's operand shapes, each
+    """The other casts of the path on the workload's operand shapes, each
     against the HBM roofline: re-quantising stored FP8 (1 x 128 tiles, random
-    codes and scale bytes) of dY [sum_k, M] and X [sum_k, N]; and the BF16
-    cast of X fused with the MoE layout (each expert's rows gathered from
-    sum_k / 2 tokens)."""
+    codes and scale bytes) of dY [sum_k, M] and X [sum_k, N]; the BF16 cast of
+    X fused with the MoE layout (each expert's rows gathered from sum_k / 2
+    tokens); and the SwiGLU backward fused with the cast of dh [sum_k, M] and
+    of the activation [sum_k, M / 2]."""
     import grouped_fp8_weight_gb300 as dg
     gen = torch.Generator(device=dev).manual_seed(w.seed + 100)
     out = {}
@@ -231,6 +235,30 @@ def measure_casts(w, ks, dev, stream, pk, steps):
                          "bound": "hbm", "achieved": nb / (ms * 1e-3) / 1e9,
                          "peak": pk["hbm_gbs"], "unit": "GB/s",
                          "frac": nb / (ms * 1e-3) / 1e9 / pk["hbm_gbs"], "algorithmic_bytes": nb}
+    del x, q, sf, src
+
+    # SwiGLU backward fused with the cast: h = [g | u] [sum_k, M] and da
+    # [sum_k, M/2] (BF16) -> dh = [dg | du] (the A operand, [sum_k, M]) and the
+    # recomputed activation a [sum_k, M/2], both cast by columns.
+    T, I = w.sum_k, w.M // 2
+    h = torch.randn(T, 2 * I, generator=gen, device=dev).to(torch.bfloat16)
+    da = torch.randn(T, I, generator=gen, device=dev).to(torch.bfloat16)
+    q = torch.empty(T, 2 * I, dtype=torch.uint8, device=dev)
+    sf = torch.empty(T // 128, 2 * I, dtype=torch.uint8, device=dev)
+    qa = torch.empty(T, I, dtype=torch.uint8, device=dev)
+    sfa = torch.empty(T // 128, I, dtype=torch.uint8, device=dev)
+
+    def swiglu_cast():
+        dg.dg_swiglu_backward_quant_fp8(h, da, q, sf, qa, sfa)
+
+    for _ in range(3):
+        swiglu_cast()
+    ms = time_events(swiglu_cast, steps, stream)
+    nb = T * I * (2 * 2 + 2) + T * I * (2 + 1) + (T // 128) * I * 3
+    out["swiglu"] = {"ms": ms, "kernel": "swiglu_bwd_cast_kernel<128, with a>",
+                     "launches_per_step": 1, "T": T, "I": I, "bound": "hbm",
+                     "achieved": nb / (ms * 1e-3) / 1e9, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": nb / (ms * 1e-3) / 1e9 / pk["hbm_gbs"], "algorithmic_bytes": nb}
     return out
 
 
@@ -342,6 +370,15 @@ def run_ours(args):
     if w.kind != "fp8":
         raise SystemExit("bench.py times the FP8 workloads (moe_upgate_fp8_g32, moe_down_fp8_g32)")
     pk, pk_kind = peaks()
+    if args.profile_casts:
+        # the cast legs alone (no GEMM buffers), for kernel captures
+        ks = workloads.counts_for(w.name)
+        casts = measure_casts(w, ks, dev, torch.cuda.current_stream(), pk, args.steps)
+        dg.dg_sync_check()
+        if rank == 0:
+            print(json.dumps({"profile_only": True, "config": workload_config(w, ks),
+                              "casts": casts}), flush=True)
+        return 0
     ks, a_raw, b_raw, qa, sa, qb, sb = make_inputs(w, dev)
     ks_dev = torch.tensor(ks, dtype=torch.int32, device=dev)
     out_dt = torch.float32 if w.out_dtype == "f32" else torch.bfloat16
@@ -422,6 +459,28 @@ def run_ours(args):
                     "algorithmic_bytes": cast_bytes}}
     dg.dg_sync_check()
 
+    # ---- the same GEMM with K-major (NT) operands from the channel-major cast
+    qa_t = torch.empty(w.M, w.sum_k, dtype=torch.uint8, device=dev)
+    qb_t = torch.empty(w.N, w.sum_k, dtype=torch.uint8, device=dev)
+    dg.dg_quant_transpose_fp8(a_raw, qa_t, sa, "channel")
+    dg.dg_quant_transpose_fp8(b_raw, qb_t, sb, "channel")
+
+    def step_nt():
+        dg.dg_k_grouped_fp8_wgrad_nt(qa_t, sa, qb_t, sb, d, None, ks, ks_dev, 128)
+
+    for _ in range(3):
+        step_nt()
+    ms_nt = time_events(step_nt, max(5, args.steps // 4), stream)
+    nt = {"ms_per_step": ms_nt, "value": flops / (ms_nt * 1e-3) / 1e12, "unit": "TFLOP/s",
+          "kernel": "kgrouped_wgrad_kernel<fp8, 224, f32, K-major>",
+          "operands": "a [M, sum_k], b [N, sum_k] from the channel-major cast",
+          "hbm_frac": alg / (ms_nt * 1e-3) / 1e9 / pk["hbm_gbs"],
+          "tensor_frac": flops / (ms_nt * 1e-3) / 1e12 / fp8_peak}
+    del qa_t, qb_t
+    dg.dg_quant_transpose_fp8(a_raw, qa, sa)      # restore the token-major scales
+    dg.dg_quant_transpose_fp8(b_raw, qb, sb)
+    dg.dg_sync_check()
+
     casts = measure_casts(w, ks, dev, stream, pk, max(5, args.steps // 4))
     dg.dg_sync_check()
 
@@ -458,7 +517,7 @@ def run_ours(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "e4m3 x e4m3 -> f32", "data": "synthetic",
             "config": workload_config(w, ks), "fp8_peak_frac": tflops / fp8_peak,
-            "roofline": roof, "pipeline": pipeline, "casts": casts, "e2e": e2e,
+            "roofline": roof, "pipeline": pipeline, "nt": nt, "casts": casts, "e2e": e2e,
             "cpu_baseline": cpu,
             "clocks": clk.summary(),
             # per step: the scale-packing pass and the GEMM kernel
@@ -481,6 +540,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile", action="store_true",
                     help="device-timed leg only (for ncu captures)")
+    ap.add_argument("--profile-casts", action="store_true",
+                    help="the cast legs only, `--steps` launches each (for ncu captures)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

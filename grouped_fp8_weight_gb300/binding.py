@@ -31,11 +31,14 @@ SIGNATURES = {
                                     _IP, _IP, _I, _VP]),
     "dg_k_grouped_fp8_wgrad_noalloc": (_I, [_VP, _U8P, _VP, _U8P, _VP, _I, _FP, _I, _I, _I,
                                             _I64, _IP, _IP, _I, _VP]),
+    "dg_k_grouped_fp8_wgrad_nt": (_I, [_VP, _U8P, _VP, _U8P, _VP, _I, _FP, _I, _I, _I, _I64,
+                                       _IP, _IP, _I, _VP]),
     "dg_k_grouped_bf16_wgrad": (_I, [_VP, _VP, _VP, _I, _FP, _I, _I, _I, _I64, _IP, _IP, _VP]),
     "dg_quant_transpose_fp8": (_I, [_VP, _I64, _I, _VP, _U8P, _I, _I, _VP]),
     "dg_requant_transpose_fp8": (_I, [_VP, _U8P, _I64, _I, _VP, _U8P, _I, _I, _VP]),
     "dg_quant_moe_layout_fp8": (_I, [_VP, _U8P, _I64, _I, _IP, _I64, _VP, _U8P, _I, _I, _VP]),
     "dg_moe_layout_plan": (_I, [_IP, _I64, _I, _I, _I, _IP, _IP, _IP, _I64, _VP]),
+    "dg_swiglu_backward_quant_fp8": (_I, [_VP, _VP, _I64, _I, _VP, _U8P, _VP, _U8P, _I, _VP]),
     "dg_last_error": (ctypes.c_char_p, []),
     "dg_sync_check": (_I, [_VP]),
     "dg_version": (_I, []),
@@ -125,6 +128,34 @@ def dg_k_grouped_fp8_wgrad(a, sfa, b, sfb, d, c, ks_host, ks_dev, gran_k: int = 
         _dptr(a8), _dptr(sfa), _dptr(b8), _dptr(sfb), _dptr(d),
         DG_BF16 if d.dtype == torch.bfloat16 else DG_F32,
         _dptr(c), G, M, N, a8.shape[0], kh, _dptr(ks_dev), gran_k, _stream(stream)))
+
+
+def dg_k_grouped_fp8_wgrad_nt(a, sfa, b, sfb, d, c, ks_host, ks_dev, gran_k: int = 128,
+                              stream=None):
+    """As dg_k_grouped_fp8_wgrad with K-major operands a [M, sum_k], b [N, sum_k]."""
+    a8 = a.view(torch.uint8) if a.dtype != torch.uint8 else a
+    b8 = b.view(torch.uint8) if b.dtype != torch.uint8 else b
+    _need(a8, torch.uint8, "a", 2)
+    _need(b8, torch.uint8, "b", 2)
+    _need(sfa, torch.uint8, "sfa", 2)
+    _need(sfb, torch.uint8, "sfb", 2)
+    if d.dim() != 3 or d.dtype not in (torch.float32, torch.bfloat16) or not d.is_contiguous():
+        raise ValueError("d: expected contiguous float32/bfloat16 [G, M, N]")
+    G, M, N = d.shape
+    if a8.shape[0] != M or b8.shape[0] != N or a8.shape[1] != b8.shape[1]:
+        raise ValueError("operand shapes do not match d")
+    if c is not None and c is not d:
+        _need(c, torch.float32, "c", 3)
+        if tuple(c.shape) != tuple(d.shape):
+            raise ValueError("c must have d's shape")
+    _need(ks_dev, torch.int32, "ks_dev", 1)
+    kh, g = _ks_host(ks_host)
+    if g != G or ks_dev.numel() != G:
+        raise ValueError("ks must have G entries")
+    _check(lib().dg_k_grouped_fp8_wgrad_nt(
+        _dptr(a8), _dptr(sfa), _dptr(b8), _dptr(sfb), _dptr(d),
+        DG_BF16 if d.dtype == torch.bfloat16 else DG_F32,
+        _dptr(c), G, M, N, a8.shape[1], kh, _dptr(ks_dev), gran_k, _stream(stream)))
 
 
 def dg_k_grouped_bf16_wgrad(a, b, d, c, ks_host, ks_dev, stream=None):
@@ -233,6 +264,28 @@ def dg_moe_layout_plan(topk_idx, G: int, align: int = 128, with_pairs: bool = Fa
     _check(lib().dg_moe_layout_plan(_dptr(topk_idx), T_tok, topk, G, align, _dptr(ks),
                                     _dptr(src), _dptr(pair), cap, _stream(stream)))
     return (ks, src, pair) if with_pairs else (ks, src)
+
+
+def dg_swiglu_backward_quant_fp8(h, da, q_dh, sf_dh, q_a=None, sf_a=None, gran_k: int = 128,
+                                 stream=None):
+    """SwiGLU backward fused with the column-block cast: h bf16 [T, 2I] = [g | u],
+    da bf16 [T, I] -> q_dh [T, 2I] / sf_dh [T/gran_k, 2I] (dh = [dg | du]) and,
+    if given, q_a [T, I] / sf_a [T/gran_k, I] (a = silu(g) * u)."""
+    _need(h, torch.bfloat16, "h", 2)
+    _need(da, torch.bfloat16, "da", 2)
+    T, I2 = h.shape
+    I = I2 // 2
+    if I2 % 2 or tuple(da.shape) != (T, I):
+        raise ValueError("h must be [T, 2I] and da [T, I]")
+    q8 = q_dh.view(torch.uint8) if q_dh.dtype != torch.uint8 else q_dh
+    _check_out(q8, sf_dh, T, I2, "token", gran_k)
+    qa8 = None
+    if q_a is not None:
+        qa8 = q_a.view(torch.uint8) if q_a.dtype != torch.uint8 else q_a
+        _check_out(qa8, sf_a, T, I, "token", gran_k)
+    _check(lib().dg_swiglu_backward_quant_fp8(
+        _dptr(h), _dptr(da), T, I, _dptr(q8), _dptr(sf_dh), _dptr(qa8), _dptr(sf_a), gran_k,
+        _stream(stream)))
 
 
 def dg_last_error() -> str:

@@ -144,6 +144,7 @@ dg_status encode(CUtensorMap *m, CUtensorMapDataType dt, const void *ptr, int ra
 
 struct GroupedArgs {
   bool fp8;
+  bool kmajor;   // FP8 only: a [M, sum_k], b [N, sum_k] (NT) instead of [sum_k, M], [sum_k, N]
   const void *a, *b;
   const uint8_t *sfa, *sfb;
   void *d;
@@ -157,7 +158,8 @@ struct GroupedArgs {
 };
 
 dg_status run_grouped(const GroupedArgs &x) {
-  const char *fn = x.fp8 ? "dg_k_grouped_fp8_wgrad" : "dg_k_grouped_bf16_wgrad";
+  const char *fn = !x.fp8 ? "dg_k_grouped_bf16_wgrad"
+                   : x.kmajor ? "dg_k_grouped_fp8_wgrad_nt" : "dg_k_grouped_fp8_wgrad";
   // ---- validation (nothing is enqueued on failure)
   if (x.G < 0) return fail(DG_ERR_INVALID_ARG, "%s: G = %d < 0", fn, x.G);
   if (x.G > DG_MAX_GROUPS)
@@ -267,7 +269,18 @@ dg_status run_grouped(const GroupedArgs &x) {
   // ---- tensor maps
   const uint64_t M = x.M, N = x.N, G = x.G, SK = x.sum_k;
   if (p.num_mma_tiles > 0) {
-    if (x.fp8) {
+    if (x.fp8 && x.kmajor) {
+      // K-major: rows of sum_k bytes; one box = 128 tokens x 128 rows (A) or
+      // x bn / 2 rows (B), 128-byte swizzled.
+      const uint64_t da[2] = {SK, M}, db[2] = {SK, N}, st[1] = {SK};
+      const uint32_t box[2] = {128, 128};
+      const uint32_t boxb[2] = {128, static_cast<uint32_t>(bn / 2)};
+      if ((s = encode(&p.tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, x.a, 2, da, st, box,
+                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "a")) ||
+          (s = encode(&p.tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, x.b, 2, db, st, boxb,
+                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "b")))
+        return s;
+    } else if (x.fp8) {
       const uint64_t da[2] = {M, SK}, sa[1] = {M};
       const uint64_t db[2] = {N, SK}, sb[1] = {N};
       const uint32_t box[2] = {128, 128};
@@ -336,8 +349,9 @@ dg_status run_grouped(const GroupedArgs &x) {
 
   // ---- launch: one persistent CTA pair per two SMs (or per tile when fewer)
   const int pairs = std::min(dev->sms / 2, p.num_tiles);
-  e = x.fp8 ? dg::launch_kgrouped_fp8(p, bn, pairs, x.stream)
-            : dg::launch_kgrouped_bf16(p, bn, pairs, x.stream);
+  e = !x.fp8    ? dg::launch_kgrouped_bf16(p, bn, pairs, x.stream)
+      : x.kmajor ? dg::launch_kgrouped_fp8_nt(p, bn, pairs, x.stream)
+                 : dg::launch_kgrouped_fp8(p, bn, pairs, x.stream);
   if (scratch != nullptr) cudaFreeAsync(scratch, x.stream);   // after the GEMM in stream order
   if (e != cudaSuccess)
     return fail(DG_ERR_CUDA, "%s: launch failed: %s", fn, cudaGetErrorString(e));
@@ -395,16 +409,26 @@ dg_status dg_k_grouped_fp8_wgrad(const void *a, const uint8_t *sfa, const void *
                                  const uint8_t *sfb, void *d, dg_dtype d_dtype, const float *c,
                                  int G, int M, int N, int64_t sum_k, const int *ks_host,
                                  const int *ks_dev, int gran_k, dg_stream_t stream) {
-  GroupedArgs x{true, a, b, sfa, sfb, d, d_dtype, c, G, M, N, sum_k, ks_host, ks_dev, gran_k,
-                reinterpret_cast<cudaStream_t>(stream)};
+  GroupedArgs x{true, false, a, b, sfa, sfb, d, d_dtype, c, G, M, N, sum_k, ks_host, ks_dev,
+                gran_k, reinterpret_cast<cudaStream_t>(stream)};
+  return run_grouped(x);
+}
+
+dg_status dg_k_grouped_fp8_wgrad_nt(const void *a, const uint8_t *sfa, const void *b,
+                                    const uint8_t *sfb, void *d, dg_dtype d_dtype,
+                                    const float *c, int G, int M, int N, int64_t sum_k,
+                                    const int *ks_host, const int *ks_dev, int gran_k,
+                                    dg_stream_t stream) {
+  GroupedArgs x{true, true, a, b, sfa, sfb, d, d_dtype, c, G, M, N, sum_k, ks_host, ks_dev,
+                gran_k, reinterpret_cast<cudaStream_t>(stream)};
   return run_grouped(x);
 }
 
 dg_status dg_k_grouped_bf16_wgrad(const void *a, const void *b, void *d, dg_dtype d_dtype,
                                   const float *c, int G, int M, int N, int64_t sum_k,
                                   const int *ks_host, const int *ks_dev, dg_stream_t stream) {
-  GroupedArgs x{false, a, b, nullptr, nullptr, d, d_dtype, c, G, M, N, sum_k, ks_host, ks_dev,
-                0, reinterpret_cast<cudaStream_t>(stream)};
+  GroupedArgs x{false, false, a, b, nullptr, nullptr, d, d_dtype, c, G, M, N, sum_k, ks_host,
+                ks_dev, 0, reinterpret_cast<cudaStream_t>(stream)};
   return run_grouped(x);
 }
 
@@ -472,6 +496,38 @@ dg_status dg_moe_layout_plan(const int *topk_idx, int64_t T_tok, int topk, int G
                     dev->status};
   e = dg::launch_moe_layout_plan(a, dev->sms, st);
   cudaFreeAsync(scratch, st);   // after the plan's kernels in stream order
+  if (e != cudaSuccess)
+    return fail(DG_ERR_CUDA, "%s: launch failed: %s", fn, cudaGetErrorString(e));
+  return ok();
+}
+
+dg_status dg_swiglu_backward_quant_fp8(const void *h, const void *da, int64_t T, int I,
+                                       void *q_dh, uint8_t *sf_dh, void *q_a, uint8_t *sf_a,
+                                       int gran_k, dg_stream_t stream) {
+  const char *fn = "dg_swiglu_backward_quant_fp8";
+  if (gran_k != 32 && gran_k != 128)
+    return fail(DG_ERR_INVALID_ARG, "%s: gran_k = %d (must be 32 or 128)", fn, gran_k);
+  if (T < 0 || T % gran_k)
+    return fail(DG_ERR_INVALID_ARG, "%s: T = %lld must be a non-negative multiple of gran_k",
+                fn, (long long)T);
+  if (I <= 0 || I % 16)
+    return fail(DG_ERR_INVALID_ARG, "%s: I = %d must be a positive multiple of 16", fn, I);
+  if ((q_a == nullptr) != (sf_a == nullptr))
+    return fail(DG_ERR_INVALID_ARG, "%s: q_a and sf_a go together", fn);
+  if ((I + 127) / 128 > 65535 || (T + 127) / 128 > 0x7FFFFFFFll)
+    return fail(DG_ERR_UNSUPPORTED, "%s: T or I too large", fn);
+  if (T == 0) return ok();
+  if (h == nullptr || da == nullptr || q_dh == nullptr || sf_dh == nullptr || !aligned16(h) ||
+      !aligned16(da) || !aligned16(q_dh) || !aligned16(sf_dh) ||
+      (q_a != nullptr && (!aligned16(q_a) || !aligned16(sf_a))))
+    return fail(DG_ERR_INVALID_ARG, "%s: device pointers must be non-NULL and 16-byte aligned",
+                fn);
+  DeviceState *dev = nullptr;
+  dg_status s = device_state(&dev);
+  if (s != DG_OK) return s;
+  dg::SwigluArgs a{h, da, T, I, static_cast<uint8_t *>(q_dh), sf_dh,
+                   static_cast<uint8_t *>(q_a), sf_a};
+  cudaError_t e = dg::launch_swiglu_bwd_cast(a, gran_k, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess)
     return fail(DG_ERR_CUDA, "%s: launch failed: %s", fn, cudaGetErrorString(e));
   return ok();

@@ -50,8 +50,9 @@
 
 namespace dg {
 
-template <bool kFP8, int kBN>
+template <bool kFP8, int kBN, bool kKMajor = false>
 struct WgradCfg {
+  static_assert(!kKMajor || kFP8, "K-major operands: FP8 only");
   static constexpr int BM = 128;                        // rows per CTA (pair: 256)
   static constexpr int ELEM = kFP8 ? 1 : 2;
   static constexpr int BK = kFP8 ? 128 : 64;            // tokens per stage
@@ -63,20 +64,25 @@ struct WgradCfg {
   static constexpr int A_ATOMS = BM / ATOM;
   static constexpr int B_ATOMS = (BN_CTA + ATOM - 1) / ATOM;
   static constexpr int ATOM_BYTES = BK * 128;           // BK rows x 128 bytes
-  static constexpr int A_BYTES = A_ATOMS * ATOM_BYTES;
-  static constexpr int B_BYTES = B_ATOMS * ATOM_BYTES;
+  // MN-major tiles are BK token rows of 128-byte swizzle atoms; K-major tiles
+  // (NT operands, [M, sum_k] / [N, sum_k]) are BM or BN_CTA rows of BK bytes,
+  // 128-byte swizzled in groups of eight rows.
+  static constexpr int A_BYTES = kKMajor ? BM * BK * ELEM : A_ATOMS * ATOM_BYTES;
+  static constexpr int B_BYTES = kKMajor ? BN_CTA * BK * ELEM : B_ATOMS * ATOM_BYTES;
   // Bytes a stage's B loads bring in: each box is min(ATOM, BN_CTA) columns
   // wide, so a CTA's 112-column half of a 224-wide tile is loaded exactly
   // (its 128-byte swizzled rows keep their 128-byte pitch in shared memory).
   static constexpr int B_BOX_COLS = BN_CTA < ATOM ? BN_CTA : ATOM;
-  static constexpr int B_LOAD_BYTES = B_ATOMS * BK * B_BOX_COLS * ELEM;
-  static constexpr int KSTEP_BYTES = MMA_K * 128;
+  static constexpr int B_LOAD_BYTES = kKMajor ? B_BYTES : B_ATOMS * BK * B_BOX_COLS * ELEM;
+  // Descriptor start-address step of one MMA along K: MN-major, MMA_K token
+  // rows of 128 bytes; K-major, MMA_K elements inside the 128-byte row.
+  static constexpr int KSTEP_BYTES = kKMajor ? MMA_K * ELEM : MMA_K * 128;
   // Descriptor strides: SBO = 1024 (8 token rows x 128 B) between K groups,
   // LBO = ATOM_BYTES between 128-byte atoms along M/N.  A single-atom operand
   // never steps along M/N, so its LBO is set to the K-group stride as well.
   static constexpr int A_LBO = A_ATOMS > 1 ? ATOM_BYTES : 1024;
   static constexpr int B_LBO = B_ATOMS > 1 ? ATOM_BYTES : 1024;
-  static constexpr int STAGES = 5;
+  static constexpr int STAGES = kKMajor ? 6 : 5;   // K-major stages are 30 KB, MN-major 32 KB
   static constexpr int NUM_ACC = 2;
   // FP8 scale groups: four UE8M0 rows (four k-blocks at gran_k 128, the four
   // 32-token sub-blocks of one k-block at gran_k 32), in a ring of SF_SLOTS.
@@ -241,10 +247,10 @@ __device__ __forceinline__ int swz_chunk(int i, int row) {
 #define DG_TACC(slot, v)
 #endif
 
-template <bool kFP8, int kBN, int kOut>
+template <bool kFP8, int kBN, int kOut, bool kKMajor>
 __global__ void __launch_bounds__(kWgradThreads, 1)
     kgrouped_wgrad_kernel(const __grid_constant__ WgradParams p) {
-  using Cfg = WgradCfg<kFP8, kBN>;
+  using Cfg = WgradCfg<kFP8, kBN, kKMajor>;
   constexpr int S = Cfg::STAGES;
   constexpr int NS = Cfg::SF_SLOTS;
   extern __shared__ uint8_t smem_raw[];
@@ -356,6 +362,11 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
             for (int b = 0; b < Cfg::B_ATOMS; ++b)
               tma_load_2d_hint(sb + b * Cfg::ATOM_BYTES, &p.tmB, &tfull[s], nb + b * Cfg::ATOM, k,
                                keep);
+          } else if constexpr (kKMajor) {
+            // one box per operand: BK bytes of tokens x this CTA's rows
+            const uint32_t fbar = mapa_shared(smem_u32(&full[s]), 0);
+            tma_load_2d_pair(sa, &p.tmA, fbar, k, tc.m0, keep);
+            tma_load_2d_pair(sb, &p.tmB, fbar, k, nb, keep);
           } else {
             const uint32_t fbar = mapa_shared(smem_u32(&full[s]), 0);
 #pragma unroll
@@ -391,13 +402,19 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
       uint32_t ph = 0, gph = 0;
       uint32_t sfa_t = 0, sfb_t = 0;
       bool ok = true;
+      // K-major operands clear the two transpose bits (15: A, 16: B).
       constexpr uint32_t kIdescBase =
-          kFP8 ? idesc_mxf8(2 * Cfg::BM, kBN, 0, 0) : idesc_bf16(2 * Cfg::BM, kBN);
+          (kFP8 ? idesc_mxf8(2 * Cfg::BM, kBN, 0, 0) : idesc_bf16(2 * Cfg::BM, kBN)) &
+          (kKMajor ? ~((1u << 15) | (1u << 16)) : ~0u);
       // Descriptors of stage 0 / scale slot 0; later stages and k-steps add
       // their byte offset >> 4 to the start-address field (shared addresses
       // stay below 256 KB, so the field never carries out).
-      const uint64_t a_desc0 = smem_desc(smem_u32(smem + Cfg::OFF_A), Cfg::A_LBO, 1024, 2);
-      const uint64_t b_desc0 = smem_desc(smem_u32(smem + Cfg::OFF_B), Cfg::B_LBO, 1024, 2);
+      // K-major 128-byte swizzle: SBO = 1024 between groups of eight rows
+      // (the leading offset is unused there).
+      const uint64_t a_desc0 =
+          smem_desc(smem_u32(smem + Cfg::OFF_A), kKMajor ? 16 : Cfg::A_LBO, 1024, 2);
+      const uint64_t b_desc0 =
+          smem_desc(smem_u32(smem + Cfg::OFF_B), kKMajor ? 16 : Cfg::B_LBO, 1024, 2);
       const uint64_t uta_desc0 = smem_desc(smem_u32(smem + Cfg::OFF_UTA), 0, 128, 0);
       const uint64_t utb_desc0 = smem_desc(smem_u32(smem + Cfg::OFF_UTB), 0, 128, 0);
       uint64_t a_desc = a_desc0, b_desc = b_desc0;
@@ -760,10 +777,10 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
   }
 }
 
-template <bool kFP8, int kBN, int kOut>
+template <bool kFP8, int kBN, int kOut, bool kKMajor>
 cudaError_t launch_wgrad_variant(const WgradParams &p, int pairs, cudaStream_t stream) {
-  using Cfg = WgradCfg<kFP8, kBN>;
-  auto kern = kgrouped_wgrad_kernel<kFP8, kBN, kOut>;
+  using Cfg = WgradCfg<kFP8, kBN, kKMajor>;
+  auto kern = kgrouped_wgrad_kernel<kFP8, kBN, kOut, kKMajor>;
   static bool attr_set = false;
   static int max_pairs = 0;
   cudaLaunchAttribute attr[1];
@@ -793,13 +810,14 @@ cudaError_t launch_wgrad_variant(const WgradParams &p, int pairs, cudaStream_t s
   return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
-template <bool kFP8, int kBN>
+template <bool kFP8, int kBN, bool kKMajor = false>
 cudaError_t launch_wgrad_bn(const WgradParams &p, int pairs, cudaStream_t stream) {
   switch (p.out_mode) {
-    case OUT_F32: return launch_wgrad_variant<kFP8, kBN, OUT_F32>(p, pairs, stream);
-    case OUT_F32_REDUCE: return launch_wgrad_variant<kFP8, kBN, OUT_F32_REDUCE>(p, pairs, stream);
-    case OUT_F32_C: return launch_wgrad_variant<kFP8, kBN, OUT_F32_C>(p, pairs, stream);
-    case OUT_BF16: return launch_wgrad_variant<kFP8, kBN, OUT_BF16>(p, pairs, stream);
+    case OUT_F32: return launch_wgrad_variant<kFP8, kBN, OUT_F32, kKMajor>(p, pairs, stream);
+    case OUT_F32_REDUCE:
+      return launch_wgrad_variant<kFP8, kBN, OUT_F32_REDUCE, kKMajor>(p, pairs, stream);
+    case OUT_F32_C: return launch_wgrad_variant<kFP8, kBN, OUT_F32_C, kKMajor>(p, pairs, stream);
+    case OUT_BF16: return launch_wgrad_variant<kFP8, kBN, OUT_BF16, kKMajor>(p, pairs, stream);
   }
   return cudaErrorInvalidValue;
 }

@@ -82,6 +82,9 @@ cudaError_t launch_kgrouped_fp8(const WgradParams &p, int block_n, int pairs,
                                 cudaStream_t stream);
 cudaError_t launch_kgrouped_bf16(const WgradParams &p, int block_n, int pairs,
                                  cudaStream_t stream);
+// FP8 with K-major operands (tmA / tmB map [M, sum_k] / [N, sum_k]).
+cudaError_t launch_kgrouped_fp8_nt(const WgradParams &p, int block_n, int pairs,
+                                   cudaStream_t stream);
 // Column-block casts (quant.cu).  x is BF16 [T_src, C], or, with x_sf set,
 // E4M3 codes [T_src, C] with one UE8M0 scale per token per 128 channels
 // (x_sf [T_src, C / 128]).  With src_rows set, output row t takes source row
@@ -109,6 +112,17 @@ struct MoePlanArgs {
   DevStatus *status;                // records DEV_BAD_ROUTE for an entry outside [-1, G)
 };
 size_t moe_plan_scratch_bytes(int64_t n, int G);
+
+// SwiGLU backward fused with the column-block cast (swiglu.cu).
+struct SwigluArgs {
+  const void *h;        // BF16 [T, 2I] = [g | u]
+  const void *da;       // BF16 [T, I]
+  int64_t T;
+  int I;
+  uint8_t *q_dh, *sf_dh;   // E4M3 [T, 2I], UE8M0 [T / gran_k, 2I]
+  uint8_t *q_a, *sf_a;     // E4M3 [T, I], UE8M0 [T / gran_k, I], or null
+};
+cudaError_t launch_swiglu_bwd_cast(const SwigluArgs &p, int gran_k, cudaStream_t stream);
 cudaError_t launch_moe_layout_plan(const MoePlanArgs &a, int sms, cudaStream_t stream);
 
 // Tile shape: a CTA pair covers 256 rows of M (128 per CTA) and block_n

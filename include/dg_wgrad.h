@@ -16,7 +16,8 @@
  * Conventions shared by every entry point
  * ---------------------------------------
  *  - Every pointer argument named a, b, sfa, sfb, d, c, x, x_sf, q_in, sf_in,
- *    src_rows, pair_rows, topk_idx, ks, q, sf, ks_dev is a
+ *    src_rows, pair_rows, topk_idx, ks, h, da, q_dh, sf_dh, q_a, sf_a, q, sf,
+ *    ks_dev is a
  *    DEVICE pointer on the current CUDA device; ks_host is a HOST pointer.
  *  - All matrices are dense row-major with the last index contiguous (no
  *    padding between rows).  Device pointers must be 16-byte aligned.
@@ -120,6 +121,28 @@ dg_status dg_k_grouped_fp8_wgrad(const void *a, const uint8_t *sfa,
                                  int G, int M, int N, int64_t sum_k,
                                  const int *ks_host, const int *ks_dev,
                                  int gran_k, dg_stream_t stream);
+
+/*
+ * dg_k_grouped_fp8_wgrad_nt -- dg_k_grouped_fp8_wgrad with K-major (NT)
+ * operands: a is E4M3 [M, sum_k] and b is E4M3 [N, sum_k] (the token axis
+ * contiguous: the channel-major output of the casts, q [C, T]).  Everything
+ * else -- scales sfa [sum_k / gran_k, M] and sfb [sum_k / gran_k, N], d, c,
+ * ks, gran_k, errors, scratch -- is as for dg_k_grouped_fp8_wgrad, and the
+ * result is the same sum.
+ *
+ * Source: "How to Use DeepGEMM Weight Gradient Kernels for Training Backward
+ * Passes", section "API Entry Points" (k_grouped_fp8_gemm_nt_contiguous: A
+ * non-transposed [M, K], B transposed [N, K]); "Is DeepGEMM directly applicable
+ * to backward in training?" (qijiaxing, 26 Mar 2025: dy^T as A [h_out,
+ * tokens], x^T as B [h_in, tokens]; 3 Apr 2025: a contiguous K axis is the
+ * layout the NT form is built for).
+ */
+dg_status dg_k_grouped_fp8_wgrad_nt(const void *a, const uint8_t *sfa,
+                                    const void *b, const uint8_t *sfb,
+                                    void *d, dg_dtype d_dtype, const float *c,
+                                    int G, int M, int N, int64_t sum_k,
+                                    const int *ks_host, const int *ks_dev,
+                                    int gran_k, dg_stream_t stream);
 
 /*
  * dg_k_grouped_bf16_wgrad -- K-grouped weight gradient with BF16 operands and
@@ -272,6 +295,39 @@ dg_status dg_moe_layout_plan(const int *topk_idx, int64_t T_tok, int topk,
                              int G, int align,
                              int *ks, int *src_rows, int *pair_rows,
                              int64_t cap, dg_stream_t stream);
+
+/*
+ * dg_swiglu_backward_quant_fp8 -- the SwiGLU backward of a MoE expert fused
+ * with the column-block cast of its outputs, token-major:
+ *
+ *   h = [g | u] (gate half first), s = 1 / (1 + e^-g), silu(g) = g * s
+ *   dg = da * u * s * (1 + g * (1 - s)),  du = da * silu(g),  a = silu(g) * u
+ *   (q_dh, sf_dh) = cast of dh = [dg | du]   (the up/gate weight gradient's A)
+ *   (q_a, sf_a)   = cast of a                 (the down-projection's B)
+ * with the cast of dg_quant_transpose_fp8 (one UE8M0 scale per column per
+ * gran_k tokens).
+ *
+ * Source: "Is DeepGEMM directly applicable to backward in training?"
+ * (LyricZhao, 26 Feb 2025: weight-gradient support needs utility kernels,
+ * among them casting fused with SwiGLU).  The pages give no formula; this is
+ * the standard SwiGLU.
+ *
+ *   h       BF16 [T, 2I];  da  BF16 [T, I].
+ *   T       non-negative multiple of gran_k.   I  positive multiple of 16.
+ *   q_dh    E4M3 [T, 2I];  sf_dh  UE8M0 [T / gran_k, 2I].
+ *   q_a     E4M3 [T, I] and sf_a UE8M0 [T / gran_k, I], or both NULL.
+ *   gran_k  32 or 128.
+ * Arithmetic: FP32 with explicitly rounded operations, e^-|g| from expf and
+ * 1 / (1 + e^-|g|) from the hardware reciprocal (within 1 ulp); dg, du and a must stay finite in FP32
+ * (non-finite values are unsupported).  Each quantised code and scale is the
+ * one of a value within a few FP32 ulp of the exact result (the tests bound
+ * it).  Errors as for dg_quant_transpose_fp8.
+ */
+dg_status dg_swiglu_backward_quant_fp8(const void *h, const void *da,
+                                       int64_t T, int I,
+                                       void *q_dh, uint8_t *sf_dh,
+                                       void *q_a, uint8_t *sf_a,
+                                       int gran_k, dg_stream_t stream);
 
 /*
  * dg_k_grouped_fp8_wgrad_noalloc -- dg_k_grouped_fp8_wgrad for callers that

@@ -104,3 +104,36 @@ def assert_close(d_gpu, D, S, out="f32", what=""):
             f"{[tuple(i) for i in idx]}: got {got[bad][:5]}, want {D[bad][:5]}, "
             f"bound {bound[bad][:5]}")
     return float(err.max()) if err.size else 0.0
+
+
+def check_cast_bound(q, sf, X, B, gran_k=128, what="", max_ambiguous=1e-3):
+    """A GPU column-block cast (q, sf) of values the GPU computes in FP32, against
+    the oracle's float64 values X with elementwise error bounds B: each scale
+    byte must be the scale rule's for some block maximum of values within
+    X +- B, and each code the RNE E4M3 code of some value within the bound at
+    that scale.  Where the bound admits one decision only (all but a small
+    fraction of elements) this is an exact comparison."""
+    from oracle.e4m3 import e4m3_decode, e4m3_encode
+    from oracle.quant import scale_exponent
+    q = q.cpu().numpy() if isinstance(q, torch.Tensor) else np.asarray(q)
+    sf = sf.cpu().numpy() if isinstance(sf, torch.Tensor) else np.asarray(sf)
+    T, C = X.shape
+    nb = T // gran_k
+    Xb, Bb = X.reshape(nb, gran_k, C), B.reshape(nb, gran_k, C)
+    e_lo = scale_exponent(np.max(np.maximum(np.abs(Xb) - Bb, 0.0), axis=1))
+    e_hi = scale_exponent(np.max(np.abs(Xb) + Bb, axis=1))
+    e = sf.astype(np.int64) - 127
+    bad = ~((e_lo <= e) & (e <= e_hi))
+    assert not bad.any(), f"{what}: scale bytes out of bound at {np.argwhere(bad)[:5]}"
+    scale = np.repeat(np.ldexp(1.0, -e), gran_k, axis=0)
+    v_lo = e4m3_decode(e4m3_encode((X - B) * scale))
+    v_hi = e4m3_decode(e4m3_encode((X + B) * scale))
+    v = e4m3_decode(q)
+    bad = ~((v_lo <= v) & (v <= v_hi))
+    if bad.any():
+        i = tuple(np.argwhere(bad)[0])
+        raise AssertionError(f"{what}: {int(bad.sum())} codes out of bound; first {i}: got "
+                             f"{v[i]}, allowed [{v_lo[i]}, {v_hi[i]}], x = {X[i]} +- {B[i]}")
+    amb = float(np.mean(v_lo != v_hi))
+    assert amb <= max_ambiguous, f"{what}: {amb:.2e} of the codes are undecided by the bound"
+    return amb

@@ -74,6 +74,13 @@ def test_fp8_invalid_arguments(L, kw, why):
     assert why in L.dg_last_error().decode()
 
 
+def test_fp8_nt_invalid_arguments(L):
+    st = L.dg_k_grouped_fp8_wgrad_nt(FAKE, FAKE, FAKE, FAKE, FAKE, B.DG_F32, None, 2, 128, 100,
+                                     256, _ks([128, 128]), FAKE, 128, None)
+    assert st == B.DG_ERR_INVALID_ARG
+    assert "dg_k_grouped_fp8_wgrad_nt" in L.dg_last_error().decode()
+
+
 def test_fp8_group_limit(L):
     ks = [0] * (B.DG_MAX_GROUPS + 1)
     assert _fp8(L, G=len(ks), ks=ks, sk=0) == B.DG_ERR_UNSUPPORTED
@@ -205,6 +212,25 @@ def _plan(L, **kw):
 ])
 def test_moe_plan_invalid_arguments(L, kw, why, st):
     assert _plan(L, **kw) == st
+    assert why in L.dg_last_error().decode()
+
+
+def _sg(L, **kw):
+    a = dict(h=FAKE, da=FAKE, T=256, I=64, q=FAKE, sf=FAKE, qa=None, sfa=None, g=128)
+    a.update(kw)
+    return L.dg_swiglu_backward_quant_fp8(a["h"], a["da"], a["T"], a["I"], a["q"], a["sf"],
+                                          a["qa"], a["sfa"], a["g"], None)
+
+
+@pytest.mark.parametrize("kw,why", [
+    (dict(I=24), "multiple of 16"),
+    (dict(T=100), "multiple of gran_k"),
+    (dict(g=64), "gran_k = 64"),
+    (dict(qa=FAKE), "go together"),
+    (dict(da=MIS), "16-byte aligned"),
+])
+def test_swiglu_invalid_arguments(L, kw, why):
+    assert _sg(L, **kw) == B.DG_ERR_INVALID_ARG
     assert why in L.dg_last_error().decode()
 
 
