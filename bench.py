@@ -218,7 +218,9 @@ def measure_casts(w, ks, dev, stream, pk, steps):
     del bufs
 
     t_tok = w.sum_k // 2
-    src = torch.from_numpy(moe_layout_rows(ks, t_tok, w.seed + 101)).to(dev)
+    src_h = moe_layout_rows(ks, t_tok, w.seed + 101)
+    uniq = int(np.unique(src_h).size)        # source rows read at least once
+    src = torch.from_numpy(src_h).to(dev)
     x = torch.randn(t_tok, w.N, generator=gen, device=dev).to(torch.bfloat16)
     q = torch.empty(w.sum_k, w.N, dtype=torch.uint8, device=dev)
     sf = torch.empty(w.sum_k // 128, w.N, dtype=torch.uint8, device=dev)
@@ -229,9 +231,12 @@ def measure_casts(w, ks, dev, stream, pk, steps):
     for _ in range(3):
         layout_cast()
     ms = time_events(layout_cast, steps, stream)
-    nb = w.sum_k * w.N * 3 + w.sum_k * 4 + (w.sum_k // 128) * w.N
+    # each distinct source row read once (a row gathered into several experts'
+    # slices is re-read from L2), each output row written once
+    nb = uniq * w.N * 2 + w.sum_k * w.N + w.sum_k * 4 + (w.sum_k // 128) * w.N
     out["moe_layout"] = {"ms": ms, "kernel": "cast_colblock_kernel<128, token, bf16, gather>",
                          "launches_per_step": 1, "source_tokens": t_tok, "rows": w.sum_k,
+                         "distinct_source_rows": uniq,
                          "bound": "hbm", "achieved": nb / (ms * 1e-3) / 1e9,
                          "peak": pk["hbm_gbs"], "unit": "GB/s",
                          "frac": nb / (ms * 1e-3) / 1e9 / pk["hbm_gbs"], "algorithmic_bytes": nb}
