@@ -235,12 +235,21 @@ dg_status run_grouped(const GroupedArgs &x) {
     p.sched[i].k_off = static_cast<int>(off[e]);
     p.sched[i].k_len = x.ks_host[e];
   }
-  const int bn = x.fp8 ? dg::fp8_pick_block_n(x.N) : dg::bf16_pick_block_n(x.N);
-  p.M = x.M;
-  p.N = x.N;
+  // FP8 with N not a multiple of 224 but M one (the down-projection's 7168 x
+  // 2048): compute D^T tiles instead, so that the 224-wide tile runs along M
+  // with no ragged edge and the 256-row side along N.
+  const bool trans = x.fp8 && (x.N % 224 != 0) && (x.M % 224 == 0);
+  const int Mk = trans ? x.N : x.M, Nk = trans ? x.M : x.N;   // the kernel's M and N
+  const void *ka = trans ? x.b : x.a;
+  const void *kb = trans ? x.a : x.b;
+  const uint8_t *ksfa = trans ? x.sfb : x.sfa;
+  const uint8_t *ksfb = trans ? x.sfa : x.sfb;
+  const int bn = x.fp8 ? dg::fp8_pick_block_n(Nk) : dg::bf16_pick_block_n(Nk);
+  p.M = Mk;
+  p.N = Nk;
   p.G = x.G;
-  p.m_tiles = (x.M + dg::kPairM - 1) / dg::kPairM;
-  p.n_tiles = (x.N + bn - 1) / bn;
+  p.m_tiles = (Mk + dg::kPairM - 1) / dg::kPairM;
+  p.n_tiles = (Nk + bn - 1) / bn;
   p.tiles_per_group = p.m_tiles * p.n_tiles;
   p.num_mma_tiles = n_mma * p.tiles_per_group;
   p.num_tiles = n_groups * p.tiles_per_group;
@@ -249,7 +258,7 @@ dg_status run_grouped(const GroupedArgs &x) {
   // Sweep the smaller operand's tiles fastest: the concurrently running tiles
   // then share the larger operand's slices, and the smaller one stays in L2
   // from one sweep to the next.
-  p.m_fastest = (x.M <= x.N) ? 1 : 0;
+  p.m_fastest = (Mk <= Nk) ? 1 : 0;
   p.out_mode = (x.d_dtype == DG_BF16) ? dg::OUT_BF16
                : (x.c == nullptr)     ? dg::OUT_F32
                : (x.c == x.d)         ? dg::OUT_F32_REDUCE
@@ -266,30 +275,31 @@ dg_status run_grouped(const GroupedArgs &x) {
   std::memset(&pk, 0, sizeof(pk));
   const size_t sf_bytes = (x.fp8 && n_mma > 0) ? dg::plan_scale_pack(p, pk, n_mma, x.gran_k, bn) : 0;
 
-  // ---- tensor maps
+  // ---- tensor maps (operands in the kernel's roles; D and C as the caller's)
   const uint64_t M = x.M, N = x.N, G = x.G, SK = x.sum_k;
+  const uint64_t MK = Mk, NK = Nk;
   if (p.num_mma_tiles > 0) {
     if (x.fp8 && x.kmajor) {
       // K-major: rows of sum_k bytes; one box = 128 tokens x 128 rows (A) or
       // x bn / 2 rows (B), 128-byte swizzled.
-      const uint64_t da[2] = {SK, M}, db[2] = {SK, N}, st[1] = {SK};
+      const uint64_t da[2] = {SK, MK}, db[2] = {SK, NK}, st[1] = {SK};
       const uint32_t box[2] = {128, 128};
       const uint32_t boxb[2] = {128, static_cast<uint32_t>(bn / 2)};
-      if ((s = encode(&p.tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, x.a, 2, da, st, box,
+      if ((s = encode(&p.tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, ka, 2, da, st, box,
                       CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "a")) ||
-          (s = encode(&p.tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, x.b, 2, db, st, boxb,
+          (s = encode(&p.tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, kb, 2, db, st, boxb,
                       CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "b")))
         return s;
     } else if (x.fp8) {
-      const uint64_t da[2] = {M, SK}, sa[1] = {M};
-      const uint64_t db[2] = {N, SK}, sb[1] = {N};
+      const uint64_t da[2] = {MK, SK}, sa[1] = {MK};
+      const uint64_t db[2] = {NK, SK}, sb[1] = {NK};
       const uint32_t box[2] = {128, 128};
       // B: one box per CTA covers its bn / 2 columns (<= one 128-byte atom)
       const uint32_t boxb[2] = {static_cast<uint32_t>(std::min(128, bn / 2)), 128};
-      if ((s = encode(&p.tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, x.a, 2, da, sa, box,
+      if ((s = encode(&p.tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, ka, 2, da, sa, box,
                       CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "a")))
         return s;
-      s = encode(&p.tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, x.b, 2, db, sb, boxb,
+      s = encode(&p.tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, kb, 2, db, sb, boxb,
                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "b");
       if (s) return s;
       // The packed scale records are mapped (and the scratch taken) below,
@@ -329,7 +339,7 @@ dg_status run_grouped(const GroupedArgs &x) {
     if ((e = cudaMallocFromPoolAsync(&scratch, sf_bytes, dev->pool, x.stream)) != cudaSuccess)
       return fail(DG_ERR_CUDA, "%s: scale scratch (%zu bytes): %s", fn, sf_bytes,
                   cudaGetErrorString(e));
-    dg::bind_scale_pack(pk, scratch, x.sfa, x.sfb);
+    dg::bind_scale_pack(pk, scratch, ksfa, ksfb);
     const uint64_t rec[1] = {512};
     const uint64_t dpa[2] = {128, static_cast<uint64_t>(pk.n_groups) * pk.MC};
     const uint64_t dpb[2] = {128, static_cast<uint64_t>(pk.n_groups) * pk.NT * pk.CB};
@@ -349,9 +359,11 @@ dg_status run_grouped(const GroupedArgs &x) {
 
   // ---- launch: one persistent CTA pair per two SMs (or per tile when fewer)
   const int pairs = std::min(dev->sms / 2, p.num_tiles);
-  e = !x.fp8    ? dg::launch_kgrouped_bf16(p, bn, pairs, x.stream)
-      : x.kmajor ? dg::launch_kgrouped_fp8_nt(p, bn, pairs, x.stream)
-                 : dg::launch_kgrouped_fp8(p, bn, pairs, x.stream);
+  e = !x.fp8              ? dg::launch_kgrouped_bf16(p, bn, pairs, x.stream)
+      : x.kmajor && trans  ? dg::launch_kgrouped_fp8_nt_t(p, bn, pairs, x.stream)
+      : x.kmajor           ? dg::launch_kgrouped_fp8_nt(p, bn, pairs, x.stream)
+      : trans              ? dg::launch_kgrouped_fp8_t(p, bn, pairs, x.stream)
+                           : dg::launch_kgrouped_fp8(p, bn, pairs, x.stream);
   if (scratch != nullptr) cudaFreeAsync(scratch, x.stream);   // after the GEMM in stream order
   if (e != cudaSuccess)
     return fail(DG_ERR_CUDA, "%s: launch failed: %s", fn, cudaGetErrorString(e));

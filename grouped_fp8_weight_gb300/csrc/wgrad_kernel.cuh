@@ -247,7 +247,7 @@ __device__ __forceinline__ int swz_chunk(int i, int row) {
 #define DG_TACC(slot, v)
 #endif
 
-template <bool kFP8, int kBN, int kOut, bool kKMajor>
+template <bool kFP8, int kBN, int kOut, bool kKMajor, bool kTransD>
 __global__ void __launch_bounds__(kWgradThreads, 1)
     kgrouped_wgrad_kernel(const __grid_constant__ WgradParams p) {
   using Cfg = WgradCfg<kFP8, kBN, kKMajor>;
@@ -677,9 +677,14 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
         if (lane == 0) bulk_wait_read<Cfg::EPI_BUFS - 1>();   // the store that last used stg is done reading
         __syncwarp();
         DG_TACC(2, w1);
+        // Output box: 32 rows x EC columns of D, or (transposed tiles) the
+        // box whose rows are this chunk's EC columns and whose columns are
+        // this warp's 32 rows.
+        const int bx = kTransD ? row0 : tc.n0 + EC * c;
+        const int by = kTransD ? tc.n0 + EC * c : row0;
         if (kHasC && lane == 0) {
           mbar_arrive_expect_tx(&wcbar[sbuf], 32 * EC * 4);
-          tma_load_3d(stg, &p.tmC, &wcbar[sbuf], tc.n0 + EC * c, row0, tc.expert);
+          tma_load_3d(stg, &p.tmC, &wcbar[sbuf], bx, by, tc.expert);
         }
         float v[EC];
         if (mma_tile) {
@@ -708,17 +713,40 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
           cuse[sbuf]++;
           ok = __all_sync(0xffffffffu, ok);
           if (!ok) break;
-          const uint8_t *rowp = stg + lane * (EC * 4);
+          if constexpr (kTransD) {
+            // element (row i, column lane) of the staged FP32 box
 #pragma unroll
-          for (int i = 0; i < EC / 4; ++i) {
-            const float4 cv = *reinterpret_cast<const float4 *>(rowp + (swz_chunk<EC * 4>(i, lane) << 4));
-            v[4 * i + 0] += cv.x;
-            v[4 * i + 1] += cv.y;
-            v[4 * i + 2] += cv.z;
-            v[4 * i + 3] += cv.w;
+            for (int i = 0; i < EC; ++i)
+              v[i] += *reinterpret_cast<const float *>(
+                  stg + i * (32 * 4) + (swz_chunk<32 * 4>(lane >> 2, i) << 4) + (lane & 3) * 4);
+          } else {
+            const uint8_t *rowp = stg + lane * (EC * 4);
+#pragma unroll
+            for (int i = 0; i < EC / 4; ++i) {
+              const float4 cv = *reinterpret_cast<const float4 *>(rowp + (swz_chunk<EC * 4>(i, lane) << 4));
+              v[4 * i + 0] += cv.x;
+              v[4 * i + 1] += cv.y;
+              v[4 * i + 2] += cv.z;
+              v[4 * i + 3] += cv.w;
+            }
           }
         }
-        if constexpr (kOut == OUT_BF16) {
+        if constexpr (kTransD) {
+          // Transposed tile: register i of lane l is D[row i of the box][column l];
+          // each i writes one staged row (a warp-wide contiguous row, swizzled).
+          static_assert(EC == 32, "transposed boxes are 32 x 32");
+          if constexpr (kOut == OUT_BF16) {
+#pragma unroll
+            for (int i = 0; i < EC; ++i)
+              *reinterpret_cast<__nv_bfloat16 *>(stg + i * 64 + (swz_chunk<64>(lane >> 3, i) << 4) +
+                                                 (lane & 7) * 2) = __float2bfloat16_rn(v[i]);
+          } else {
+#pragma unroll
+            for (int i = 0; i < EC; ++i)
+              *reinterpret_cast<float *>(stg + i * 128 + (swz_chunk<128>(lane >> 2, i) << 4) +
+                                         (lane & 3) * 4) = v[i];
+          }
+        } else if constexpr (kOut == OUT_BF16) {
           uint8_t *rowp = stg + lane * (EC * 2);
 #pragma unroll
           for (int i = 0; i < EC / 8; ++i) {
@@ -743,9 +771,9 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
         __syncwarp();
         if (lane == 0) {
           if constexpr (kOut == OUT_F32_REDUCE)
-            tma_reduce_add_3d_hint(&p.tmD, stg, tc.n0 + EC * c, row0, tc.expert, stream_out);
+            tma_reduce_add_3d_hint(&p.tmD, stg, bx, by, tc.expert, stream_out);
           else
-            tma_store_3d_hint(&p.tmD, stg, tc.n0 + EC * c, row0, tc.expert, stream_out);
+            tma_store_3d_hint(&p.tmD, stg, bx, by, tc.expert, stream_out);
           bulk_commit();
         }
       }
@@ -777,10 +805,10 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
   }
 }
 
-template <bool kFP8, int kBN, int kOut, bool kKMajor>
+template <bool kFP8, int kBN, int kOut, bool kKMajor, bool kTransD>
 cudaError_t launch_wgrad_variant(const WgradParams &p, int pairs, cudaStream_t stream) {
   using Cfg = WgradCfg<kFP8, kBN, kKMajor>;
-  auto kern = kgrouped_wgrad_kernel<kFP8, kBN, kOut, kKMajor>;
+  auto kern = kgrouped_wgrad_kernel<kFP8, kBN, kOut, kKMajor, kTransD>;
   static bool attr_set = false;
   static int max_pairs = 0;
   cudaLaunchAttribute attr[1];
@@ -810,14 +838,19 @@ cudaError_t launch_wgrad_variant(const WgradParams &p, int pairs, cudaStream_t s
   return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
-template <bool kFP8, int kBN, bool kKMajor = false>
+// kTransD: the kernel computes D^T tiles (the host passes B as the kernel's A
+// and A as its B, with M and N swapped) and writes them transposed into D.
+template <bool kFP8, int kBN, bool kKMajor = false, bool kTransD = false>
 cudaError_t launch_wgrad_bn(const WgradParams &p, int pairs, cudaStream_t stream) {
   switch (p.out_mode) {
-    case OUT_F32: return launch_wgrad_variant<kFP8, kBN, OUT_F32, kKMajor>(p, pairs, stream);
+    case OUT_F32:
+      return launch_wgrad_variant<kFP8, kBN, OUT_F32, kKMajor, kTransD>(p, pairs, stream);
     case OUT_F32_REDUCE:
-      return launch_wgrad_variant<kFP8, kBN, OUT_F32_REDUCE, kKMajor>(p, pairs, stream);
-    case OUT_F32_C: return launch_wgrad_variant<kFP8, kBN, OUT_F32_C, kKMajor>(p, pairs, stream);
-    case OUT_BF16: return launch_wgrad_variant<kFP8, kBN, OUT_BF16, kKMajor>(p, pairs, stream);
+      return launch_wgrad_variant<kFP8, kBN, OUT_F32_REDUCE, kKMajor, kTransD>(p, pairs, stream);
+    case OUT_F32_C:
+      return launch_wgrad_variant<kFP8, kBN, OUT_F32_C, kKMajor, kTransD>(p, pairs, stream);
+    case OUT_BF16:
+      return launch_wgrad_variant<kFP8, kBN, OUT_BF16, kKMajor, kTransD>(p, pairs, stream);
   }
   return cudaErrorInvalidValue;
 }

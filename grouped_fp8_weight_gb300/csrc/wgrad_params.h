@@ -85,6 +85,12 @@ cudaError_t launch_kgrouped_bf16(const WgradParams &p, int block_n, int pairs,
 // FP8 with K-major operands (tmA / tmB map [M, sum_k] / [N, sum_k]).
 cudaError_t launch_kgrouped_fp8_nt(const WgradParams &p, int block_n, int pairs,
                                    cudaStream_t stream);
+// Transposed output tiles (the kernel's A is the caller's B, its M the
+// caller's N; D and C maps keep the caller's [G, M, N]); block_n 224 only.
+cudaError_t launch_kgrouped_fp8_t(const WgradParams &p, int block_n, int pairs,
+                                  cudaStream_t stream);
+cudaError_t launch_kgrouped_fp8_nt_t(const WgradParams &p, int block_n, int pairs,
+                                     cudaStream_t stream);
 // Column-block casts (quant.cu).  x is BF16 [T_src, C], or, with x_sf set,
 // E4M3 codes [T_src, C] with one UE8M0 scale per token per 128 channels
 // (x_sf [T_src, C / 128]).  With src_rows set, output row t takes source row

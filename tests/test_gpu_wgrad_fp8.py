@@ -188,3 +188,46 @@ def test_full_size_upgate_sampled():
 @pytest.mark.slow
 def test_full_size_down_bf16_sampled():
     _full_size_sampled("moe_down_fp8_g32", "bf16")
+
+
+@pytest.mark.parametrize("gran_k", [128, 32])
+@pytest.mark.parametrize("out,c_mode", [("f32", "none"), ("f32", "inplace"),
+                                        ("f32", "separate"), ("bf16", "none")])
+def test_transposed_tiles_modes(gran_k, out, c_mode):
+    """M a multiple of 224 and N not (the down-projection's orientation): the
+    library computes D^T tiles and writes them transposed."""
+    ks = [256, 0, 384, 128]
+    M, N = 448, 272
+    qa, sa, qb, sb = _case(ks, M, N, 13, gran_k, scale_noise=True)
+    C = workloads.randn((len(ks), M, N), 98).numpy()
+    d = run_fp8(qa, sa, qb, sb, ks, gran_k, out, C if c_mode != "none" else None, c_mode)
+    D, S = oracle.kgrouped_fp8_wgrad(qa, sa, qb, sb, ks, gran_k,
+                                     C if c_mode != "none" else None)
+    assert_close(d, D, S, out, what=f"transposed {out}/{c_mode}/g{gran_k}")
+    if c_mode == "inplace":
+        assert torch.equal(d[1].cpu(), torch.from_numpy(C[1]))
+    if c_mode == "none":
+        assert torch.count_nonzero(d[1]).item() == 0
+
+
+@pytest.mark.parametrize("M,N", [(224, 16), (672, 2048 // 8), (224 * 5, 80)])
+def test_transposed_tiles_shapes(M, N):
+    ks = [128, 256, 0, 128]
+    qa, sa, qb, sb = _case(ks, M, N, M + 3 * N)
+    d = run_fp8(qa, sa, qb, sb, ks, 128, "bf16")
+    D, S = oracle.kgrouped_fp8_wgrad(qa, sa, qb, sb, ks, 128)
+    assert_close(d, D, S, "bf16", what=f"transposed {M}x{N}")
+
+
+def test_transposed_tiles_lanes():
+    """Long and short experts across several tiles per CTA pair, transposed."""
+    ks = [128 * 60, 128 * 17, 0, 128 * 3, 128]
+    M, N = 2240, 1024
+    qa, sa, qb, sb = _case(ks, M, N, 23, 128, scale_noise=True)
+    d = run_fp8(qa, sa, qb, sb, ks, 128, "bf16")
+    rows = np.sort(np.random.default_rng(23).choice(M, 24, replace=False))
+    part = oracle.kgrouped_fp8_wgrad_rows(qa, sa, qb, sb, ks, rows, 128)
+    dr = d[:, torch.from_numpy(rows).to(DEV)].float().cpu().double().numpy()
+    for e, (De, Se) in part.items():
+        assert_close(dr[e], De, Se, "bf16", what=f"transposed lanes expert {e}")
+    assert torch.count_nonzero(d[2]).item() == 0

@@ -140,3 +140,15 @@ def test_nt_full_size_upgate_sampled():
     dr = d[:, torch.from_numpy(rows).to(DEV)].double().cpu().numpy()
     for e, (De, Se) in part.items():
         assert_close(dr[e], De, Se, what=f"nt {name} expert {e}")
+
+
+@pytest.mark.parametrize("out,c_mode", [("f32", "none"), ("f32", "inplace"), ("bf16", "none")])
+def test_nt_transposed_tiles(out, c_mode):
+    """K-major operands with M a multiple of 224 and N not: transposed tiles."""
+    ks = [256, 0, 384, 128]
+    M, N = 448, 272
+    qa, sa, qb, sb = _case(ks, M, N, 17, 128, scale_noise=True)
+    C = workloads.randn((len(ks), M, N), 97).numpy()
+    d = run_nt(qa, sa, qb, sb, ks, 128, out, C if c_mode != "none" else None, c_mode)
+    D, S = oracle.kgrouped_fp8_wgrad(qa, sa, qb, sb, ks, 128, C if c_mode != "none" else None)
+    assert_close(d, D, S, out, what=f"nt transposed {out}/{c_mode}")
