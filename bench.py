@@ -267,6 +267,52 @@ def measure_casts(w, ks, dev, stream, pk, steps):
     return out
 
 
+def profile_inplace(w, args, dev, pk, rank):
+    """Device-timed leg of the in-place workloads: the BF16 fine-grained GEMM
+    (BF16 operands, D += A^T B) or the pipeline's FP8 GEMM (operands cast from
+    BF16 draws by the library's cast, D += A^T B), inputs drawn on the device."""
+    import grouped_fp8_weight_gb300 as dg
+    ks, A, B, C = workloads.draw_operands(w.name, device=str(dev))
+    ks_dev = torch.tensor(ks, dtype=torch.int32, device=dev)
+    d = C
+    ne = sum(1 for k in ks if k > 0)
+    if w.kind == "bf16":
+        ops = w.sum_k * (w.M + w.N) * 2
+
+        def step():
+            dg.dg_k_grouped_bf16_wgrad(A, B, d, d, ks, ks_dev)
+        kname = "kgrouped_wgrad_kernel<bf16, 256, f32 reduce>"
+        peak_t = pk["bf16_tflops"]
+    else:
+        qa = torch.empty(w.sum_k, w.M, dtype=torch.uint8, device=dev)
+        sa = torch.empty(w.sum_k // 128, w.M, dtype=torch.uint8, device=dev)
+        qb = torch.empty(w.sum_k, w.N, dtype=torch.uint8, device=dev)
+        sb = torch.empty(w.sum_k // 128, w.N, dtype=torch.uint8, device=dev)
+        dg.dg_quant_transpose_fp8(A, qa, sa)
+        dg.dg_quant_transpose_fp8(B, qb, sb)
+        del A, B
+        ops = w.sum_k * (w.M + w.N) + (w.sum_k // 128) * (w.M + w.N)
+
+        def step():
+            dg.dg_k_grouped_fp8_wgrad(qa, sa, qb, sb, d, d, ks, ks_dev, 128)
+        kname = "kgrouped_wgrad_kernel<fp8, 224, f32 reduce>"
+        peak_t = 2.0 * pk["bf16_tflops"]
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    ms = time_events(step, args.steps, torch.cuda.current_stream())
+    dg.dg_sync_check()
+    alg = ops + ne * w.M * w.N * 4 * 2          # D read and written for non-empty experts
+    tf = w.flops / (ms * 1e-3) / 1e12
+    if rank == 0:
+        print(json.dumps({"profile_only": True, "workload": w.name, "ms_per_step": ms,
+                          "tflops": tf, "tensor_frac": tf / peak_t, "kernel": kname,
+                          "algorithmic_bytes": alg, "hbm_gbs": alg / (ms * 1e-3) / 1e9,
+                          "hbm_frac": alg / (ms * 1e-3) / 1e9 / pk["hbm_gbs"],
+                          "nonempty_experts": ne}), flush=True)
+    return 0
+
+
 def cpu_oracle_sample(w, ks, qa, sa, qb, sb, n_rows=16):
     """Time the float64 oracle on all experts x n_rows seeded rows of M x all N."""
     import oracle
@@ -372,9 +418,12 @@ def run_ours(args):
         import torch.distributed as tdist
         tdist.init_process_group("nccl", device_id=dev)
     w = workloads.WORKLOADS[args.workload]
-    if w.kind != "fp8":
-        raise SystemExit("bench.py times the FP8 workloads (moe_upgate_fp8_g32, moe_down_fp8_g32)")
     pk, pk_kind = peaks()
+    if w.kind != "fp8":
+        if not args.profile:
+            raise SystemExit("the full bench line runs the FP8 workloads; the BF16 and "
+                             "pipeline workloads have the device-timed --profile leg only")
+        return profile_inplace(w, args, dev, pk, rank)
     if args.profile_casts:
         # the cast legs alone (no GEMM buffers), for kernel captures
         ks = workloads.counts_for(w.name)
