@@ -419,6 +419,7 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
       const uint64_t utb_desc0 = smem_desc(smem_u32(smem + Cfg::OFF_UTB), 0, 128, 0);
       uint64_t a_desc = a_desc0, b_desc = b_desc0;
       uint32_t uses[2] = {0, 0};   // tiles completed per accumulator buffer
+      uint32_t gate_ph = 0;        // BF16: phase bit of each slot's `gate` (tail stages only)
       LaneSched L;
       lane_init(L, p, pid, R);
       Chunk ch;
@@ -459,9 +460,13 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
             }
           }
           DG_T0(w2);
-          // FP8 stages are complete once both CTAs' bytes land; BF16 stages
-          // once warp 6 has also masked an expert's tail rows.
-          ok = mbar_wait(kFP8 ? &full[s] : &gate[s], ph, abort_flag, lim, p.status, W_MMA_FULL, t);
+          // A stage is complete once both CTAs' bytes land (`full`); an
+          // expert's last, partial BF16 stage once warp 6 has also masked the
+          // rows past the slice in both CTAs (`gate`, used by tail stages only).
+          const bool tail = !kFP8 && jj == ch.nk - 1 && tcm.k_len - jj * Cfg::BK < Cfg::BK;
+          ok = mbar_wait(tail ? &gate[s] : &full[s], tail ? (gate_ph >> s) & 1u : ph, abort_flag,
+                         lim, p.status, W_MMA_FULL, t);
+          if (tail) gate_ph ^= 1u << s;
           DG_TACC(2, w2);
           if (!ok) break;
           tc_fence_after();
@@ -504,13 +509,13 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
   } else if (warp == 6) {
     if constexpr (!kFP8) {
       // ---------------------------------------------------------- BF16 stage gate
-      // Every stage passes through here in order, in both CTAs.  An expert's
-      // last stage may run past its slice: each CTA zeroes those token rows of
-      // its own operand tiles (row k of an atom is bytes [k*128, k*128 + 128))
-      // once they have landed, makes the writes visible to the tensor core
-      // (CTA-scope proxy fence) and arrives on the even CTA's `gate`.  The
-      // odd CTA's other stages need no work: it arrives once the stage's slot
-      // is free, well before their data land on the even CTA's `full`.
+      // An expert's last stage may run past its slice: each CTA zeroes those
+      // token rows of its own operand tiles (row k of an atom is bytes
+      // [k*128, k*128 + 128)) once they have landed, makes the writes visible
+      // to the tensor core (CTA-scope proxy fence) and arrives on the even
+      // CTA's `gate`, which the MMA thread waits on for such stages only.
+      // Every stage is walked in order and waited on through `empty`, so this
+      // warp is never more than one use of a slot ahead.
       {
         int s = 0;
         uint32_t ph = 0;
@@ -530,13 +535,15 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
           for (int j = ch.j0; j < ch.j1; ++j) {
             const int jj = rot_stage(j, rot);
             const bool tail_stage = (jj == nk - 1 && tail < Cfg::BK);
-            // the slot's previous use has been consumed (keeps gate phases in order)
+            // the slot's previous use has been consumed (keeps phases in order)
             ok = mbar_wait(&empty[s], ph ^ 1, abort_flag, lim, p.status, W_SF_FULL, t);
-            if (ok && leader)
-              ok = mbar_wait(&full[s], ph, abort_flag, lim, p.status, W_SF_FULL, t);
-            if (ok && !leader && tail_stage) {
-              ok = mbar_wait(&tfull[s], (tph >> s) & 1, abort_flag, lim, p.status, W_SF_FULL, t);
-              tph ^= 1u << s;
+            if (ok && tail_stage) {
+              if (leader) {
+                ok = mbar_wait(&full[s], ph, abort_flag, lim, p.status, W_SF_FULL, t);
+              } else {
+                ok = mbar_wait(&tfull[s], (tph >> s) & 1, abort_flag, lim, p.status, W_SF_FULL, t);
+                tph ^= 1u << s;
+              }
             }
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
@@ -553,15 +560,13 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
                 *reinterpret_cast<uint4 *>(base + tail * 128 + r * 16) = make_uint4(0, 0, 0, 0);
               }
               fence_proxy_async_smem();
-            }
-            __syncwarp();
-            if (lane == 0) {
-              if (leader)
-                mbar_arrive(&gate[s]);
-              else if (tail_stage)
-                mbar_arrive_cluster(gate_leader + 8 * s);   // publishes the zeroed rows
-              else
-                mbar_arrive_remote(gate_leader + 8 * s);
+              __syncwarp();
+              if (lane == 0) {
+                if (leader)
+                  mbar_arrive(&gate[s]);
+                else
+                  mbar_arrive_cluster(gate_leader + 8 * s);   // publishes the zeroed rows
+              }
             }
             if (++s == S) { s = 0; ph ^= 1; }
           }
