@@ -211,30 +211,10 @@ dg_status run_grouped(const GroupedArgs &x) {
   dg_status s = device_state(&dev);
   if (s != DG_OK) return s;
 
-  // ---- schedule: longest experts first, then output-only (fill) experts
-  std::unique_ptr<dg::WgradParams> hold(new dg::WgradParams);   // ~17 KB: off the stack
+  // ---- schedule: longest entries first, then output-only (fill) experts
+  std::unique_ptr<dg::WgradParams> hold(new dg::WgradParams);   // ~21 KB: off the stack
   dg::WgradParams &p = *hold;
   std::memset(&p, 0, sizeof(p));
-  std::vector<int> order;
-  order.reserve(x.G);
-  std::vector<int64_t> off(x.G + 1, 0);
-  for (int e = 0; e < x.G; ++e) off[e + 1] = off[e] + x.ks_host[e];
-  for (int e = 0; e < x.G; ++e)
-    if (x.ks_host[e] > 0) order.push_back(e);
-  std::stable_sort(order.begin(), order.end(),
-                   [&](int u, int v) { return x.ks_host[u] > x.ks_host[v]; });
-  const int n_mma = static_cast<int>(order.size());
-  const bool fill_empty = (x.c != x.d);    // no accumulator, or a separate one
-  if (fill_empty)
-    for (int e = 0; e < x.G; ++e)
-      if (x.ks_host[e] == 0) order.push_back(e);
-  const int n_groups = static_cast<int>(order.size());
-  for (int i = 0; i < n_groups; ++i) {
-    const int e = order[i];
-    p.sched[i].expert = e;
-    p.sched[i].k_off = static_cast<int>(off[e]);
-    p.sched[i].k_len = x.ks_host[e];
-  }
   // FP8 with N not a multiple of 224 but M one (the down-projection's 7168 x
   // 2048): compute D^T tiles instead, so that the 224-wide tile runs along M
   // with no ragged edge and the 256-row side along N.
@@ -245,6 +225,63 @@ dg_status run_grouped(const GroupedArgs &x) {
   const uint8_t *ksfa = trans ? x.sfb : x.sfa;
   const uint8_t *ksfb = trans ? x.sfa : x.sfb;
   const int bn = x.fp8 ? dg::fp8_pick_block_n(Nk) : dg::bf16_pick_block_n(Nk);
+  const int tpg = ((Mk + dg::kPairM - 1) / dg::kPairM) * ((Nk + bn - 1) / bn);
+  const bool reduce = (x.c == x.d) && x.d_dtype == DG_F32;   // D += acc in place
+
+  struct Entry {
+    int expert;
+    int64_t k_off;
+    int k_len;
+  };
+  std::vector<int64_t> off(x.G + 1, 0);
+  for (int e = 0; e < x.G; ++e) off[e + 1] = off[e] + x.ks_host[e];
+  std::vector<Entry> ents;
+  for (int e = 0; e < x.G; ++e)
+    if (x.ks_host[e] > 0) ents.push_back(Entry{e, off[e], x.ks_host[e]});
+  // In-place accumulation: experts much longer than a CTA pair's fair share of
+  // the work are split along K into several entries, each adding its part
+  // into D (exact by linearity; the order of the FP32 additions then depends
+  // on timing).  A pair's fair share is (stages x tiles) / pairs; entries are
+  // capped at a quarter of it, in whole scale groups for FP8.
+  if (reduce && !ents.empty()) {
+    const int bk = x.fp8 ? 128 : 64;            // tokens per stage
+    const int unit = x.fp8 ? 4 : 1;             // stages per split unit
+    int64_t total = 0;
+    for (const Entry &en : ents) total += (en.k_len + bk - 1) / bk;
+    const int64_t share = total * tpg / std::max(1, dev->sms / 2);
+    const int64_t cap = std::max<int64_t>(8, share / 4);   // stages per entry
+    std::vector<Entry> split;
+    for (const Entry &en : ents) {
+      const int64_t st = (en.k_len + bk - 1) / bk;
+      if (st <= cap) {
+        split.push_back(en);
+        continue;
+      }
+      const int64_t parts = (st + cap - 1) / cap;
+      int64_t per = (st + parts - 1) / parts;
+      per = (per + unit - 1) / unit * unit;
+      for (int64_t s0 = 0; s0 < st; s0 += per) {
+        const int64_t t0 = s0 * bk;
+        const int64_t t1 = std::min<int64_t>(en.k_len, (s0 + per) * bk);
+        split.push_back(Entry{en.expert, en.k_off + t0, static_cast<int>(t1 - t0)});
+      }
+    }
+    if (static_cast<int>(split.size()) <= dg::kMaxGroups) ents.swap(split);
+  }
+  std::stable_sort(ents.begin(), ents.end(),
+                   [](const Entry &u, const Entry &v) { return u.k_len > v.k_len; });
+  const int n_mma = static_cast<int>(ents.size());
+  const bool fill_empty = (x.c != x.d);    // no accumulator, or a separate one
+  if (fill_empty)
+    for (int e = 0; e < x.G; ++e)
+      if (x.ks_host[e] == 0) ents.push_back(Entry{e, off[e], 0});
+  const int n_groups = static_cast<int>(ents.size());
+  for (int i = 0; i < n_groups; ++i) {
+    p.sched[i].expert = ents[i].expert;
+    p.sched[i].k_off = static_cast<int>(ents[i].k_off);
+    p.sched[i].k_len = ents[i].k_len;
+    p.sched[i].k_exp = x.ks_host[ents[i].expert];
+  }
   p.M = Mk;
   p.N = Nk;
   p.G = x.G;

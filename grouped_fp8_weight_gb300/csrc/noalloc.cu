@@ -215,6 +215,7 @@ extern "C" dg_status dg_k_grouped_fp8_wgrad_noalloc(
     p.sched[n].expert = order[n];
     p.sched[n].k_off = static_cast<int>(offs[order[n]]);
     p.sched[n].k_len = ks_host[order[n]];
+    p.sched[n].k_exp = ks_host[order[n]];
   }
   const int bn = dg::fp8_pick_block_n(N);
   p.M = M;

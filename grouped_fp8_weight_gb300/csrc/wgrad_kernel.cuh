@@ -10,8 +10,9 @@
 // MMA thread issues every MMA for both; the operands of one stage are thus
 // loaded once per pair, halving each SM's B traffic.
 //
-// Pairs own every R-th tile of the list (expert, 256-row M tile, BN-column N
-// tile), which the host sorts longest expert first.  A pair's two tensor-memory
+// Pairs own one tile of every round of R tiles of the list (expert entry,
+// 256-row M tile, BN-column N tile), which the host sorts longest entry first,
+// in snake order.  A pair's two tensor-memory
 // accumulators serve as two lanes: lane 0 takes its tiles from the head of its
 // list, lane 1 from the tail, and the MMA stream alternates `chunk` stages of
 // lane 0's (long) tile with the whole of lane 1's (short) tile, so the
@@ -163,7 +164,20 @@ __device__ __forceinline__ int rot_stage(int j, KRot r) {
 }
 
 // ---------------------------------------------------------------- schedule
-// A pair owns the tiles u = pid + i * R (i = 0, 1, ...) of the longest-first
+// A pair owns one tile of every round of R tiles of the longest-first list,
+// in snake order (round i: position pid when i is even, R - 1 - pid when odd),
+// which balances the pairs' totals better than the same position every round
+// while keeping each pair's list longest first.
+__device__ __forceinline__ int owned_tile(int i, int pid, int R) {
+  return i * R + ((i & 1) ? R - 1 - pid : pid);
+}
+__device__ __forceinline__ int owned_count(int num_tiles, int pid, int R) {
+  const int full = num_tiles / R;
+  const int off = (full & 1) ? R - 1 - pid : pid;
+  return full + (off < num_tiles - full * R ? 1 : 0);
+}
+
+// A pair owns the tiles u = owned_tile(i) (i = 0, 1, ...) of the longest-first
 // tile list.  Its two accumulator buffers work as two lanes: lane 0 takes
 // tiles from the head of its list (long, MMA-heavy) and lane 1 from the tail
 // (short or output-only, store-heavy).  The MMA stream alternates between the
@@ -186,7 +200,7 @@ struct LaneSched {
 
 __device__ __forceinline__ void lane_init(LaneSched &L, const WgradParams &p, int pid, int R) {
   L.head = 0;
-  L.tail = (p.num_tiles - pid + R - 1) / R - 1;
+  L.tail = owned_count(p.num_tiles, pid, R) - 1;
   L.u0 = L.u1 = -1;
   L.nk0 = L.nk1 = L.j0 = L.j1 = 0;
   L.turn = 0;
@@ -200,7 +214,7 @@ __device__ __forceinline__ bool lane_turn(LaneSched &L, const WgradParams &p, in
   if (u < 0) {
     if (L.head > L.tail) return false;
     const int i = (l == 0) ? L.head++ : L.tail--;
-    u = pid + i * R;
+    u = owned_tile(i, pid, R);
     nk = (u < p.num_mma_tiles) ? (p.sched[u / p.tiles_per_group].k_len + bk - 1) / bk : 0;
     j = 0;
     if (nk == 0) {   // output-only tile: a completion without MMAs
@@ -333,7 +347,7 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
         const TileCoord tc = tile_coord(p, ch.u, kBN, rank);
         const int t = ch.u;
         if (leader && ch.j0 == 0 && p.ks_dev != nullptr && tc.m0 == 0 && tc.n0 == 0 &&
-            p.ks_dev[tc.expert] != tc.k_len)
+            p.ks_dev[tc.expert] != p.sched[t / p.tiles_per_group].k_exp)
           atomicCAS(&p.status->code, DEV_OK, DEV_KS_MISMATCH);
         const int nb = tc.n0 + static_cast<int>(rank) * Cfg::BN_CTA;   // this CTA's B columns
         const KRot rot = tile_rot(tc.mt, tc.nt, ch.nk, Cfg::ROT_UNIT);

@@ -11,14 +11,16 @@ namespace dg {
 
 constexpr int kMaxGroups = 1024;   // must equal DG_MAX_GROUPS
 
-// One schedule entry: an expert and its token slice.  Entries with k_len > 0
-// come first, longest first; after them come experts whose output must be
-// written without a GEMM (K_e == 0 with no accumulator or a separate one).
+// One schedule entry: an expert and a token slice of it (the whole slice, or
+// for in-place accumulation one part of a long expert's).  Entries with
+// k_len > 0 come first, longest first; after them come experts whose output
+// must be written without a GEMM (K_e == 0 with no accumulator or a separate one).
 struct SchedEntry {
   int expert;
   int k_off;
   int k_len;
   int g_off;   // FP8: first packed scale group of this entry
+  int k_exp;   // the expert's whole token count (an entry may be one part of it)
 };
 
 enum OutMode : int {

@@ -90,7 +90,11 @@ typedef enum {
  *           nearest-even from the FP32 accumulator.
  *   c       NULL: Cterm = 0.  c == d: accumulate in place (D += ...).  Any other
  *           pointer: a separate FP32 [G, M, N] accumulator (not modified).
- *           Only with d_dtype == DG_F32.
+ *           Only with d_dtype == DG_F32.  In place, an expert much longer than
+ *           the others is split along K into parts that each add into D, so
+ *           the order of the FP32 additions (and the last bits of D) may vary
+ *           from run to run; every other mode writes each element once and is
+ *           bitwise reproducible.
  *   G       number of experts, 0 <= G <= DG_MAX_GROUPS.
  *   M, N    positive multiples of 16.
  *   sum_k   total tokens; must equal ks_host[0] + ... + ks_host[G-1].
