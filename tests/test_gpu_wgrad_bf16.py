@@ -73,3 +73,16 @@ def test_fine_grained_workload_full():
     for e, k in enumerate(ks):
         if k == 0:
             assert torch.equal(d[e].cpu(), C[e])
+
+
+def test_inplace_long_expert_is_split():
+    """In place on a one-tile grid, an expert of 5000 tokens (78 full stages of
+    64 and a tail of 8) runs as several K parts, the last one with the tail."""
+    ks = [5000, 3, 0, 130]
+    M = N = 256
+    a, b = _ops(ks, M, N, 41)
+    C = workloads.randn((len(ks), M, N), 8, std=0.1).numpy()
+    d = run_bf16(a, b, ks, "f32", C, "inplace")
+    D, S = oracle.kgrouped_bf16_wgrad(a.float().numpy(), b.float().numpy(), ks, C)
+    assert_close(d, D, S, what="bf16 split")
+    assert torch.equal(d[2].cpu(), torch.from_numpy(C[2]))

@@ -231,3 +231,18 @@ def test_transposed_tiles_lanes():
     for e, (De, Se) in part.items():
         assert_close(dr[e], De, Se, "bf16", what=f"transposed lanes expert {e}")
     assert torch.count_nonzero(d[2]).item() == 0
+
+
+@pytest.mark.parametrize("gran_k", [128, 32])
+@pytest.mark.parametrize("M,N", [(256, 224), (448, 272)])
+def test_inplace_long_expert_is_split(gran_k, M, N):
+    """In place, one expert far longer than a CTA pair's share of the work (a
+    one- or two-tile grid): it runs as several K parts that each add into D.
+    (448 x 272 also takes the transposed tiles.)"""
+    ks = [128 * 70, 128, 0, 128 * 3]
+    qa, sa, qb, sb = _case(ks, M, N, 31, gran_k, scale_noise=True)
+    C = workloads.randn((len(ks), M, N), 96).numpy()
+    d = run_fp8(qa, sa, qb, sb, ks, gran_k, "f32", C, "inplace")
+    D, S = oracle.kgrouped_fp8_wgrad(qa, sa, qb, sb, ks, gran_k, C)
+    assert_close(d, D, S, what=f"split {M}x{N} g{gran_k}")
+    assert torch.equal(d[2].cpu(), torch.from_numpy(C[2]))

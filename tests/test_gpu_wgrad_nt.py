@@ -152,3 +152,13 @@ def test_nt_transposed_tiles(out, c_mode):
     d = run_nt(qa, sa, qb, sb, ks, 128, out, C if c_mode != "none" else None, c_mode)
     D, S = oracle.kgrouped_fp8_wgrad(qa, sa, qb, sb, ks, 128, C if c_mode != "none" else None)
     assert_close(d, D, S, out, what=f"nt transposed {out}/{c_mode}")
+
+
+def test_nt_inplace_long_expert_is_split():
+    ks = [128 * 70, 128, 0, 128 * 3]
+    M, N = 256, 224
+    qa, sa, qb, sb = _case(ks, M, N, 33, 128, scale_noise=True)
+    C = workloads.randn((len(ks), M, N), 95).numpy()
+    d = run_nt(qa, sa, qb, sb, ks, 128, "f32", C, "inplace")
+    D, S = oracle.kgrouped_fp8_wgrad(qa, sa, qb, sb, ks, 128, C)
+    assert_close(d, D, S, what="nt split")
