@@ -123,6 +123,15 @@ uint64_t wait_limit_ns() {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// DG_LOG=1 in the environment: each GEMM call prints its plan to stderr.
+bool log_enabled() {
+  static const bool on = [] {
+    const char *v = std::getenv("DG_LOG");
+    return v != nullptr && *v != '\0' && *v != '0';
+  }();
+  return on;
+}
+
 dg_status encode(CUtensorMap *m, CUtensorMapDataType dt, const void *ptr, int rank,
                  const uint64_t *dims, const uint64_t *strides_bytes, const uint32_t *box,
                  CUtensorMapSwizzle sw, CUtensorMapL2promotion l2, const char *what) {
@@ -306,6 +315,26 @@ dg_status run_grouped(const GroupedArgs &x) {
 #ifdef DG_KERNEL_TIMERS
   p.timers = g_timers;
 #endif
+  if (log_enabled()) {
+    int empty = 0, max_k = 0;
+    for (int e = 0; e < x.G; ++e) {
+      empty += (x.ks_host[e] == 0);
+      max_k = std::max(max_k, x.ks_host[e]);
+    }
+    std::fprintf(stderr,
+                 "[dg] %s: G=%d M=%d N=%d sum_k=%lld (%d empty, max K %d) | %s operands, %s tiles "
+                 "256 x %d, %d x %d per expert | %d GEMM entries (+%d from splits along K), "
+                 "%d GEMM tiles + %d output-only | out=%s | pairs=%d\n",
+                 fn, x.G, x.M, x.N, static_cast<long long>(x.sum_k), empty, max_k,
+                 x.kmajor ? "K-major" : "token-major", trans ? "transposed" : "direct", bn,
+                 p.m_tiles, p.n_tiles, n_mma, n_mma - (x.G - empty), p.num_mma_tiles,
+                 p.num_tiles - p.num_mma_tiles,
+                 p.out_mode == dg::OUT_BF16        ? "bf16"
+                 : p.out_mode == dg::OUT_F32       ? "f32"
+                 : p.out_mode == dg::OUT_F32_REDUCE ? "f32 += (reduce-add)"
+                                                    : "f32 = C +",
+                 std::min(dev->sms / 2, p.num_tiles));
+  }
   if (p.num_tiles == 0) return ok();     // every expert empty and D accumulates in place
   std::unique_ptr<dg::PackParams> pk_hold(new dg::PackParams);   // ~12 KB
   dg::PackParams &pk = *pk_hold;

@@ -34,6 +34,9 @@
  *    must stay valid until the enqueued work completes.
  *  - Argument errors are returned before anything is enqueued; the output is
  *    then untouched.  dg_last_error() gives a message for the calling thread.
+ *  - DG_LOG=1 in the environment makes each GEMM call print its plan (tile
+ *    orientation and width, tiles, entries split along K, output mode) to
+ *    stderr.
  *  - Device-side waits are bounded (default 4 s, environment variable
  *    DG_WAIT_LIMIT_MS).  A wait that runs out makes the kernel stop early and
  *    record DG_ERR_TIMEOUT in the device status word, which dg_sync_check()
