@@ -234,7 +234,7 @@ def measure_casts(w, ks, dev, stream, pk, steps):
     # each distinct source row read once (a row gathered into several experts'
     # slices is re-read from L2), each output row written once
     nb = uniq * w.N * 2 + w.sum_k * w.N + w.sum_k * 4 + (w.sum_k // 128) * w.N
-    out["moe_layout"] = {"ms": ms, "kernel": "cast_colblock_kernel<128, token, bf16, gather>",
+    out["moe_layout"] = {"ms": ms, "kernel": "gather_cast_kernel<128> (TMA gather4 rows, token-major)",
                          "launches_per_step": 1, "source_tokens": t_tok, "rows": w.sum_k,
                          "distinct_source_rows": uniq,
                          "bound": "hbm", "achieved": nb / (ms * 1e-3) / 1e9,

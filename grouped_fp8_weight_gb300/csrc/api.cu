@@ -436,6 +436,21 @@ dg_status run_grouped(const GroupedArgs &x) {
   return ok();
 }
 
+dg::CastArgs cast_args(const void *x, const uint8_t *x_sf, const int *src_rows, int64_t T_src,
+                       int64_t T, int C, void *q, uint8_t *sf) {
+  dg::CastArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.x = x;
+  a.x_sf = x_sf;
+  a.src_rows = src_rows;
+  a.T_src = T_src;
+  a.T = T;
+  a.C = C;
+  a.q = static_cast<uint8_t *>(q);
+  a.sf = sf;
+  return a;
+}
+
 // Validation and launch shared by the three column-block casts.  a.x_sf set:
 // E4M3 source with 1 x 128 scales (C a multiple of 128); a.src_rows set: MoE
 // layout gather from T_src source rows.
@@ -468,6 +483,18 @@ dg_status run_cast(const char *fn, dg::CastArgs a, dg_layout q_layout, int gran_
   dg_status s = device_state(&dev);
   if (s != DG_OK) return s;
   a.status = dev->status;
+  a.wait_limit_ns = wait_limit_ns();
+  // BF16 rows gathered into the token-major layout: the rows come in by TMA
+  // (four indexed rows per instruction) through a map of x as {C, T_src}.
+  if (!fp8 && a.src_rows != nullptr && q_layout == DG_TOKEN_MAJOR && a.T_src > 0) {
+    const uint64_t dims[2] = {static_cast<uint64_t>(a.C), static_cast<uint64_t>(a.T_src)};
+    const uint64_t strides[1] = {static_cast<uint64_t>(a.C) * 2};
+    const uint32_t box[2] = {256, 1};
+    if ((s = encode(&a.tmx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.x, 2, dims, strides, box,
+                    CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B, "x rows")))
+      return s;
+    a.use_tmx = 1;
+  }
   cudaError_t e = dg::launch_cast_colblock(a, q_layout == DG_CHANNEL_MAJOR, gran_k, stream);
   if (e != cudaSuccess)
     return fail(DG_ERR_CUDA, "%s: launch failed: %s", fn, cudaGetErrorString(e));
@@ -512,7 +539,7 @@ dg_status dg_k_grouped_bf16_wgrad(const void *a, const void *b, void *d, dg_dtyp
 
 dg_status dg_quant_transpose_fp8(const void *x, int64_t T, int C, void *q, uint8_t *sf,
                                  dg_layout q_layout, int gran_k, dg_stream_t stream) {
-  dg::CastArgs a{x, nullptr, nullptr, T, T, C, static_cast<uint8_t *>(q), sf, nullptr};
+  dg::CastArgs a = cast_args(x, nullptr, nullptr, T, T, C, q, sf);
   return run_cast("dg_quant_transpose_fp8", a, q_layout, gran_k,
                   reinterpret_cast<cudaStream_t>(stream));
 }
@@ -523,7 +550,7 @@ dg_status dg_requant_transpose_fp8(const void *q_in, const uint8_t *sf_in, int64
   const char *fn = "dg_requant_transpose_fp8";
   if (T > 0 && sf_in == nullptr)
     return fail(DG_ERR_INVALID_ARG, "%s: sf_in is required", fn);
-  dg::CastArgs a{q_in, sf_in, nullptr, T, T, C, static_cast<uint8_t *>(q), sf, nullptr};
+  dg::CastArgs a = cast_args(q_in, sf_in, nullptr, T, T, C, q, sf);
   return run_cast(fn, a, q_layout, gran_k, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -534,7 +561,7 @@ dg_status dg_quant_moe_layout_fp8(const void *x, const uint8_t *x_sf, int64_t T_
   if (T_src < 0) return fail(DG_ERR_INVALID_ARG, "%s: T_src < 0", fn);
   if (T > 0 && src_rows == nullptr)
     return fail(DG_ERR_INVALID_ARG, "%s: src_rows is required", fn);
-  dg::CastArgs a{x, x_sf, src_rows, T_src, T, C, static_cast<uint8_t *>(q), sf, nullptr};
+  dg::CastArgs a = cast_args(x, x_sf, src_rows, T_src, T, C, q, sf);
   return run_cast(fn, a, q_layout, gran_k, reinterpret_cast<cudaStream_t>(stream));
 }
 

@@ -144,6 +144,18 @@ __device__ __forceinline__ void tma_load_2d_hint(void *dst, const CUtensorMap *m
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "l"(pol)
       : "memory");
 }
+// Four rows of a 2-D tensor map whose box is one row high (row indices r0..r3;
+// an index outside the tensor reads as zeros), starting at column c0, into
+// consecutive box-sized slots of this CTA's shared memory.
+__device__ __forceinline__ void tma_gather4_2d(void *dst, const CUtensorMap *map, uint64_t *bar,
+                                               int c0, int r0, int r1, int r2, int r3) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(r0), "r"(r1), "r"(r2),
+      "r"(r3)
+      : "memory");
+}
 // Load into this CTA's shared memory; the byte count completes on the mbarrier
 // at cluster address `bar_cluster` (this CTA's or its pair's).
 __device__ __forceinline__ void tma_load_2d_pair(void *dst, const CUtensorMap *map,

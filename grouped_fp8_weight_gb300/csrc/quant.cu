@@ -473,6 +473,139 @@ __global__ void __launch_bounds__(256, 2) requant_tm_kernel(const CastArgs a) {
   }
 }
 
+// BF16 rows gathered into the token-major MoE layout, brought in by TMA: one
+// CTA covers 128 output rows x 256 channels; its first thread issues 32
+// gather4 loads (four indexed rows of 512 bytes each) into a 64 KB shared
+// tile, so that the whole tile is in flight at once without holding
+// registers (three CTAs per SM: 206 KB).  Padding rows (-1) load row 0, which
+// the passes below replace by zeros, so every gathered row is in bounds.
+// Then the column-block cast as above, reading the tile twice (maxima, then
+// quantise and store), one 16-byte row chunk at a time.
+constexpr int kGtSmem = kTileT * kTileC * 2 + kTileT * 4 + 8 * 32 * 16 + 16;
+
+template <int kGran>
+__global__ void __launch_bounds__(256, 3) gather_cast_kernel(const __grid_constant__ CastArgs a) {
+  extern __shared__ __align__(1024) uint8_t gt_smem[];
+  uint8_t *tile = gt_smem;                                                 // [128][512 B]
+  int *idx = reinterpret_cast<int *>(gt_smem + kTileT * kTileC * 2);       // [128]
+  uint4 *red = reinterpret_cast<uint4 *>(gt_smem + kTileT * kTileC * 2 + kTileT * 4);   // [8][32]
+  uint64_t *bar = reinterpret_cast<uint64_t *>(gt_smem + kTileT * kTileC * 2 + kTileT * 4 + 8 * 32 * 16);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(bar + 1);
+  const int tid = threadIdx.x;
+  const int w = tid >> 5, l = tid & 31;
+  const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kTileT;
+  const int C = a.C;
+  const int c0 = blockIdx.y * kTileC;
+  const int col = c0 + 8 * l;
+  const bool col_ok = col < C;
+
+  if (tid < kTileT) {
+    const int64_t t = t0 + tid;
+    int s = t < a.T ? __ldg(a.src_rows + t) : -1;
+    if (s < -1 || s >= a.T_src) {
+      atomicCAS(&a.status->code, DEV_OK, DEV_BAD_ROW);
+      s = -1;
+    }
+    idx[tid] = s;
+  }
+  if (tid == 0) {
+    mbar_init(bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (tid == 0) {
+    mbar_arrive_expect_tx(bar, kTileT * kTileC * 2);
+#pragma unroll 4
+    for (int j = 0; j < kTileT / 4; ++j)
+      tma_gather4_2d(tile + j * 4 * kTileC * 2, &a.tmx, bar, c0, max(idx[4 * j], 0),
+                     max(idx[4 * j + 1], 0), max(idx[4 * j + 2], 0), max(idx[4 * j + 3], 0));
+  }
+  if (!mbar_wait(bar, 0, abort_flag, a.wait_limit_ns, a.status, 0x41, blockIdx.x)) {
+    // gave up: let the copies in flight land (bounded) before the CTA exits
+    mbar_wait(bar, 0, abort_flag, a.wait_limit_ns, a.status, 0x42, blockIdx.x, false);
+    return;
+  }
+
+  // ---- pass 1: packed 16-bit maxima of |x| over this thread's 16 rows
+  uint32_t m[4] = {0, 0, 0, 0};
+#pragma unroll 4
+  for (int i = 0; i < 16; ++i) {
+    uint4 v = *reinterpret_cast<const uint4 *>(tile + (16 * w + i) * (kTileC * 2) + l * 16);
+    if (idx[16 * w + i] < 0) v = make_uint4(0, 0, 0, 0);
+    m[0] = __vmaxu2(m[0], v.x & 0x7FFF7FFFu);
+    m[1] = __vmaxu2(m[1], v.y & 0x7FFF7FFFu);
+    m[2] = __vmaxu2(m[2], v.z & 0x7FFF7FFFu);
+    m[3] = __vmaxu2(m[3], v.w & 0x7FFF7FFFu);
+  }
+  red[w * 32 + l] = make_uint4(m[0], m[1], m[2], m[3]);
+  __syncthreads();
+  constexpr int kWarps = (kGran == 128) ? 8 : 2;
+  const int w0 = (kGran == 128) ? 0 : (w & ~1);
+  uint4 r = red[w0 * 32 + l];
+#pragma unroll
+  for (int ww = 1; ww < kWarps; ++ww) {
+    const uint4 o = red[(w0 + ww) * 32 + l];
+    r.x = __vmaxu2(r.x, o.x);
+    r.y = __vmaxu2(r.y, o.y);
+    r.z = __vmaxu2(r.z, o.z);
+    r.w = __vmaxu2(r.w, o.w);
+  }
+  const uint32_t aw[4] = {r.x, r.y, r.z, r.w};
+  float mul[8];
+  uint32_t sfw[2] = {0, 0};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int e = scale_exp_from_bf16((aw[k] >> (16 * h)) & 0xFFFFu);
+      mul[2 * k + h] = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+      sfw[k >> 1] |= static_cast<uint32_t>(e + 127) << (8 * (2 * (k & 1) + h));
+    }
+  }
+  if (col_ok) {
+    if constexpr (kGran == 128) {
+      if (w == 0)
+        *reinterpret_cast<uint2 *>(a.sf + (t0 / 128) * C + col) = make_uint2(sfw[0], sfw[1]);
+    } else {
+      const int64_t tb = t0 + 16 * w;
+      if ((w & 1) == 0 && tb < a.T)
+        *reinterpret_cast<uint2 *>(a.sf + (tb / 32) * C + col) = make_uint2(sfw[0], sfw[1]);
+    }
+  }
+
+  // ---- pass 2: quantise and store (rows past T are not written)
+#pragma unroll 4
+  for (int i = 0; i < 16; ++i) {
+    const int64_t t = t0 + 16 * w + i;
+    uint4 v = *reinterpret_cast<const uint4 *>(tile + (16 * w + i) * (kTileC * 2) + l * 16);
+    if (idx[16 * w + i] < 0) v = make_uint4(0, 0, 0, 0);
+    const uint2 o =
+        make_uint2(quant_word(v.x, mul[0], mul[1]) | (quant_word(v.y, mul[2], mul[3]) << 16),
+                   quant_word(v.z, mul[4], mul[5]) | (quant_word(v.w, mul[6], mul[7]) << 16));
+    if (col_ok && t < a.T) __stcs(reinterpret_cast<uint2 *>(a.q + t * C + col), o);
+  }
+}
+
+template <int kGran>
+cudaError_t launch_gather_tma(const CastArgs &a, cudaStream_t stream) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(gather_cast_kernel<kGran>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kGtSmem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(gather_cast_kernel<kGran>,
+                               cudaFuncAttributePreferredSharedMemoryCarveout,
+                               cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const dim3 grid(static_cast<unsigned>((a.T + kTileT - 1) / kTileT),
+                  static_cast<unsigned>((a.C + kTileC - 1) / kTileC));
+  gather_cast_kernel<kGran><<<grid, 256, kGtSmem, stream>>>(a);
+  return cudaGetLastError();
+}
+
 template <bool kFp8Src, bool kGather>
 cudaError_t launch_src(const CastArgs &a, int channel_major, int gran_k, cudaStream_t stream) {
   const dim3 grid(static_cast<unsigned>((a.T + kTileT - 1) / kTileT),
@@ -518,6 +651,8 @@ cudaError_t launch_cast_colblock(const CastArgs &a, int channel_major, int gran_
                                  cudaStream_t stream) {
   const bool fp8 = (a.x_sf != nullptr);
   const bool gather = (a.src_rows != nullptr);
+  if (a.use_tmx)
+    return gran_k == 128 ? launch_gather_tma<128>(a, stream) : launch_gather_tma<32>(a, stream);
   if (fp8 && !channel_major)
     return gather ? launch_requant_tm<true>(a, gran_k, stream)
                   : launch_requant_tm<false>(a, gran_k, stream);

@@ -98,6 +98,7 @@ cudaError_t launch_kgrouped_fp8_nt_t(const WgradParams &p, int block_n, int pair
 // (x_sf [T_src, C / 128]).  With src_rows set, output row t takes source row
 // src_rows[t] (-1: a row of zeros); otherwise row t (T_src == T).
 struct CastArgs {
+  CUtensorMap tmx;     // BF16 gather, token-major: x as {C, T_src}, boxes of 256 x 1
   const void *x;
   const uint8_t *x_sf;
   const int *src_rows;
@@ -105,6 +106,8 @@ struct CastArgs {
   int C;
   uint8_t *q, *sf;
   DevStatus *status;   // records DEV_BAD_ROW for a src_rows entry outside [-1, T_src)
+  int use_tmx;         // 1: tmx is valid and the row gather runs through TMA
+  uint64_t wait_limit_ns;
 };
 cudaError_t launch_cast_colblock(const CastArgs &a, int channel_major, int gran_k,
                                  cudaStream_t stream);
