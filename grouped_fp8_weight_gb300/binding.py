@@ -34,6 +34,8 @@ SIGNATURES = {
     "dg_k_grouped_fp8_wgrad_nt": (_I, [_VP, _U8P, _VP, _U8P, _VP, _I, _FP, _I, _I, _I, _I64,
                                        _IP, _IP, _I, _VP]),
     "dg_k_grouped_bf16_wgrad": (_I, [_VP, _VP, _VP, _I, _FP, _I, _I, _I, _I64, _IP, _IP, _VP]),
+    "dg_m_grouped_fp8_dgrad": (_I, [_VP, _U8P, _VP, _U8P, _VP, _I, _I, _I, _I, _I64, _IP, _IP,
+                                    _I, _VP]),
     "dg_quant_transpose_fp8": (_I, [_VP, _I64, _I, _VP, _U8P, _I, _I, _VP]),
     "dg_requant_transpose_fp8": (_I, [_VP, _U8P, _I64, _I, _VP, _U8P, _I, _I, _VP]),
     "dg_quant_moe_layout_fp8": (_I, [_VP, _U8P, _I64, _I, _IP, _I64, _VP, _U8P, _I, _I, _VP]),
@@ -176,6 +178,39 @@ def dg_k_grouped_bf16_wgrad(a, b, d, c, ks_host, ks_dev, stream=None):
     _check(lib().dg_k_grouped_bf16_wgrad(
         _dptr(a), _dptr(b), _dptr(d), DG_BF16 if d.dtype == torch.bfloat16 else DG_F32,
         _dptr(c), G, M, N, a.shape[0], kh, _dptr(ks_dev), _stream(stream)))
+
+
+def dg_m_grouped_fp8_dgrad(a, sfa, w, sfw, d, ms_host, ms_dev, gran_k: int = 128,
+                           stream=None):
+    """D[t] = dy[t] W_e for the token rows t of expert e (M-grouped, contiguous).
+
+    a: E4M3 [sum_m, K] (or uint8 codes), sfa: uint8 [sum_m, K / gran_k];
+    w: E4M3 [G, K, N], sfw: uint8 [G, K / gran_k, N]; d: float32 or bfloat16
+    [sum_m, N]; ms_host: G token counts (multiples of 128), ms_dev the same as
+    an int32 CUDA tensor.
+    """
+    a8 = a.view(torch.uint8) if a.dtype != torch.uint8 else a
+    w8 = w.view(torch.uint8) if w.dtype != torch.uint8 else w
+    _need(a8, torch.uint8, "a", 2)
+    _need(w8, torch.uint8, "w", 3)
+    _need(sfa, torch.uint8, "sfa", 2)
+    _need(sfw, torch.uint8, "sfw", 3)
+    if d.dim() != 2 or d.dtype not in (torch.float32, torch.bfloat16) or not d.is_contiguous():
+        raise ValueError("d: expected contiguous float32/bfloat16 [sum_m, N]")
+    G, K, N = w8.shape
+    sum_m = a8.shape[0]
+    if a8.shape[1] != K or tuple(d.shape) != (sum_m, N):
+        raise ValueError("operand shapes do not match: a [sum_m, K], w [G, K, N], d [sum_m, N]")
+    if tuple(sfa.shape) != (sum_m, K // gran_k) or tuple(sfw.shape) != (G, K // gran_k, N):
+        raise ValueError("scale shapes: sfa [sum_m, K / gran_k], sfw [G, K / gran_k, N]")
+    _need(ms_dev, torch.int32, "ms_dev", 1)
+    mh, g = _ks_host(ms_host)
+    if g != G or ms_dev.numel() != G:
+        raise ValueError("ms must have G entries")
+    _check(lib().dg_m_grouped_fp8_dgrad(
+        _dptr(a8), _dptr(sfa), _dptr(w8), _dptr(sfw), _dptr(d),
+        DG_BF16 if d.dtype == torch.bfloat16 else DG_F32,
+        G, K, N, sum_m, mh, _dptr(ms_dev), gran_k, _stream(stream)))
 
 
 def dg_quant_transpose_fp8(x, q, sf, layout: str = "token", gran_k: int = 128, stream=None):

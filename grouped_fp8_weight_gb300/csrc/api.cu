@@ -436,6 +436,193 @@ dg_status run_grouped(const GroupedArgs &x) {
   return ok();
 }
 
+// M-grouped FP8 data gradient: validation, schedule (one entry per expert with
+// tokens), tensor maps, the two scale-pack passes and the GEMM launch.
+dg_status run_mgrouped(const void *a, const uint8_t *sfa, const void *w, const uint8_t *sfw,
+                       void *d, dg_dtype d_dtype, int G, int K, int N, int64_t sum_m,
+                       const int *ms_host, const int *ms_dev, int gran_k, cudaStream_t stream) {
+  const char *fn = "dg_m_grouped_fp8_dgrad";
+  if (G < 0) return fail(DG_ERR_INVALID_ARG, "%s: G = %d < 0", fn, G);
+  if (G > DG_MAX_GROUPS) return fail(DG_ERR_UNSUPPORTED, "%s: G = %d above DG_MAX_GROUPS", fn, G);
+  if (K <= 0 || K % 128)
+    return fail(DG_ERR_INVALID_ARG, "%s: K = %d must be a positive multiple of 128", fn, K);
+  if (N <= 0 || N % 16)
+    return fail(DG_ERR_INVALID_ARG, "%s: N = %d must be a positive multiple of 16", fn, N);
+  if (gran_k != 32 && gran_k != 128)
+    return fail(DG_ERR_INVALID_ARG, "%s: gran_k = %d (must be 32 or 128)", fn, gran_k);
+  if (d_dtype != DG_F32 && d_dtype != DG_BF16)
+    return fail(DG_ERR_INVALID_ARG, "%s: unknown output dtype %d", fn, (int)d_dtype);
+  if (sum_m < 0) return fail(DG_ERR_INVALID_ARG, "%s: sum_m < 0", fn);
+  if (sum_m > (int64_t)0x7FFFFF00)
+    return fail(DG_ERR_UNSUPPORTED, "%s: sum_m above 2^31 - 256", fn);
+  if (static_cast<int64_t>(G) * K > 0x7FFFFFFFll)
+    return fail(DG_ERR_UNSUPPORTED, "%s: G * K above 2^31 - 1", fn);
+  if (G == 0) {
+    if (sum_m != 0) return fail(DG_ERR_INVALID_ARG, "%s: G = 0 but sum_m = %lld", fn, (long long)sum_m);
+    return ok();
+  }
+  if (ms_host == nullptr || ms_dev == nullptr)
+    return fail(DG_ERR_INVALID_ARG, "%s: ms_host and ms_dev are required", fn);
+  int64_t total = 0;
+  for (int e = 0; e < G; ++e) {
+    const int m = ms_host[e];
+    if (m < 0) return fail(DG_ERR_INVALID_ARG, "%s: ms[%d] = %d < 0", fn, e, m);
+    if (m % 128) return fail(DG_ERR_INVALID_ARG, "%s: ms[%d] = %d is not a multiple of 128", fn, e, m);
+    total += m;
+  }
+  if (total != sum_m)
+    return fail(DG_ERR_INVALID_ARG, "%s: sum of ms (%lld) != sum_m (%lld)", fn, (long long)total,
+                (long long)sum_m);
+  if (sum_m == 0) return ok();
+  if (a == nullptr || w == nullptr || d == nullptr || sfa == nullptr || sfw == nullptr ||
+      !aligned16(a) || !aligned16(w) || !aligned16(d) || !aligned16(sfa) || !aligned16(sfw))
+    return fail(DG_ERR_INVALID_ARG, "%s: a, sfa, w, sfw and d must be 16-byte aligned device pointers",
+                fn);
+  const int es = (d_dtype == DG_BF16) ? 2 : 4;
+  if (static_cast<double>(sum_m) * N * es >= 1099511627776.0)
+    return fail(DG_ERR_UNSUPPORTED, "%s: output of 2^40 bytes or more", fn);
+  DeviceState *dev = nullptr;
+  dg_status s = device_state(&dev);
+  if (s != DG_OK) return s;
+
+  const int bn = dg::fp8_pick_block_n(N);
+  const int n_tiles = (N + bn - 1) / bn;
+  const int KB = K / gran_k;                          // scale columns of A, scale rows per W_e
+  const int gs = (gran_k == 128) ? 4 : 1;             // 128-wide k-blocks per scale group
+  const int NGK = (K / 128 + gs - 1) / gs;            // scale groups along K
+  const int TC = static_cast<int>(sum_m / 128) + 1;   // 128-token chunks (+1: a last odd half)
+
+  std::unique_ptr<dg::WgradParams> hold(new dg::WgradParams);
+  dg::WgradParams &p = *hold;
+  std::memset(&p, 0, sizeof(p));
+  int n_ent = 0;
+  int64_t tiles = 0, row = 0;
+  for (int e = 0; e < G; ++e) {
+    const int m = ms_host[e];
+    if (m > 0) {
+      dg::SchedEntry &se = p.sched[n_ent];
+      se.expert = e;
+      se.k_off = e * K;
+      se.k_len = K;
+      se.g_off = n_ent * NGK;
+      se.k_exp = m;
+      se.row_off = static_cast<int>(row);
+      se.tile_off = static_cast<int>(tiles);
+      tiles += static_cast<int64_t>((m + dg::kPairM - 1) / dg::kPairM) * n_tiles;
+      ++n_ent;
+    }
+    row += m;
+  }
+  if (tiles > 0x7FFFFFFFll) return fail(DG_ERR_UNSUPPORTED, "%s: more than 2^31 - 1 tiles", fn);
+  p.M = K;
+  p.N = N;
+  p.G = G;
+  p.m_tiles = 1;
+  p.n_tiles = n_tiles;
+  p.tiles_per_group = n_tiles;
+  p.num_mma_tiles = static_cast<int>(tiles);
+  p.num_tiles = static_cast<int>(tiles);
+  p.gran_k = gran_k;
+  p.chunk = dg::kFp8Chunk;
+  p.out_mode = (d_dtype == DG_BF16) ? dg::OUT_BF16 : dg::OUT_F32;
+  p.sf_mc = TC;
+  p.mgroup = 1;
+  p.n_entries = n_ent;
+  p.wait_limit_ns = wait_limit_ns();
+  p.status = dev->status;
+  p.ks_dev = ms_dev;
+#ifdef DG_KERNEL_TIMERS
+  p.timers = g_timers;
+#endif
+  if (log_enabled())
+    std::fprintf(stderr,
+                 "[dg] %s: G=%d K=%d N=%d sum_m=%lld | %d experts with tokens, tiles 256 x %d, "
+                 "%lld tiles | out=%s | pairs=%d\n",
+                 fn, G, K, N, static_cast<long long>(sum_m), n_ent, bn,
+                 static_cast<long long>(tiles), d_dtype == DG_BF16 ? "bf16" : "f32",
+                 std::min<int64_t>(dev->sms / 2, tiles) > 0 ? static_cast<int>(std::min<int64_t>(dev->sms / 2, tiles)) : 0);
+
+  // ---- tensor maps: dy as {K, sum_m} (K-major boxes of 128 x 128), the
+  // weights as {N, G K} (MN-major boxes of bn / 2 x 128), D as {N, sum_m, 1}
+  const uint64_t SM = static_cast<uint64_t>(sum_m), UK = K, UN = N, GK = static_cast<uint64_t>(G) * K;
+  {
+    const uint64_t da[2] = {UK, SM}, sa[1] = {UK};
+    const uint64_t db[2] = {UN, GK}, sb[1] = {UN};
+    const uint32_t boxa[2] = {128, 128};
+    const uint32_t boxb[2] = {static_cast<uint32_t>(std::min(128, bn / 2)), 128};
+    if ((s = encode(&p.tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, a, 2, da, sa, boxa,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "a")) ||
+        (s = encode(&p.tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, 2, db, sb, boxb,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "w")))
+      return s;
+    const bool bf = (d_dtype == DG_BF16);
+    const uint64_t dd[3] = {UN, SM, 1}, sd[2] = {es * UN, es * UN * SM};
+    const uint32_t box[3] = {dg::kEpiCols, 32, 1};
+    if ((s = encode(&p.tmD, bf ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                    d, 3, dd, sd, box, dg::epi_swizzle(es), CU_TENSOR_MAP_L2_PROMOTION_NONE, "d")))
+      return s;
+  }
+
+  // ---- scale records: A per token chunk ([NGK][TC]), W per (entry, group, N tile)
+  std::unique_ptr<dg::PackParams> pk_hold(new dg::PackParams);
+  dg::PackParams &pk = *pk_hold;
+  std::memset(&pk, 0, sizeof(pk));
+  for (int i = 0; i < n_ent; ++i) {
+    pk.g_off[i] = p.sched[i].g_off;
+    pk.row_off[i] = p.sched[i].expert * KB;
+    pk.row_end[i] = pk.row_off[i] + KB;
+  }
+  pk.M = 0;
+  pk.N = N;
+  pk.MC = 0;
+  pk.NT = n_tiles;
+  pk.CB = (bn + 127) / 128;
+  pk.BN = bn;
+  pk.n_entries = n_ent;
+  pk.n_groups = n_ent * NGK;
+  const size_t a_rec = static_cast<size_t>(NGK) * TC * 512;
+  const size_t b_rec = static_cast<size_t>(pk.n_groups) * pk.NT * pk.CB * 512;
+  void *scratch = nullptr;
+  cudaError_t e = cudaMallocFromPoolAsync(&scratch, a_rec + b_rec, dev->pool, stream);
+  if (e != cudaSuccess)
+    return fail(DG_ERR_CUDA, "%s: scale scratch (%zu bytes): %s", fn, a_rec + b_rec,
+                cudaGetErrorString(e));
+  dg::TokenPackParams tp;
+  tp.sfa = sfa;
+  tp.sfa_p = static_cast<uint32_t *>(scratch);
+  tp.sum_m = sum_m;
+  tp.KB = KB;
+  tp.NGK = NGK;
+  tp.TC = TC;
+  pk.sfa = nullptr;
+  pk.sfb = sfw;
+  pk.sfa_p = nullptr;
+  pk.sfb_p = reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(scratch) + a_rec);
+  {
+    const uint64_t rec[1] = {512};
+    const uint64_t dpa[2] = {128, static_cast<uint64_t>(NGK) * TC};
+    const uint64_t dpb[2] = {128, static_cast<uint64_t>(pk.n_groups) * pk.NT * pk.CB};
+    const uint32_t bpa[2] = {128, 1}, bpb[2] = {128, static_cast<uint32_t>(pk.CB)};
+    if ((s = encode(&p.tmSFA, CU_TENSOR_MAP_DATA_TYPE_UINT32, tp.sfa_p, 2, dpa, rec, bpa,
+                    CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE, "sfa records")) ||
+        (s = encode(&p.tmSFB, CU_TENSOR_MAP_DATA_TYPE_UINT32, pk.sfb_p, 2, dpb, rec, bpb,
+                    CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE, "sfw records"))) {
+      cudaFreeAsync(scratch, stream);
+      return s;
+    }
+  }
+  if ((e = dg::launch_pack_token_scales(tp, stream)) != cudaSuccess ||
+      (e = dg::launch_pack_scales(pk, stream)) != cudaSuccess) {
+    cudaFreeAsync(scratch, stream);
+    return fail(DG_ERR_CUDA, "%s: scale pack launch failed: %s", fn, cudaGetErrorString(e));
+  }
+  const int pairs = static_cast<int>(std::min<int64_t>(dev->sms / 2, tiles));
+  e = dg::launch_mgrouped_fp8(p, bn, pairs, stream);
+  cudaFreeAsync(scratch, stream);   // after the GEMM in stream order
+  if (e != cudaSuccess) return fail(DG_ERR_CUDA, "%s: launch failed: %s", fn, cudaGetErrorString(e));
+  return ok();
+}
+
 dg::CastArgs cast_args(const void *x, const uint8_t *x_sf, const int *src_rows, int64_t T_src,
                        int64_t T, int C, void *q, uint8_t *sf) {
   dg::CastArgs a;
@@ -535,6 +722,14 @@ dg_status dg_k_grouped_bf16_wgrad(const void *a, const void *b, void *d, dg_dtyp
   GroupedArgs x{false, false, a, b, nullptr, nullptr, d, d_dtype, c, G, M, N, sum_k, ks_host,
                 ks_dev, 0, reinterpret_cast<cudaStream_t>(stream)};
   return run_grouped(x);
+}
+
+dg_status dg_m_grouped_fp8_dgrad(const void *a, const uint8_t *sfa, const void *w,
+                                 const uint8_t *sfw, void *d, dg_dtype d_dtype, int G, int K,
+                                 int N, int64_t sum_m, const int *ms_host, const int *ms_dev,
+                                 int gran_k, dg_stream_t stream) {
+  return run_mgrouped(a, sfa, w, sfw, d, d_dtype, G, K, N, sum_m, ms_host, ms_dev, gran_k,
+                      reinterpret_cast<cudaStream_t>(stream));
 }
 
 dg_status dg_quant_transpose_fp8(const void *x, int64_t T, int C, void *q, uint8_t *sf,

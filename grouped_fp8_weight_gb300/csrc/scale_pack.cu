@@ -15,6 +15,9 @@
 // where gp runs over the scale groups of all experts with K_e > 0 in schedule
 // order: group j of schedule entry s is gp = g_off[s] + j and covers scale
 // rows k_off[s] / gran_k + 4j .. + 3 (rows past the expert's end are 0).
+// The M-grouped data gradient uses the B records alone (MC = 0) for its
+// weights' scales [G * K / gran_k, N], and its own A records (per token row,
+// pack_token_scales_kernel).
 #include "wgrad_params.h"
 
 namespace dg {
@@ -55,7 +58,29 @@ __global__ void __launch_bounds__(128) pack_scales_kernel(const __grid_constant_
   }
 }
 
+// A's records for the M-grouped data gradient: one CTA per (group, token
+// chunk); thread 4l + q packs the four scale columns of token 128 tc + 32 q + l.
+__global__ void __launch_bounds__(128) pack_token_scales_kernel(const __grid_constant__ TokenPackParams p) {
+  const int j = blockIdx.x, tc = blockIdx.y;
+  const int t = threadIdx.x;
+  const int l = t >> 2, q = t & 3;
+  const int64_t row = 128ll * tc + 32 * q + l;
+  uint32_t w = 0;
+  if (row < p.sum_m)
+    for (int i = 0; i < 4; ++i) {
+      const int col = 4 * j + i;
+      if (col < p.KB) w |= static_cast<uint32_t>(p.sfa[row * p.KB + col]) << (8 * i);
+    }
+  p.sfa_p[(static_cast<int64_t>(j) * p.TC + tc) * 128 + t] = w;
+}
+
 }  // namespace
+
+cudaError_t launch_pack_token_scales(const TokenPackParams &p, cudaStream_t stream) {
+  if (p.NGK <= 0 || p.TC <= 0) return cudaSuccess;
+  pack_token_scales_kernel<<<dim3(p.NGK, p.TC), 128, 0, stream>>>(p);
+  return cudaGetLastError();
+}
 
 size_t plan_scale_pack(WgradParams &p, PackParams &pk, int n_mma, int gran_k, int bn) {
   const int gs = (gran_k == 128) ? 4 : 1;   // k-blocks per scale group

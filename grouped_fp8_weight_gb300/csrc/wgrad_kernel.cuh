@@ -51,9 +51,15 @@
 
 namespace dg {
 
-template <bool kFP8, int kBN, bool kKMajor = false>
+template <bool kFP8, int kBN, bool kKMajor = false, bool kMG = false>
 struct WgradCfg {
   static_assert(!kKMajor || kFP8, "K-major operands: FP8 only");
+  static_assert(!kMG || (kFP8 && !kKMajor), "M-grouped: FP8, K-major A with MN-major B");
+  // Operand majorness: kKMajor makes both operands K-major (NT weight
+  // gradient); the M-grouped data gradient has a K-major A (token rows of dy)
+  // and an MN-major B (the expert weight [K, N]).
+  static constexpr bool A_KM = kKMajor || kMG;
+  static constexpr bool B_KM = kKMajor;
   static constexpr int BM = 128;                        // rows per CTA (pair: 256)
   static constexpr int ELEM = kFP8 ? 1 : 2;
   static constexpr int BK = kFP8 ? 128 : 64;            // tokens per stage
@@ -68,22 +74,23 @@ struct WgradCfg {
   // MN-major tiles are BK token rows of 128-byte swizzle atoms; K-major tiles
   // (NT operands, [M, sum_k] / [N, sum_k]) are BM or BN_CTA rows of BK bytes,
   // 128-byte swizzled in groups of eight rows.
-  static constexpr int A_BYTES = kKMajor ? BM * BK * ELEM : A_ATOMS * ATOM_BYTES;
-  static constexpr int B_BYTES = kKMajor ? BN_CTA * BK * ELEM : B_ATOMS * ATOM_BYTES;
+  static constexpr int A_BYTES = A_KM ? BM * BK * ELEM : A_ATOMS * ATOM_BYTES;
+  static constexpr int B_BYTES = B_KM ? BN_CTA * BK * ELEM : B_ATOMS * ATOM_BYTES;
   // Bytes a stage's B loads bring in: each box is min(ATOM, BN_CTA) columns
   // wide, so a CTA's 112-column half of a 224-wide tile is loaded exactly
   // (its 128-byte swizzled rows keep their 128-byte pitch in shared memory).
   static constexpr int B_BOX_COLS = BN_CTA < ATOM ? BN_CTA : ATOM;
-  static constexpr int B_LOAD_BYTES = kKMajor ? B_BYTES : B_ATOMS * BK * B_BOX_COLS * ELEM;
+  static constexpr int B_LOAD_BYTES = B_KM ? B_BYTES : B_ATOMS * BK * B_BOX_COLS * ELEM;
   // Descriptor start-address step of one MMA along K: MN-major, MMA_K token
   // rows of 128 bytes; K-major, MMA_K elements inside the 128-byte row.
-  static constexpr int KSTEP_BYTES = kKMajor ? MMA_K * ELEM : MMA_K * 128;
+  static constexpr int A_KSTEP = A_KM ? MMA_K * ELEM : MMA_K * 128;
+  static constexpr int B_KSTEP = B_KM ? MMA_K * ELEM : MMA_K * 128;
   // Descriptor strides: SBO = 1024 (8 token rows x 128 B) between K groups,
   // LBO = ATOM_BYTES between 128-byte atoms along M/N.  A single-atom operand
   // never steps along M/N, so its LBO is set to the K-group stride as well.
   static constexpr int A_LBO = A_ATOMS > 1 ? ATOM_BYTES : 1024;
   static constexpr int B_LBO = B_ATOMS > 1 ? ATOM_BYTES : 1024;
-  static constexpr int STAGES = kKMajor ? 6 : 5;   // K-major stages are 30 KB, MN-major 32 KB
+  static constexpr int STAGES = (A_KM && B_KM) ? 6 : 5;   // all-K-major stages are 30 KB, others 32 KB
   static constexpr int NUM_ACC = 2;
   // FP8 scale groups: four UE8M0 rows (four k-blocks at gran_k 128, the four
   // 32-token sub-blocks of one k-block at gran_k 32), in a ring of SF_SLOTS.
@@ -125,18 +132,45 @@ enum : int { W_PROD_EMPTY = 0x01, W_PROD_DRAIN = 0x02, W_PROD_SFE = 0x03, W_MMA_
 
 struct TileCoord {
   int expert, k_off, k_len, m0, n0;   // m0: this CTA's first row; n0: the pair's first column
-  int mt, nt, g_off;                  // M- and N-tile index; first packed scale group of the expert
+  int mt, nt, g_off;                  // M- and N-tile index; first packed scale group of the entry
+  int ka_off;                         // A's offset along K (k_off, or 0 when M-grouped)
+  int rows;                           // M-grouped: this CTA's rows inside the expert (<= 0: none)
+  int k_exp;                          // the entry's k_exp (checked against ks_dev)
 };
 
+// Weight gradient: entry u / tiles_per_group, tiles (M tile, N tile) of the
+// expert's [M, N] output.  M-grouped data gradient: the entry whose tile_off
+// range holds u; its tiles are (256-token chunk, N tile) of the expert's rows,
+// N tiles fastest, and A's rows are the tokens (m0 is a row of the [sum_m, K]
+// operand), B's rows the expert's K rows of W.
+template <bool kMG>
 __device__ __forceinline__ TileCoord tile_coord(const WgradParams &p, int u, int bn,
                                                 uint32_t rank) {
-  const int gi = u / p.tiles_per_group;
-  const int lt = u - gi * p.tiles_per_group;
-  const SchedEntry se = p.sched[gi];
-  const int mt = p.m_fastest ? lt % p.m_tiles : lt / p.n_tiles;
-  const int nt = p.m_fastest ? lt / p.m_tiles : lt % p.n_tiles;
-  return TileCoord{se.expert, se.k_off, se.k_len, mt * 256 + static_cast<int>(rank) * 128,
-                   nt * bn, mt, nt, se.g_off};
+  TileCoord c;
+  if constexpr (kMG) {
+    int lo = 0, hi = p.n_entries - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (p.sched[mid].tile_off <= u) lo = mid; else hi = mid - 1;
+    }
+    const SchedEntry se = p.sched[lo];
+    const int lt = u - se.tile_off;
+    const int mt = lt / p.n_tiles, nt = lt - mt * p.n_tiles;
+    const int r0 = mt * 256 + static_cast<int>(rank) * 128;
+    c.expert = se.expert; c.k_off = se.k_off; c.k_len = se.k_len;
+    c.m0 = se.row_off + r0; c.n0 = nt * bn; c.mt = mt; c.nt = nt; c.g_off = se.g_off;
+    c.ka_off = 0; c.rows = se.k_exp - r0; c.k_exp = se.k_exp;
+  } else {
+    const int gi = u / p.tiles_per_group;
+    const int lt = u - gi * p.tiles_per_group;
+    const SchedEntry se = p.sched[gi];
+    const int mt = p.m_fastest ? lt % p.m_tiles : lt / p.n_tiles;
+    const int nt = p.m_fastest ? lt / p.m_tiles : lt % p.n_tiles;
+    c.expert = se.expert; c.k_off = se.k_off; c.k_len = se.k_len;
+    c.m0 = mt * 256 + static_cast<int>(rank) * 128; c.n0 = nt * bn; c.mt = mt; c.nt = nt;
+    c.g_off = se.g_off; c.ka_off = se.k_off; c.rows = 128; c.k_exp = se.k_exp;
+  }
+  return c;
 }
 
 // Rotation of a tile's k loop.  Tiles running at the same time that share an
@@ -215,7 +249,9 @@ __device__ __forceinline__ bool lane_turn(LaneSched &L, const WgradParams &p, in
     if (L.head > L.tail) return false;
     const int i = (l == 0) ? L.head++ : L.tail--;
     u = owned_tile(i, pid, R);
-    nk = (u < p.num_mma_tiles) ? (p.sched[u / p.tiles_per_group].k_len + bk - 1) / bk : 0;
+    // (M-grouped: every entry's K is the same, sched[0].k_len)
+    const int kl = p.mgroup ? p.sched[0].k_len : p.sched[u / p.tiles_per_group].k_len;
+    nk = (u < p.num_mma_tiles) ? (kl + bk - 1) / bk : 0;
     j = 0;
     if (nk == 0) {   // output-only tile: a completion without MMAs
       c = Chunk{u, 0, 0, 0, l};
@@ -261,10 +297,12 @@ __device__ __forceinline__ int swz_chunk(int i, int row) {
 #define DG_TACC(slot, v)
 #endif
 
-template <bool kFP8, int kBN, int kOut, bool kKMajor, bool kTransD>
+template <bool kFP8, int kBN, int kOut, bool kKMajor, bool kTransD, bool kMG = false>
 __global__ void __launch_bounds__(kWgradThreads, 1)
     kgrouped_wgrad_kernel(const __grid_constant__ WgradParams p) {
-  using Cfg = WgradCfg<kFP8, kBN, kKMajor>;
+  using Cfg = WgradCfg<kFP8, kBN, kKMajor, kMG>;
+  static_assert(!kMG || (!kTransD && (kOut == OUT_F32 || kOut == OUT_BF16)),
+                "M-grouped: direct tiles, no accumulator");
   constexpr int S = Cfg::STAGES;
   constexpr int NS = Cfg::SF_SLOTS;
   extern __shared__ uint8_t smem_raw[];
@@ -344,16 +382,17 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
       Chunk ch;
       while (ok && lane_next(L, p, pid, R, Cfg::BK, ch)) {
         if (ch.nk == 0) continue;
-        const TileCoord tc = tile_coord(p, ch.u, kBN, rank);
+        const TileCoord tc = tile_coord<kMG>(p, ch.u, kBN, rank);
         const int t = ch.u;
-        if (leader && ch.j0 == 0 && p.ks_dev != nullptr && tc.m0 == 0 && tc.n0 == 0 &&
-            p.ks_dev[tc.expert] != p.sched[t / p.tiles_per_group].k_exp)
+        if (leader && ch.j0 == 0 && p.ks_dev != nullptr && tc.mt == 0 && tc.nt == 0 &&
+            p.ks_dev[tc.expert] != tc.k_exp)
           atomicCAS(&p.status->code, DEV_OK, DEV_KS_MISMATCH);
         const int nb = tc.n0 + static_cast<int>(rank) * Cfg::BN_CTA;   // this CTA's B columns
         const KRot rot = tile_rot(tc.mt, tc.nt, ch.nk, Cfg::ROT_UNIT);
         for (int j = ch.j0; j < ch.j1; ++j) {
           const int jj = rot_stage(j, rot);   // stage of the tile's k range at position j
-          const int k = tc.k_off + jj * Cfg::BK;
+          const int k = tc.k_off + jj * Cfg::BK;      // B's row (token) coordinate
+          const int ka = tc.ka_off + jj * Cfg::BK;    // A's (the same unless M-grouped)
           DG_T0(w1);
           ok = mbar_wait(&empty[s], ph ^ 1, abort_flag, lim, p.status, W_PROD_EMPTY, t);
           DG_TACC(0, w1);
@@ -376,21 +415,26 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
             for (int b = 0; b < Cfg::B_ATOMS; ++b)
               tma_load_2d_hint(sb + b * Cfg::ATOM_BYTES, &p.tmB, &tfull[s], nb + b * Cfg::ATOM, k,
                                keep);
-          } else if constexpr (kKMajor) {
-            // one box per operand: BK bytes of tokens x this CTA's rows
-            const uint32_t fbar = mapa_shared(smem_u32(&full[s]), 0);
-            tma_load_2d_pair(sa, &p.tmA, fbar, k, tc.m0, keep);
-            tma_load_2d_pair(sb, &p.tmB, fbar, k, nb, keep);
           } else {
+            // K-major operand: one box of BK bytes along K x this CTA's rows;
+            // MN-major: BK rows along K of 128-byte atoms.
             const uint32_t fbar = mapa_shared(smem_u32(&full[s]), 0);
+            if constexpr (Cfg::A_KM) {
+              tma_load_2d_pair(sa, &p.tmA, fbar, ka, tc.m0, keep);
+            } else {
 #pragma unroll
-            for (int a = 0; a < Cfg::A_ATOMS; ++a)
-              tma_load_2d_pair(sa + a * Cfg::ATOM_BYTES, &p.tmA, fbar, tc.m0 + a * Cfg::ATOM, k,
-                               keep);
+              for (int a = 0; a < Cfg::A_ATOMS; ++a)
+                tma_load_2d_pair(sa + a * Cfg::ATOM_BYTES, &p.tmA, fbar, tc.m0 + a * Cfg::ATOM,
+                                 ka, keep);
+            }
+            if constexpr (Cfg::B_KM) {
+              tma_load_2d_pair(sb, &p.tmB, fbar, k, nb, keep);
+            } else {
 #pragma unroll
-            for (int b = 0; b < Cfg::B_ATOMS; ++b)
-              tma_load_2d_pair(sb + b * Cfg::ATOM_BYTES, &p.tmB, fbar, nb + b * Cfg::ATOM, k,
-                               keep);
+              for (int b = 0; b < Cfg::B_ATOMS; ++b)
+                tma_load_2d_pair(sb + b * Cfg::ATOM_BYTES, &p.tmB, fbar, nb + b * Cfg::ATOM, k,
+                                 keep);
+            }
           }
           ++armed;
           if (++s == S) { s = 0; ph ^= 1; }
@@ -416,19 +460,19 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
       uint32_t ph = 0, gph = 0;
       uint32_t sfa_t = 0, sfb_t = 0;
       bool ok = true;
-      // K-major operands clear the two transpose bits (15: A, 16: B).
+      // A K-major operand clears its transpose bit (15: A, 16: B).
       constexpr uint32_t kIdescBase =
           (kFP8 ? idesc_mxf8(2 * Cfg::BM, kBN, 0, 0) : idesc_bf16(2 * Cfg::BM, kBN)) &
-          (kKMajor ? ~((1u << 15) | (1u << 16)) : ~0u);
+          (Cfg::A_KM ? ~(1u << 15) : ~0u) & (Cfg::B_KM ? ~(1u << 16) : ~0u);
       // Descriptors of stage 0 / scale slot 0; later stages and k-steps add
       // their byte offset >> 4 to the start-address field (shared addresses
       // stay below 256 KB, so the field never carries out).
       // K-major 128-byte swizzle: SBO = 1024 between groups of eight rows
       // (the leading offset is unused there).
       const uint64_t a_desc0 =
-          smem_desc(smem_u32(smem + Cfg::OFF_A), kKMajor ? 16 : Cfg::A_LBO, 1024, 2);
+          smem_desc(smem_u32(smem + Cfg::OFF_A), Cfg::A_KM ? 16 : Cfg::A_LBO, 1024, 2);
       const uint64_t b_desc0 =
-          smem_desc(smem_u32(smem + Cfg::OFF_B), kKMajor ? 16 : Cfg::B_LBO, 1024, 2);
+          smem_desc(smem_u32(smem + Cfg::OFF_B), Cfg::B_KM ? 16 : Cfg::B_LBO, 1024, 2);
       const uint64_t uta_desc0 = smem_desc(smem_u32(smem + Cfg::OFF_UTA), 0, 128, 0);
       const uint64_t utb_desc0 = smem_desc(smem_u32(smem + Cfg::OFF_UTB), 0, 128, 0);
       uint64_t a_desc = a_desc0, b_desc = b_desc0;
@@ -450,7 +494,7 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
           tc_fence_after();
         }
         const uint32_t d_tmem = tmem_base + b * kBN;
-        const TileCoord tcm = tile_coord(p, ch.u, kBN, 0);
+        const TileCoord tcm = tile_coord<kMG>(p, ch.u, kBN, 0);
         const KRot rot = tile_rot(tcm.mt, tcm.nt, ch.nk, Cfg::ROT_UNIT);
         for (int j = ch.j0; j < ch.j1; ++j) {
           const int jj = rot_stage(j, rot);   // k-block of this position
@@ -489,8 +533,8 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
           const uint32_t idesc_j = kIdescBase | ((gs == 4) ? (static_cast<uint32_t>(jj & 3) * 0x20000010u) : 0u);
 #pragma unroll
           for (int ks = 0; ks < Cfg::KSTEPS; ++ks) {
-            const uint64_t ad = a_desc + static_cast<uint64_t>(ks * (Cfg::KSTEP_BYTES >> 4));
-            const uint64_t bd = b_desc + static_cast<uint64_t>(ks * (Cfg::KSTEP_BYTES >> 4));
+            const uint64_t ad = a_desc + static_cast<uint64_t>(ks * (Cfg::A_KSTEP >> 4));
+            const uint64_t bd = b_desc + static_cast<uint64_t>(ks * (Cfg::B_KSTEP >> 4));
             if constexpr (kFP8) {
               const uint32_t idesc = (gs == 4) ? idesc_j : (kIdescBase | (static_cast<uint32_t>(ks) * 0x20000010u));
               mma_mxf8_pair(d_tmem, ad, bd, idesc, sfa_t, sfb_t, (j | ks) != 0);
@@ -544,7 +588,7 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
           const int t = ch.u;
           const int nk = ch.nk;
           const int tail = p.sched[ch.u / p.tiles_per_group].k_len - (nk - 1) * Cfg::BK;
-          const TileCoord tcg = tile_coord(p, ch.u, kBN, 0);
+          const TileCoord tcg = tile_coord<kMG>(p, ch.u, kBN, 0);
           const KRot rot = tile_rot(tcg.mt, tcg.nt, nk, Cfg::ROT_UNIT);
           for (int j = ch.j0; j < ch.j1; ++j) {
             const int jj = rot_stage(j, rot);
@@ -614,7 +658,7 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
               have = lane_next(L, p, pid, R, Cfg::BK, ch);
               if (!have) break;
               if (ch.nk == 0) { have = false; continue; }
-              tc = tile_coord(p, ch.u, kBN, rank);
+              tc = tile_coord<kMG>(p, ch.u, kBN, rank);
               rot = tile_rot(tc.mt, tc.nt, ch.nk, Cfg::ROT_UNIT);
               j = ch.j0;
               continue;
@@ -631,8 +675,12 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
           if (!ok) break;
           if (leader) mbar_arrive_expect_tx(&sfr[g], 2 * (Cfg::UT_A + Cfg::UT_B));
           const int grp = tc.g_off + jj / gs;
+          // A's records: per (group, 128-row chunk); M-grouped, the chunk is a
+          // 128-token chunk of the whole [sum_m, K] operand and the group one
+          // of K's, shared by every expert.
+          const int grp_a = kMG ? jj / gs : grp;
           tma_load_2d_pair(smem + Cfg::OFF_UTA + g * Cfg::UT_A, &p.tmSFA, sfr_leader + 8 * g, 0,
-                           grp * p.sf_mc + tc.m0 / 128, keep);
+                           grp_a * p.sf_mc + tc.m0 / 128, keep);
           tma_load_2d_pair(smem + Cfg::OFF_UTB + g * Cfg::UT_B, &p.tmSFB, sfr_leader + 8 * g, 0,
                            (grp * p.n_tiles + tc.nt) * Cfg::SF_CHUNKS_B, keep);
           ++ig;
@@ -673,8 +721,12 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
     while (lane_next(L, p, pid, R, Cfg::BK, ch)) {
       if (ch.nk > 0 && ch.j1 != ch.nk) continue;   // only tile completions
       const int t = ch.u;
-      const TileCoord tc = tile_coord(p, ch.u, kBN, rank);
+      const TileCoord tc = tile_coord<kMG>(p, ch.u, kBN, rank);
       const bool mma_tile = ch.nk > 0;
+      // M-grouped: a CTA whose 128 rows lie past its expert's last token
+      // (the second half of an expert's last 256-row chunk) stores nothing.
+      const bool store = !kMG || tc.rows > 0;
+      const int dz = kMG ? 0 : tc.expert;   // D's third coordinate
       const int b = ch.lane;
       if (mma_tile) {
         DG_T0(w0);
@@ -788,11 +840,11 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
         }
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) {
+        if (lane == 0 && store) {
           if constexpr (kOut == OUT_F32_REDUCE)
-            tma_reduce_add_3d_hint(&p.tmD, stg, bx, by, tc.expert, stream_out);
+            tma_reduce_add_3d_hint(&p.tmD, stg, bx, by, dz, stream_out);
           else
-            tma_store_3d_hint(&p.tmD, stg, bx, by, tc.expert, stream_out);
+            tma_store_3d_hint(&p.tmD, stg, bx, by, dz, stream_out);
           bulk_commit();
         }
       }
@@ -824,10 +876,10 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
   }
 }
 
-template <bool kFP8, int kBN, int kOut, bool kKMajor, bool kTransD>
+template <bool kFP8, int kBN, int kOut, bool kKMajor, bool kTransD, bool kMG = false>
 cudaError_t launch_wgrad_variant(const WgradParams &p, int pairs, cudaStream_t stream) {
-  using Cfg = WgradCfg<kFP8, kBN, kKMajor>;
-  auto kern = kgrouped_wgrad_kernel<kFP8, kBN, kOut, kKMajor, kTransD>;
+  using Cfg = WgradCfg<kFP8, kBN, kKMajor, kMG>;
+  auto kern = kgrouped_wgrad_kernel<kFP8, kBN, kOut, kKMajor, kTransD, kMG>;
   static bool attr_set = false;
   static int max_pairs = 0;
   cudaLaunchAttribute attr[1];
@@ -870,6 +922,19 @@ cudaError_t launch_wgrad_bn(const WgradParams &p, int pairs, cudaStream_t stream
       return launch_wgrad_variant<kFP8, kBN, OUT_F32_C, kKMajor, kTransD>(p, pairs, stream);
     case OUT_BF16:
       return launch_wgrad_variant<kFP8, kBN, OUT_BF16, kKMajor, kTransD>(p, pairs, stream);
+  }
+  return cudaErrorInvalidValue;
+}
+
+// M-grouped FP8 data gradient: A K-major (token rows of dy), B MN-major (the
+// expert weights), direct tiles, FP32 or BF16 output.
+template <int kBN>
+cudaError_t launch_mgrouped_bn(const WgradParams &p, int pairs, cudaStream_t stream) {
+  switch (p.out_mode) {
+    case OUT_F32:
+      return launch_wgrad_variant<true, kBN, OUT_F32, false, false, true>(p, pairs, stream);
+    case OUT_BF16:
+      return launch_wgrad_variant<true, kBN, OUT_BF16, false, false, true>(p, pairs, stream);
   }
   return cudaErrorInvalidValue;
 }

@@ -15,12 +15,20 @@ constexpr int kMaxGroups = 1024;   // must equal DG_MAX_GROUPS
 // for in-place accumulation one part of a long expert's).  Entries with
 // k_len > 0 come first, longest first; after them come experts whose output
 // must be written without a GEMM (K_e == 0 with no accumulator or a separate one).
+//
+// M-grouped data gradient (mgroup = 1): one entry per expert with tokens, in
+// expert order; k_off = e * K (the expert's first row of W), k_len = K,
+// k_exp = the expert's token count, row_off its first token row, tile_off its
+// first tile (tiles: 256-token chunks x N tiles), g_off its first packed scale
+// group of W.
 struct SchedEntry {
   int expert;
   int k_off;
   int k_len;
   int g_off;   // FP8: first packed scale group of this entry
   int k_exp;   // the expert's whole token count (an entry may be one part of it)
+  int row_off;    // M-grouped only
+  int tile_off;   // M-grouped only
 };
 
 enum OutMode : int {
@@ -46,6 +54,8 @@ struct WgradParams {
   int m_fastest;       // tile order inside an expert: 1 = M tiles vary fastest
   int sf_mc;           // FP8: packed A records per scale group (2 * m_tiles)
   int chunk;           // stages of a lane-0 tile per turn (FP8: a multiple of 4)
+  int mgroup;          // 1: M-grouped data gradient (see SchedEntry)
+  int n_entries;       // M-grouped: schedule entries
   uint64_t wait_limit_ns;
   DevStatus *status;
   const int *ks_dev;
@@ -54,6 +64,7 @@ struct WgradParams {
 #endif
   SchedEntry sched[kMaxGroups];
 };
+static_assert(sizeof(WgradParams) <= 32764, "kernel parameters are limited to 32764 bytes");
 
 // FP8 scale packing (scale_pack.cu): every scale group the GEMM uses, laid
 // out as the 32-row x 16-byte records tcgen05.cp copies into tensor memory.
@@ -78,6 +89,18 @@ size_t plan_scale_pack(WgradParams &p, PackParams &pk, int n_mma, int gran_k, in
 void bind_scale_pack(PackParams &pk, void *scratch, const uint8_t *sfa, const uint8_t *sfb);
 cudaError_t launch_pack_scales(const PackParams &p, cudaStream_t stream);
 
+// M-grouped data gradient: A's scales are per token row ([sum_m, KB] with
+// KB = K / gran_k scale columns); their records are [NGK][TC][128 words]
+// (group j of K's scale columns 4j..4j+3, 128-token chunk tc: word 4l + q
+// holds the scales of token 128 tc + 32 q + l), zero past sum_m or KB.
+struct TokenPackParams {
+  const uint8_t *sfa;
+  uint32_t *sfa_p;
+  int64_t sum_m;
+  int KB, NGK, TC;
+};
+cudaError_t launch_pack_token_scales(const TokenPackParams &p, cudaStream_t stream);
+
 // Launchers (one translation unit each): `pairs` clusters of two CTAs (capped
 // at the number that fit the GPU at once).  Return the launch error, if any.
 cudaError_t launch_kgrouped_fp8(const WgradParams &p, int block_n, int pairs,
@@ -93,6 +116,10 @@ cudaError_t launch_kgrouped_fp8_t(const WgradParams &p, int block_n, int pairs,
                                   cudaStream_t stream);
 cudaError_t launch_kgrouped_fp8_nt_t(const WgradParams &p, int block_n, int pairs,
                                      cudaStream_t stream);
+// M-grouped FP8 data gradient (tmA maps dy as {K, sum_m}, tmB the weights as
+// {N, G * K}, tmD the output as {N, sum_m, 1}).
+cudaError_t launch_mgrouped_fp8(const WgradParams &p, int block_n, int pairs,
+                                cudaStream_t stream);
 // Column-block casts (quant.cu).  x is BF16 [T_src, C], or, with x_sf set,
 // E4M3 codes [T_src, C] with one UE8M0 scale per token per 128 channels
 // (x_sf [T_src, C / 128]).  With src_rows set, output row t takes source row

@@ -68,6 +68,11 @@ WORKLOADS = {
     # Full pipeline: bf16 dY [T, 4096] and X [T, 7168] -> cast -> K-grouped FP8 GEMM.
     "pipeline_fp8_g64": Workload("pipeline_fp8_g64", 4, 64, 4096, 7168, 131072,
                                  "pipeline", "f32", True, c_std=0.01),
+    # M-grouped data gradient of the up/gate projection: dx [T, 7168] =
+    # dh [T, 4096] W[e] with W [32, 4096, 7168]; here M is the contraction
+    # (h_out = 4096), N = h_in, sum_k the tokens.  Operands are E4M3 codes.
+    "moe_upgate_dgrad_fp8_g32": Workload("moe_upgate_dgrad_fp8_g32", 6, 32, 4096, 7168, 32768,
+                                         "dgrad", "bf16", False),
 }
 
 
@@ -144,6 +149,35 @@ def draw_operands(name: str, device: str = "cpu", rows_limit: Optional[int] = No
         C = torch.randn(w.G, w.M, w.N, generator=gen, device=device,
                         dtype=torch.float32) * w.c_std
     return ks, A, B, C
+
+
+def random_codes(shape, gen: torch.Generator, device: str = "cpu") -> torch.Tensor:
+    """Uniform random E4M3 bytes, the two NaN encodings (0x7F, 0xFF) replaced
+    by 0x3C and 0xBC."""
+    c = torch.randint(0, 256, shape, generator=gen, device=device, dtype=torch.uint8)
+    nan = (c & 0x7F) == 0x7F
+    return torch.where(nan, c ^ 0x43, c)
+
+
+def draw_dgrad_operands(name: str, device: str = "cpu"):
+    """Draw (ms, a, sfa, w, sfw) for an M-grouped data-gradient workload:
+    a E4M3 [sum_m, K] with UE8M0 sfa [sum_m, K / gran_k] in [120, 136), w E4M3
+    [G, K, N] with sfw [G, K / gran_k, N] in [112, 128), all uint8.  Token
+    counts as ``expert_counts``.  ``device="cuda"`` draws on the GPU (values
+    differ from the CPU draw)."""
+    w = WORKLOADS[name]
+    gen = torch.Generator(device="cpu").manual_seed(w.seed)
+    ms = expert_counts(w, gen)
+    if device != "cpu":
+        gen = torch.Generator(device=device).manual_seed(w.seed)
+    K, N, g = w.M, w.N, w.gran_k
+    a = random_codes((w.sum_k, K), gen, device)
+    sfa = torch.randint(120, 136, (w.sum_k, K // g), generator=gen, device=device,
+                        dtype=torch.uint8)
+    wt = random_codes((w.G, K, N), gen, device)
+    sfw = torch.randint(112, 128, (w.G, K // g, N), generator=gen, device=device,
+                        dtype=torch.uint8)
+    return ms, a, sfa, wt, sfw
 
 
 def random_counts(G: int, sum_blocks: int, unit: int, seed: int, empty: int = 0) -> list:

@@ -170,6 +170,56 @@ dg_status dg_k_grouped_bf16_wgrad(const void *a, const void *b,
                                   dg_stream_t stream);
 
 /*
+ * dg_m_grouped_fp8_dgrad -- the other GEMM of a MoE expert's backward, the
+ * data (input) gradient, M-grouped over a contiguous token layout:
+ *
+ *   D[t, n] = sum_{k < K} fp8(A[t, k]) 2^(sfa[t, k / gran_k] - 127)
+ *                         * fp8(W[e, k, n]) 2^(sfw[e, k / gran_k, n] - 127)
+ *
+ * for every token row t of expert e (rows [off_e, off_e + M_e), off_e =
+ * M_0 + ... + M_{e-1}): dx_e = dy_e W_e with W_e the expert's [h_out, h_in]
+ * weight as a linear layer stores it.
+ *
+ * Source: "Is DeepGEMM directly applicable to backward in training?"
+ * (YouJiacheng, 26 Feb 2025: a GEMM's backward is two GEMMs; LyricZhao, same
+ * day: the library ships the data-gradient GEMM, the weight gradient needs
+ * the K-grouped kernel and the fused casts).  The pages give no layout or
+ * scale recipe for it; this entry point takes the plainest one consistent
+ * with the rest of the path: dy as the forward pass stores activations (E4M3,
+ * one UE8M0 scale per token per gran_k channels, the 1 x 128 tile) and the
+ * weight with one UE8M0 scale per column per gran_k rows of K (a 128 x 128
+ * block scale is this with each block's byte repeated over its columns), both
+ * scales along the contraction axis as the tensor core's block-scaled MMA
+ * consumes them ("UE8M0 Format in DeepGEMM", packed scales on SM100).
+ *
+ *   a      E4M3 [sum_m, K], row-major (K contiguous): dy, experts' rows contiguous.
+ *   sfa    UE8M0 [sum_m, K / gran_k].
+ *   w      E4M3 [G, K, N], row-major (N contiguous).
+ *   sfw    UE8M0 [G, K / gran_k, N].
+ *   d      [sum_m, N] FP32 (d_dtype DG_F32) or BF16 (DG_BF16, round to
+ *          nearest even), written (no accumulator).
+ *   G      0 <= G <= DG_MAX_GROUPS; K a positive multiple of 128; N a
+ *          positive multiple of 16; G * K < 2^31.
+ *   ms_host, ms_dev  per-expert token counts (host / device copies, same
+ *          values), each >= 0 and a multiple of 128 (the padded MoE layout,
+ *          dg_moe_layout_plan); they sum to sum_m.  Experts with no tokens
+ *          own no rows.  ms_dev is checked by the kernel as ks_dev is.
+ *   gran_k 32 or 128.
+ * Work enqueued: two scale-packing passes (dy's scales per 128-token chunk,
+ * the weights' per N tile), then the GEMM.  Scratch from the device pool:
+ * (ceil(K / 128 / g) x (sum_m / 128 + 1) + E x ceil(K / 128 / g) x
+ * ceil(N / BN) x ceil(BN / 128)) x 512 bytes, g = 4 at gran_k 128 and 1 at
+ * 32, E the experts with tokens, BN as above.  Errors as for the weight
+ * gradient calls; DG_ERR_UNSUPPORTED also for an output of 2^40 bytes or more.
+ */
+dg_status dg_m_grouped_fp8_dgrad(const void *a, const uint8_t *sfa,
+                                 const void *w, const uint8_t *sfw,
+                                 void *d, dg_dtype d_dtype,
+                                 int G, int K, int N, int64_t sum_m,
+                                 const int *ms_host, const int *ms_dev,
+                                 int gran_k, dg_stream_t stream);
+
+/*
  * dg_quant_transpose_fp8 -- the cast a weight-gradient GEMM needs: per column,
  * per gran_k-token block, one power-of-two scale, values to E4M3.
  *

@@ -20,6 +20,8 @@ Modules
            recomputed activation a), cast by columns.
 ``wgrad``  the K-grouped GEMM ``D[e] = C[e] + A_e^T B_e`` with per-block
            scales, in float64, plus the tolerance budget ``S = sum |a b s|``.
+``dgrad``  the M-grouped data gradient ``dx_e = dy_e W_e`` (the other GEMM of
+           an expert's backward) with per-block scales along K, in float64.
 
 Parity status: every function here is pinned by ``tests/test_oracle_*.py``
 against something other than itself (a library cast, exact rational
@@ -36,3 +38,4 @@ from .wgrad import (  # noqa: F401
     kgrouped_fp8_wgrad_rows, kgrouped_bf16_wgrad_rows, expert_offsets,
     fp32_bound, bf16_bound,
 )
+from .dgrad import mgrouped_fp8_dgrad, mgrouped_fp8_dgrad_rows  # noqa: F401

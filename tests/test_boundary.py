@@ -103,6 +103,46 @@ def test_noalloc_rejects_oversize_scale_records_without_device(L):
     assert "packed scale factors need" in L.dg_last_error().decode()
 
 
+def _dgrad(L, **kw):
+    a = dict(a=FAKE, sfa=FAKE, w=FAKE, sfw=FAKE, d=FAKE, dt=B.DG_BF16, G=2, K=256, N=224,
+             sm=384, ms=[128, 256], msd=FAKE, g=128)
+    a.update(kw)
+    return L.dg_m_grouped_fp8_dgrad(a["a"], a["sfa"], a["w"], a["sfw"], a["d"], a["dt"], a["G"],
+                                    a["K"], a["N"], a["sm"], _ks(a["ms"]), a["msd"], a["g"], None)
+
+
+@pytest.mark.parametrize("kw,why", [
+    (dict(G=-1), "G = -1"),
+    (dict(K=192), "K = 192 must be a positive multiple of 128"),
+    (dict(K=0), "multiple of 128"),
+    (dict(N=200), "N = 200 must be a positive multiple of 16"),
+    (dict(g=64), "gran_k = 64"),
+    (dict(dt=5), "unknown output dtype"),
+    (dict(ms=[128, 64], sm=192), "not a multiple of 128"),
+    (dict(ms=[512, -128]), "< 0"),
+    (dict(sm=512), "!= sum_m"),
+    (dict(msd=None), "ms_host and ms_dev"),
+    (dict(G=0, sm=128), "G = 0 but"),
+    (dict(a=MIS), "16-byte aligned"),
+    (dict(sfw=None), "16-byte aligned"),
+    (dict(d=None), "16-byte aligned"),
+])
+def test_dgrad_invalid_arguments(L, kw, why):
+    assert _dgrad(L, **kw) == B.DG_ERR_INVALID_ARG
+    assert "dg_m_grouped_fp8_dgrad" in L.dg_last_error().decode()
+    assert why in L.dg_last_error().decode()
+
+
+def test_dgrad_limits_and_empty_problems_without_device(L):
+    ms = [0] * (B.DG_MAX_GROUPS + 1)
+    assert _dgrad(L, G=len(ms), ms=ms, sm=0) == B.DG_ERR_UNSUPPORTED
+    assert _dgrad(L, G=2, K=2 ** 30, ms=[128, 256]) == B.DG_ERR_UNSUPPORTED   # G * K >= 2^31
+    assert _dgrad(L, G=0, sm=0) == B.DG_OK
+    # every expert empty: no rows to write, nothing enqueued
+    assert _dgrad(L, ms=[0, 0], sm=0, a=None, w=None, d=None) == B.DG_OK
+    assert L.dg_last_error().decode() == ""
+
+
 def _bf16(L, **kw):
     a = dict(a=FAKE, b=FAKE, d=FAKE, dt=B.DG_F32, c=None, G=2, M=64, N=72, sk=7, ks=[3, 4],
              ksd=FAKE)
