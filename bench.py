@@ -267,6 +267,40 @@ def measure_casts(w, ks, dev, stream, pk, steps):
     return out
 
 
+def measure_dgrad(dev, stream, pk, steps):
+    """The M-grouped FP8 data gradient of the up/gate projection (dx = dh W_e,
+    K = 4096, N = 7168, the headline's token counts law), device-resident,
+    CUDA events; one dg_m_grouped_fp8_dgrad call = two scale-packing passes +
+    the GEMM."""
+    import grouped_fp8_weight_gb300 as dg
+    name = "moe_upgate_dgrad_fp8_g32"
+    w = workloads.WORKLOADS[name]
+    ms_, a, sfa, wt, sfw = workloads.draw_dgrad_operands(name, device=str(dev))
+    ms_dev = torch.tensor(ms_, dtype=torch.int32, device=dev)
+    d = torch.empty(w.sum_k, w.N, dtype=torch.bfloat16, device=dev)
+
+    def call():
+        dg.dg_m_grouped_fp8_dgrad(a, sfa, wt, sfw, d, ms_, ms_dev, 128)
+
+    for _ in range(3):
+        call()
+    ms = time_events(call, steps, stream)
+    dg.dg_sync_check()
+    live = sum(1 for m in ms_ if m > 0)
+    K, N, T = w.M, w.N, w.sum_k
+    nbytes = T * K + T * (K // 128) + live * K * N + live * (K // 128) * N + T * N * 2
+    flops = 2.0 * T * K * N
+    fp8_peak = 2.0 * pk["bf16_tflops"]
+    tflops = flops / (ms * 1e-3) / 1e12
+    del a, sfa, wt, sfw, d
+    return {"ms": ms, "value": tflops, "unit": "TFLOP/s", "workload": name,
+            "kernel": "kgrouped_wgrad_kernel<fp8, 224, bf16, M-grouped>",
+            "shape": {"G": w.G, "K": K, "N": N, "sum_m": T, "experts_with_tokens": live},
+            "launches_per_step": 3, "bound": "tensor", "achieved": tflops, "peak": fp8_peak,
+            "frac": tflops / fp8_peak, "algorithmic_bytes": nbytes,
+            "hbm_frac": nbytes / (ms * 1e-3) / 1e9 / pk["hbm_gbs"]}
+
+
 def profile_inplace(w, args, dev, pk, rank):
     """Device-timed leg of the in-place workloads: the BF16 fine-grained GEMM
     (BF16 operands, D += A^T B) or the pipeline's FP8 GEMM (operands cast from
@@ -424,6 +458,12 @@ def run_ours(args):
             raise SystemExit("the full bench line runs the FP8 workloads; the BF16 and "
                              "pipeline workloads have the device-timed --profile leg only")
         return profile_inplace(w, args, dev, pk, rank)
+    if args.profile_dgrad:
+        # the data-gradient leg alone, for kernel captures
+        out = measure_dgrad(dev, torch.cuda.current_stream(), pk, args.steps)
+        if rank == 0:
+            print(json.dumps({"profile_only": True, "dgrad": out}), flush=True)
+        return 0
     if args.profile_casts:
         # the cast legs alone (no GEMM buffers), for kernel captures
         ks = workloads.counts_for(w.name)
@@ -537,6 +577,7 @@ def run_ours(args):
 
     casts = measure_casts(w, ks, dev, stream, pk, max(5, args.steps // 4))
     dg.dg_sync_check()
+    dgrad = measure_dgrad(dev, stream, pk, max(5, args.steps // 4))
 
     # ---- end to end through the C ABI with pinned host buffers
     h_qa, h_sa = qa.cpu().pin_memory(), sa.cpu().pin_memory()
@@ -571,7 +612,8 @@ def run_ours(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "e4m3 x e4m3 -> f32", "data": "synthetic",
             "config": workload_config(w, ks), "fp8_peak_frac": tflops / fp8_peak,
-            "roofline": roof, "pipeline": pipeline, "nt": nt, "casts": casts, "e2e": e2e,
+            "roofline": roof, "pipeline": pipeline, "nt": nt, "casts": casts, "dgrad": dgrad,
+            "e2e": e2e,
             "cpu_baseline": cpu,
             "clocks": clk.summary(),
             # per step: the scale-packing pass and the GEMM kernel
@@ -594,6 +636,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile", action="store_true",
                     help="device-timed leg only (for ncu captures)")
+    ap.add_argument("--profile-dgrad", action="store_true",
+                    help="time the M-grouped data-gradient leg alone (for kernel captures)")
     ap.add_argument("--profile-casts", action="store_true",
                     help="the cast legs only, `--steps` launches each (for ncu captures)")
     args = ap.parse_args()
