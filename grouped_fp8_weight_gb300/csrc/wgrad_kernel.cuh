@@ -66,7 +66,9 @@ struct WgradCfg {
   static constexpr int ATOM = 128 / ELEM;               // elements per swizzle row
   static constexpr int MMA_K = kFP8 ? 32 : 16;          // K of one tcgen05.mma
   static constexpr int KSTEPS = BK / MMA_K;             // 4
-  static constexpr int ROT_UNIT = kFP8 ? 8 : 16;        // k-loop rotation step (stages)
+  // k-loop rotation step (stages); M-grouped tiles are not rotated (a unit
+  // longer than any k loop): their operand slices all stay in L2.
+  static constexpr int ROT_UNIT = kMG ? (1 << 24) : kFP8 ? 8 : 16;
   static constexpr int BN_CTA = kBN / 2;                // B columns held per CTA
   static constexpr int A_ATOMS = BM / ATOM;
   static constexpr int B_ATOMS = (BN_CTA + ATOM - 1) / ATOM;
@@ -247,7 +249,9 @@ __device__ __forceinline__ bool lane_turn(LaneSched &L, const WgradParams &p, in
                                           int bk, int l, int &u, int &nk, int &j, Chunk &c) {
   if (u < 0) {
     if (L.head > L.tail) return false;
-    const int i = (l == 0) ? L.head++ : L.tail--;
+    // M-grouped tiles all have the same length: both lanes take the next tile
+    // in order, so the running tiles share one expert's weight in L2.
+    const int i = (l == 0 || p.mgroup) ? L.head++ : L.tail--;
     u = owned_tile(i, pid, R);
     // (M-grouped: every entry's K is the same, sched[0].k_len)
     const int kl = p.mgroup ? p.sched[0].k_len : p.sched[u / p.tiles_per_group].k_len;

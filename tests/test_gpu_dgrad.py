@@ -4,7 +4,7 @@ tolerances (FP32 |D_gpu - D| <= 1e-5 S + 1e-6; BF16 2^-7 |D| + 1e-5 S + 1e-6;
 integer-valued problems bit-exact).  Cases span several tiles, ragged N
 tiles, experts whose token count is an odd multiple of 128 (the second half
 of their last 256-row chunk is not stored), empty experts, partial scale
-groups along K, rotated k loops, and the full-size up/gate workload on
+groups along K, long k loops, and the full-size up/gate workload on
 sampled rows."""
 import numpy as np
 import pytest
@@ -58,9 +58,9 @@ def test_dgrad_ragged_shapes(K, N):
 
 
 @pytest.mark.parametrize("gran_k", [128, 32])
-def test_dgrad_many_tiles_and_rotated_k_loops(gran_k):
-    """More tiles than CTA pairs (both lanes busy), K long enough that tile
-    k loops start rotated, one expert of a single 128-row half."""
+def test_dgrad_many_tiles_and_long_k_loops(gran_k):
+    """More tiles than CTA pairs (both lanes busy), 16-stage k loops, one
+    expert of a single 128-row half."""
     ms, K, N = [128 * 21, 128 * 7, 0, 128 * 3, 128], 2048, 896
     a, sfa, w, sfw = _case(ms, K, N, 41, gran_k)
     d = run_dgrad(a, sfa, w, sfw, ms, gran_k, "bf16")
