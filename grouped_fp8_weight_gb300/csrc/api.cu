@@ -424,6 +424,7 @@ dg_status run_grouped(const GroupedArgs &x) {
   }
 
   // ---- launch: one persistent CTA pair per two SMs (or per tile when fewer)
+  dg::set_derived(p, n_groups);
   const int pairs = std::min(dev->sms / 2, p.num_tiles);
   e = !x.fp8              ? dg::launch_kgrouped_bf16(p, bn, pairs, x.stream)
       : x.kmajor && trans  ? dg::launch_kgrouped_fp8_nt_t(p, bn, pairs, x.stream)
@@ -616,6 +617,7 @@ dg_status run_mgrouped(const void *a, const uint8_t *sfa, const void *w, const u
     cudaFreeAsync(scratch, stream);
     return fail(DG_ERR_CUDA, "%s: scale pack launch failed: %s", fn, cudaGetErrorString(e));
   }
+  dg::set_derived(p, n_ent);
   const int pairs = static_cast<int>(std::min<int64_t>(dev->sms / 2, tiles));
   e = dg::launch_mgrouped_fp8(p, bn, pairs, stream);
   cudaFreeAsync(scratch, stream);   // after the GEMM in stream order

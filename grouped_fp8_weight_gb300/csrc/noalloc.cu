@@ -281,6 +281,7 @@ extern "C" dg_status dg_k_grouped_fp8_wgrad_noalloc(
   if (e != cudaSuccess) return nfail(DG_ERR_CUDA, "%s: clearing scratch: %s", fn, cudaGetErrorString(e));
   if (sf_bytes > 0 && (e = dg::launch_pack_scales(pk, st)) != cudaSuccess)
     return nfail(DG_ERR_CUDA, "%s: scale pack launch failed: %s", fn, cudaGetErrorString(e));
+  dg::set_derived(p, order_len);
   e = dg::launch_kgrouped_fp8(p, bn, std::min(dev->sms / 2, p.num_tiles), st);
   if (e != cudaSuccess) return nfail(DG_ERR_CUDA, "%s: launch failed: %s", fn, cudaGetErrorString(e));
   dg::set_last_error("");

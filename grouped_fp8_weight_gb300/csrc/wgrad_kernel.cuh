@@ -121,7 +121,14 @@ struct WgradCfg {
   // cbar[4 warps x 2], sfr/sfe[SLOTS], drain
   static constexpr int NUM_BARS = 4 * STAGES + 2 * NUM_ACC + 8 + 2 * SF_SLOTS + 1;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
-  static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;   // + alignment slack
+  // The schedule table is read once per chunk by every role; indexed reads
+  // of the kernel parameters miss the constant cache, so it is copied here
+  // when it fits (up to SCHED_CAP entries, from the space left over).
+  static constexpr int OFF_SCHED = OFF_MISC + 16;
+  static constexpr int SCHED_LEFT = (232448 - 1024 - OFF_SCHED) / static_cast<int>(sizeof(SchedEntry));
+  static constexpr int SCHED_CAP = SCHED_LEFT < 256 ? SCHED_LEFT : 256;
+  static constexpr int SMEM_BYTES = OFF_SCHED + SCHED_CAP * static_cast<int>(sizeof(SchedEntry)) + 1024;
+  static_assert(SCHED_CAP >= 64, "schedule table in shared memory");
   static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
 
@@ -146,28 +153,30 @@ struct TileCoord {
 // N tiles fastest, and A's rows are the tokens (m0 is a row of the [sum_m, K]
 // operand), B's rows the expert's K rows of W.
 template <bool kMG>
-__device__ __forceinline__ TileCoord tile_coord(const WgradParams &p, int u, int bn,
-                                                uint32_t rank) {
+__device__ __forceinline__ TileCoord tile_coord(const WgradParams &p, const SchedEntry *sched,
+                                                int u, int bn, uint32_t rank) {
   TileCoord c;
   if constexpr (kMG) {
     int lo = 0, hi = p.n_entries - 1;
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
-      if (p.sched[mid].tile_off <= u) lo = mid; else hi = mid - 1;
+      if (sched[mid].tile_off <= u) lo = mid; else hi = mid - 1;
     }
-    const SchedEntry se = p.sched[lo];
+    const SchedEntry se = sched[lo];
     const int lt = u - se.tile_off;
-    const int mt = lt / p.n_tiles, nt = lt - mt * p.n_tiles;
+    const int mt = fast_div(lt, p.div_nt), nt = lt - mt * p.n_tiles;
     const int r0 = mt * 256 + static_cast<int>(rank) * 128;
     c.expert = se.expert; c.k_off = se.k_off; c.k_len = se.k_len;
     c.m0 = se.row_off + r0; c.n0 = nt * bn; c.mt = mt; c.nt = nt; c.g_off = se.g_off;
     c.ka_off = 0; c.rows = se.k_exp - r0; c.k_exp = se.k_exp;
   } else {
-    const int gi = u / p.tiles_per_group;
+    const int gi = fast_div(u, p.div_tpg);
     const int lt = u - gi * p.tiles_per_group;
-    const SchedEntry se = p.sched[gi];
-    const int mt = p.m_fastest ? lt % p.m_tiles : lt / p.n_tiles;
-    const int nt = p.m_fastest ? lt / p.m_tiles : lt % p.n_tiles;
+    const SchedEntry se = sched[gi];
+    const int q = fast_div(lt, p.m_fastest ? p.div_mt : p.div_nt);
+    const int r = lt - q * (p.m_fastest ? p.m_tiles : p.n_tiles);
+    const int mt = p.m_fastest ? r : q;
+    const int nt = p.m_fastest ? q : r;
     c.expert = se.expert; c.k_off = se.k_off; c.k_len = se.k_len;
     c.m0 = mt * 256 + static_cast<int>(rank) * 128; c.n0 = nt * bn; c.mt = mt; c.nt = nt;
     c.g_off = se.g_off; c.ka_off = se.k_off; c.rows = 128; c.k_exp = se.k_exp;
@@ -190,7 +199,9 @@ struct KRot {
 __device__ __forceinline__ KRot tile_rot(int mt, int nt, int nk, int unit) {
   const int F = nk & ~3;
   const int nu = F / unit;
-  return KRot{nu >= 2 ? unit * ((mt + nt) % nu) : 0, F};
+  // start unit: (mt + nt) modulo the largest power of two <= nu (no division)
+  const int mask = nu >= 2 ? (1 << (31 - __clz(nu))) - 1 : 0;
+  return KRot{unit * ((mt + nt) & mask), F};
 }
 // Stage of the tile's k range visited at loop position j.
 __device__ __forceinline__ int rot_stage(int j, KRot r) {
@@ -228,13 +239,16 @@ struct Chunk {
 };
 
 struct LaneSched {
+  const SchedEntry *sched;   // the schedule table (shared memory, or the parameters)
   int head, tail;   // list positions not yet taken: [head, tail]
   int u0, nk0, j0;  // lane 0: tile (-1: none), its stages, next stage
   int u1, nk1, j1;  // lane 1
   int turn;
 };
 
-__device__ __forceinline__ void lane_init(LaneSched &L, const WgradParams &p, int pid, int R) {
+__device__ __forceinline__ void lane_init(LaneSched &L, const WgradParams &p, int pid, int R,
+                                          const SchedEntry *sched) {
+  L.sched = sched;
   L.head = 0;
   L.tail = owned_count(p.num_tiles, pid, R) - 1;
   L.u0 = L.u1 = -1;
@@ -254,7 +268,7 @@ __device__ __forceinline__ bool lane_turn(LaneSched &L, const WgradParams &p, in
     const int i = (l == 0 || p.mgroup) ? L.head++ : L.tail--;
     u = owned_tile(i, pid, R);
     // (M-grouped: every entry's K is the same, sched[0].k_len)
-    const int kl = p.mgroup ? p.sched[0].k_len : p.sched[u / p.tiles_per_group].k_len;
+    const int kl = p.mgroup ? L.sched[0].k_len : L.sched[fast_div(u, p.div_tpg)].k_len;
     nk = (u < p.num_mma_tiles) ? (kl + bk - 1) / bk : 0;
     j = 0;
     if (nk == 0) {   // output-only tile: a completion without MMAs
@@ -366,6 +380,15 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
     tmem_alloc_pair(tmem_slot, Cfg::TMEM_COLS);
     tmem_relinquish_pair();
   }
+  const bool sched_smem = p.n_sched <= Cfg::SCHED_CAP;
+  SchedEntry *sched_s = reinterpret_cast<SchedEntry *>(smem + Cfg::OFF_SCHED);
+  if (sched_smem) {
+    const int *src = reinterpret_cast<const int *>(p.sched);
+    int *dst = reinterpret_cast<int *>(sched_s);
+    constexpr int W = static_cast<int>(sizeof(SchedEntry) / sizeof(int));
+    for (int i = threadIdx.x; i < p.n_sched * W; i += blockDim.x) dst[i] = src[i];
+  }
+  const SchedEntry *sched = sched_smem ? sched_s : p.sched;
   tc_fence_before();
   cluster_sync();                   // barriers of both CTAs initialised before any remote arrive
   tc_fence_after();
@@ -382,11 +405,11 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
       uint32_t ph = 0, armed = 0;
       bool ok = true;
       LaneSched L;
-      lane_init(L, p, pid, R);
+      lane_init(L, p, pid, R, sched);
       Chunk ch;
       while (ok && lane_next(L, p, pid, R, Cfg::BK, ch)) {
         if (ch.nk == 0) continue;
-        const TileCoord tc = tile_coord<kMG>(p, ch.u, kBN, rank);
+        const TileCoord tc = tile_coord<kMG>(p, sched, ch.u, kBN, rank);
         const int t = ch.u;
         if (leader && ch.j0 == 0 && p.ks_dev != nullptr && tc.mt == 0 && tc.nt == 0 &&
             p.ks_dev[tc.expert] != tc.k_exp)
@@ -483,7 +506,7 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
       uint32_t uses[2] = {0, 0};   // tiles completed per accumulator buffer
       uint32_t gate_ph = 0;        // BF16: phase bit of each slot's `gate` (tail stages only)
       LaneSched L;
-      lane_init(L, p, pid, R);
+      lane_init(L, p, pid, R, sched);
       Chunk ch;
       while (ok && lane_next(L, p, pid, R, Cfg::BK, ch)) {
         if (ch.nk == 0) continue;
@@ -498,7 +521,7 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
           tc_fence_after();
         }
         const uint32_t d_tmem = tmem_base + b * kBN;
-        const TileCoord tcm = tile_coord<kMG>(p, ch.u, kBN, 0);
+        const TileCoord tcm = tile_coord<kMG>(p, sched, ch.u, kBN, 0);
         const KRot rot = tile_rot(tcm.mt, tcm.nt, ch.nk, Cfg::ROT_UNIT);
         for (int j = ch.j0; j < ch.j1; ++j) {
           const int jj = rot_stage(j, rot);   // k-block of this position
@@ -585,14 +608,14 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
         bool ok = true;
         const uint32_t gate_leader = mapa_shared(smem_u32(&gate[0]), 0);
         LaneSched L;
-        lane_init(L, p, pid, R);
+        lane_init(L, p, pid, R, sched);
         Chunk ch;
         while (ok && lane_next(L, p, pid, R, Cfg::BK, ch)) {
           if (ch.nk == 0) continue;
           const int t = ch.u;
           const int nk = ch.nk;
-          const int tail = p.sched[ch.u / p.tiles_per_group].k_len - (nk - 1) * Cfg::BK;
-          const TileCoord tcg = tile_coord<kMG>(p, ch.u, kBN, 0);
+          const int tail = sched[fast_div(ch.u, p.div_tpg)].k_len - (nk - 1) * Cfg::BK;
+          const TileCoord tcg = tile_coord<kMG>(p, sched, ch.u, kBN, 0);
           const KRot rot = tile_rot(tcg.mt, tcg.nt, nk, Cfg::ROT_UNIT);
           for (int j = ch.j0; j < ch.j1; ++j) {
             const int jj = rot_stage(j, rot);
@@ -646,7 +669,7 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
         const uint64_t keep = l2_policy_evict_last();   // B's records serve every M tile
         const uint32_t sfr_leader = mapa_shared(smem_u32(&sfr[0]), 0);
         LaneSched L;
-        lane_init(L, p, pid, R);
+        lane_init(L, p, pid, R, sched);
         Chunk ch;
         TileCoord tc{};
         int j = 0, jj = 0;            // position in the current chunk, its k-block
@@ -662,7 +685,7 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
               have = lane_next(L, p, pid, R, Cfg::BK, ch);
               if (!have) break;
               if (ch.nk == 0) { have = false; continue; }
-              tc = tile_coord<kMG>(p, ch.u, kBN, rank);
+              tc = tile_coord<kMG>(p, sched, ch.u, kBN, rank);
               rot = tile_rot(tc.mt, tc.nt, ch.nk, Cfg::ROT_UNIT);
               j = ch.j0;
               continue;
@@ -720,12 +743,12 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
     constexpr int EC = Cfg::EC;
     uint32_t r[EC];   // tensor-memory chunk in flight
     LaneSched L;
-    lane_init(L, p, pid, R);
+    lane_init(L, p, pid, R, sched);
     Chunk ch;
     while (lane_next(L, p, pid, R, Cfg::BK, ch)) {
       if (ch.nk > 0 && ch.j1 != ch.nk) continue;   // only tile completions
       const int t = ch.u;
-      const TileCoord tc = tile_coord<kMG>(p, ch.u, kBN, rank);
+      const TileCoord tc = tile_coord<kMG>(p, sched, ch.u, kBN, rank);
       const bool mma_tile = ch.nk > 0;
       // M-grouped: a CTA whose 128 rows lie past its expert's last token
       // (the second half of an expert's last 256-row chunk) stores nothing.

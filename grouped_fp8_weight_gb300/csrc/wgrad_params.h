@@ -31,6 +31,29 @@ struct SchedEntry {
   int tile_off;   // M-grouped only
 };
 
+// Division by an invariant divisor d >= 1 for numerators x < 2^31
+// (Granlund and Montgomery, "Division by Invariant Integers using
+// Multiplication", PLDI 1994): with l = ceil(log2 d) and p = 31 + l,
+// mul = ceil(2^p / d) fits 32 bits and x / d = umulhi(x, mul) >> (p - 32);
+// d == 1 is the identity (mul = 0).
+struct FastDiv {
+  uint32_t mul;
+  uint32_t shift;
+};
+inline FastDiv make_fastdiv(uint32_t d) {
+  FastDiv f{0, 0};
+  if (d <= 1) return f;
+  uint32_t l = 0;
+  while ((1ull << l) < d) ++l;
+  const uint32_t p = 31 + l;
+  f.mul = static_cast<uint32_t>(((1ull << p) + d - 1) / d);
+  f.shift = p - 32;
+  return f;
+}
+__device__ __forceinline__ int fast_div(int x, FastDiv f) {
+  return f.mul == 0 ? x : static_cast<int>(__umulhi(static_cast<uint32_t>(x), f.mul) >> f.shift);
+}
+
 enum OutMode : int {
   OUT_F32 = 0,         // D = acc
   OUT_F32_REDUCE = 1,  // D += acc (C aliases D), done by TMA reduce-add
@@ -56,6 +79,8 @@ struct WgradParams {
   int chunk;           // stages of a lane-0 tile per turn (FP8: a multiple of 4)
   int mgroup;          // 1: M-grouped data gradient (see SchedEntry)
   int n_entries;       // M-grouped: schedule entries
+  int n_sched;         // valid entries of sched (copied to shared memory when they fit)
+  FastDiv div_tpg, div_mt, div_nt;   // by tiles_per_group, m_tiles, n_tiles
   uint64_t wait_limit_ns;
   DevStatus *status;
   const int *ks_dev;
@@ -65,6 +90,14 @@ struct WgradParams {
   SchedEntry sched[kMaxGroups];
 };
 static_assert(sizeof(WgradParams) <= 32764, "kernel parameters are limited to 32764 bytes");
+
+// Host: the fields derived from the tile counts, and the schedule length.
+inline void set_derived(WgradParams &p, int n_sched) {
+  p.n_sched = n_sched;
+  p.div_tpg = make_fastdiv(static_cast<uint32_t>(p.tiles_per_group > 0 ? p.tiles_per_group : 1));
+  p.div_mt = make_fastdiv(static_cast<uint32_t>(p.m_tiles > 0 ? p.m_tiles : 1));
+  p.div_nt = make_fastdiv(static_cast<uint32_t>(p.n_tiles > 0 ? p.n_tiles : 1));
+}
 
 // FP8 scale packing (scale_pack.cu): every scale group the GEMM uses, laid
 // out as the 32-row x 16-byte records tcgen05.cp copies into tensor memory.
