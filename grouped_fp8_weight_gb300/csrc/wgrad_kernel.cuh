@@ -351,6 +351,8 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
   const int R = gridDim.x >> 1;                     // number of pairs
   // k-blocks covered by one scale group
   const int gs = kFP8 ? (p.gran_k == 128 ? 4 : 1) : 1;
+  // gs is 1 or 4: group tests by mask and shift (no runtime division per stage)
+  const int gs_mask = gs - 1, gs_shift = (gs == 4) ? 2 : 0;
 #ifdef DG_KERNEL_TIMERS
   unsigned long long tm[7] = {0, 0, 0, 0, 0, 0, 0};
   const unsigned long long t_start = clock64();
@@ -526,7 +528,7 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
         for (int j = ch.j0; j < ch.j1; ++j) {
           const int jj = rot_stage(j, rot);   // k-block of this position
           if constexpr (kFP8) {
-            if (jj % gs == 0) {
+            if ((jj & gs_mask) == 0) {
               DG_T0(w1);
               ok = mbar_wait(&sfr[g], gph, abort_flag, lim, p.status, W_MMA_SFR, t);
               DG_TACC(2, w1);
@@ -691,7 +693,7 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
               continue;
             }
             jj = rot_stage(j, rot);
-            if (jj % gs == 0) found = true; else ++j;
+            if ((jj & gs_mask) == 0) found = true; else ++j;
           }
           if (!found) break;
           const int g = ig % NS;
@@ -701,11 +703,11 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
           DG_TACC(2, w0);
           if (!ok) break;
           if (leader) mbar_arrive_expect_tx(&sfr[g], 2 * (Cfg::UT_A + Cfg::UT_B));
-          const int grp = tc.g_off + jj / gs;
+          const int grp = tc.g_off + (jj >> gs_shift);
           // A's records: per (group, 128-row chunk); M-grouped, the chunk is a
           // 128-token chunk of the whole [sum_m, K] operand and the group one
           // of K's, shared by every expert.
-          const int grp_a = kMG ? jj / gs : grp;
+          const int grp_a = kMG ? (jj >> gs_shift) : grp;
           tma_load_2d_pair(smem + Cfg::OFF_UTA + g * Cfg::UT_A, &p.tmSFA, sfr_leader + 8 * g, 0,
                            grp_a * p.sf_mc + tc.m0 / 128, keep);
           tma_load_2d_pair(smem + Cfg::OFF_UTB + g * Cfg::UT_B, &p.tmSFB, sfr_leader + 8 * g, 0,
