@@ -18,7 +18,7 @@
 // lane 0's (long) tile with the whole of lane 1's (short) tile, so the
 // epilogue drains short tiles while a long one accumulates.
 //
-// Roles per CTA (224 threads):
+// Roles per CTA (224 threads; 352 with transposed tiles):
 //   warp 0      TMA producer (one thread): A/B stages of 128 (FP8) or 64
 //               (BF16) tokens; both CTAs' bytes complete on the even CTA's
 //               `full` barrier.
@@ -28,7 +28,9 @@
 //   warps 2..5  epilogue, one warp per tensor-memory lane quadrant (32 rows),
 //               each on its own: tensor memory -> registers -> swizzled
 //               shared-memory staging -> TMA store (or TMA reduce-add for
-//               in-place D += acc) of 32-row x kEpiCols boxes.
+//               in-place D += acc) of 32-row x kEpiCols boxes.  Transposed
+//               tiles add warps 7..10: two warps per quadrant, each over
+//               every other 32-column chunk.
 //   warp 6      FP8: scale loader -- fetches each scale group's packed
 //               records (written beforehand by the scale pack pass in the
 //               layout tcgen05.cp copies into tensor memory) up to five groups
@@ -51,8 +53,16 @@
 
 namespace dg {
 
-template <bool kFP8, int kBN, bool kKMajor = false, bool kMG = false>
+template <bool kFP8, int kBN, bool kKMajor = false, bool kMG = false, bool kTransD = false>
 struct WgradCfg {
+  // Epilogue warps: one per tensor-memory lane quadrant (warps 2..5), or, for
+  // transposed tiles (whose staging is a scattered 4-byte write per element),
+  // two per quadrant (warps 2..5 and 7..10) each draining every other
+  // 32-column chunk with one staging buffer, which releases an accumulator in
+  // about half the time.  Roles: warp 0 producer, 1 MMA, 6 scale loader /
+  // BF16 gate, the rest epilogue.
+  static constexpr int EPI_WARPS = kTransD ? 8 : 4;
+  static constexpr int THREADS = 32 * (3 + EPI_WARPS);
   static_assert(!kKMajor || kFP8, "K-major operands: FP8 only");
   static_assert(!kMG || (kFP8 && !kKMajor), "M-grouped: FP8, K-major A with MN-major B");
   // Operand majorness: kKMajor makes both operands K-major (NT weight
@@ -106,7 +116,7 @@ struct WgradCfg {
   static constexpr int SF_COL0 = NUM_ACC * kBN;
   static constexpr int EC = kEpiCols;                   // output columns per epilogue chunk
   static constexpr int WSTG_BYTES = 32 * EC * 4;        // per epilogue warp and buffer: 32 FP32 rows
-  static constexpr int EPI_BUFS = 2;                    // staging buffers per epilogue warp
+  static constexpr int EPI_BUFS = 8 / EPI_WARPS;        // staging buffers per epilogue warp
   static constexpr int TMEM_COLS = 512;
   static_assert(SF_COL0 + SF_SLOTS * SF_COLS <= TMEM_COLS, "tmem budget");
   static_assert(kBN % 32 == 0 && kBN <= 256, "block N");
@@ -114,7 +124,8 @@ struct WgradCfg {
   static constexpr int OFF_B = 0;
   static constexpr int OFF_A = OFF_B + STAGES * B_BYTES;
   static constexpr int OFF_STG = OFF_A + STAGES * A_BYTES;
-  static constexpr int OFF_UTA = OFF_STG + 4 * EPI_BUFS * WSTG_BYTES;
+  static constexpr int OFF_UTA = OFF_STG + EPI_WARPS * EPI_BUFS * WSTG_BYTES;
+  static_assert(EPI_WARPS * EPI_BUFS == 8, "eight staging buffers and separate-C barriers");
   static constexpr int OFF_UTB = OFF_UTA + SF_SLOTS * UT_A;
   static constexpr int OFF_BAR = (OFF_UTB + SF_SLOTS * UT_B + 7) / 8 * 8;
   // barriers: full[S], empty[S], gate[S], tfull[S], accf[2], acce[2],
@@ -132,7 +143,6 @@ struct WgradCfg {
   static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
 
-constexpr int kWgradThreads = 224;
 
 // Roles' wait sites, reported in DevStatus::where.
 enum : int { W_PROD_EMPTY = 0x01, W_PROD_DRAIN = 0x02, W_PROD_SFE = 0x03, W_MMA_ACCE = 0x11,
@@ -316,9 +326,9 @@ __device__ __forceinline__ int swz_chunk(int i, int row) {
 #endif
 
 template <bool kFP8, int kBN, int kOut, bool kKMajor, bool kTransD, bool kMG = false>
-__global__ void __launch_bounds__(kWgradThreads, 1)
+__global__ void __launch_bounds__((WgradCfg<kFP8, kBN, kKMajor, kMG, kTransD>::THREADS), 1)
     kgrouped_wgrad_kernel(const __grid_constant__ WgradParams p) {
-  using Cfg = WgradCfg<kFP8, kBN, kKMajor, kMG>;
+  using Cfg = WgradCfg<kFP8, kBN, kKMajor, kMG, kTransD>;
   static_assert(!kMG || (!kTransD && (kOut == OUT_F32 || kOut == OUT_BF16)),
                 "M-grouped: direct tiles, no accumulator");
   constexpr int S = Cfg::STAGES;
@@ -367,9 +377,9 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&accf[i], 1);
-      mbar_init(&acce[i], 8);       // four epilogue warps in each CTA
+      mbar_init(&acce[i], 2 * Cfg::EPI_WARPS);   // every epilogue warp of both CTAs
     }
-    for (int i = 0; i < 8; ++i) mbar_init(&cbar[i], 1);
+    for (int i = 0; i < Cfg::EPI_WARPS * Cfg::EPI_BUFS; ++i) mbar_init(&cbar[i], 1);
     for (int i = 0; i < NS; ++i) {
       mbar_init(&sfr[i], 1);
       mbar_init(&sfe[i], 1);
@@ -735,13 +745,16 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
     // another: tcgen05.ld of EC columns -> one of its EPI_BUFS swizzled
     // staging buffers -> TMA store (or reduce-add) of that 32-row box.
     const int q = warp & 3;               // tensor-memory lane quadrant of this warp
+    const int ew = warp < 6 ? warp - 2 : warp - 3;   // epilogue warp index
+    constexpr int CSTEP = Cfg::EPI_WARPS / 4;         // warps per quadrant
+    const int half = ew >> 2;                         // first chunk of this warp
     uint32_t uses[2] = {0, 0}, nchunk = 0;
     uint32_t cuse[2] = {0, 0};
     constexpr bool kHasC = (kOut == OUT_F32_C);
     const uint64_t stream_out = l2_policy_evict_first();   // D is written once
     const uint32_t acce_leader = mapa_shared(smem_u32(&acce[0]), 0);
-    uint8_t *wstg = smem + Cfg::OFF_STG + q * Cfg::EPI_BUFS * Cfg::WSTG_BYTES;
-    uint64_t *wcbar = cbar + 2 * q;
+    uint8_t *wstg = smem + Cfg::OFF_STG + ew * Cfg::EPI_BUFS * Cfg::WSTG_BYTES;
+    uint64_t *wcbar = cbar + Cfg::EPI_BUFS * ew;
     constexpr int EC = Cfg::EC;
     uint32_t r[EC];   // tensor-memory chunk in flight
     LaneSched L;
@@ -768,9 +781,15 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
       const int nch = (ncols + EC - 1) / EC;
       const int row0 = tc.m0 + 32 * q;    // first output row of this warp's boxes
       const uint32_t tmem_row = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + b * kBN;
-      if (mma_tile) tmem_ld_row<EC>(tmem_row, r);
+      if (mma_tile && half < nch) tmem_ld_row<EC>(tmem_row + EC * half, r);
+      if (mma_tile && half >= nch) {
+        // no chunk of this tile for this warp: release the accumulator now
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_remote(acce_leader + 8 * b);
+      }
       bool ok = true;
-      for (int c = 0; c < nch; ++c, ++nchunk) {
+      for (int c = half; c < nch; c += CSTEP, ++nchunk) {
         const int sbuf = static_cast<int>(nchunk % Cfg::EPI_BUFS);
         uint8_t *stg = wstg + sbuf * Cfg::WSTG_BYTES;
         DG_T0(w1);
@@ -788,14 +807,14 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
         }
         float v[EC];
         if (mma_tile) {
-          // Chunk c was requested one iteration earlier; request chunk c + 1
-          // now so that it streams in while this one is staged.
+          // Chunk c was requested one iteration earlier; request this warp's
+          // next chunk now so that it streams in while this one is staged.
           tmem_wait_ld();
           tmem_reg_fence_n<EC>(r);
 #pragma unroll
           for (int i = 0; i < EC; ++i) v[i] = __uint_as_float(r[i]);
-          if (c + 1 < nch) {
-            tmem_ld_row<EC>(tmem_row + EC * (c + 1), r);
+          if (c + CSTEP < nch) {
+            tmem_ld_row<EC>(tmem_row + EC * (c + CSTEP), r);
           } else {
             // Every read of this buffer has completed (tcgen05.wait::ld above);
             // the tcgen05 fence orders them before the release, so a CTA-scope
@@ -907,7 +926,7 @@ __global__ void __launch_bounds__(kWgradThreads, 1)
 
 template <bool kFP8, int kBN, int kOut, bool kKMajor, bool kTransD, bool kMG = false>
 cudaError_t launch_wgrad_variant(const WgradParams &p, int pairs, cudaStream_t stream) {
-  using Cfg = WgradCfg<kFP8, kBN, kKMajor, kMG>;
+  using Cfg = WgradCfg<kFP8, kBN, kKMajor, kMG, kTransD>;
   auto kern = kgrouped_wgrad_kernel<kFP8, kBN, kOut, kKMajor, kTransD, kMG>;
   static bool attr_set = false;
   static int max_pairs = 0;
@@ -917,7 +936,7 @@ cudaError_t launch_wgrad_variant(const WgradParams &p, int pairs, cudaStream_t s
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.blockDim = dim3(kWgradThreads, 1, 1);
+  cfg.blockDim = dim3(Cfg::THREADS, 1, 1);
   cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
   cfg.stream = stream;
   cfg.attrs = attr;
