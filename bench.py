@@ -267,6 +267,36 @@ def measure_casts(w, ks, dev, stream, pk, steps):
     return out
 
 
+def measure_tiny(dev, stream, steps):
+    """Latency of the tiny in-place workload (G = 4, M = 128, N = 256,
+    ks = [128, 0, 256, 128], D += A^T B): host time per call (validation,
+    planning, tensor maps, two launches; calls issued back to back) and device
+    time per call (CUDA events over the same back-to-back calls)."""
+    import time
+    import grouped_fp8_weight_gb300 as dg
+    w = workloads.WORKLOADS["fp8_tiny_g4"]
+    ks, _, _, qa, sa, qb, sb = make_inputs(w, dev)
+    ks_dev = torch.tensor(ks, dtype=torch.int32, device=dev)
+    d = torch.zeros(w.G, w.M, w.N, dtype=torch.float32, device=dev)
+
+    def call():
+        dg.dg_k_grouped_fp8_wgrad(qa, sa, qb, sb, d, d, ks, ks_dev, 128)
+
+    for _ in range(10):
+        call()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        call()
+    host_us = (time.perf_counter() - t0) / steps * 1e6
+    torch.cuda.synchronize()
+    dev_ms = time_events(call, steps, stream)
+    dg.dg_sync_check()
+    return {"workload": w.name, "host_us_per_call": host_us, "device_us_per_call": dev_ms * 1e3,
+            "launches_per_call": 2, "flops": w.flops,
+            "note": "back-to-back calls; the device time includes the scale-pack launch"}
+
+
 def measure_dgrad(dev, stream, pk, steps):
     """The M-grouped FP8 data gradient of the up/gate projection (dx = dh W_e,
     K = 4096, N = 7168, the headline's token counts law), device-resident,
@@ -458,6 +488,11 @@ def run_ours(args):
             raise SystemExit("the full bench line runs the FP8 workloads; the BF16 and "
                              "pipeline workloads have the device-timed --profile leg only")
         return profile_inplace(w, args, dev, pk, rank)
+    if args.profile_tiny:
+        out = measure_tiny(dev, torch.cuda.current_stream(), max(args.steps, 50))
+        if rank == 0:
+            print(json.dumps({"profile_only": True, "tiny": out}), flush=True)
+        return 0
     if args.profile_dgrad:
         # the data-gradient leg alone, for kernel captures
         out = measure_dgrad(dev, torch.cuda.current_stream(), pk, args.steps)
@@ -578,6 +613,7 @@ def run_ours(args):
     casts = measure_casts(w, ks, dev, stream, pk, max(5, args.steps // 4))
     dg.dg_sync_check()
     dgrad = measure_dgrad(dev, stream, pk, max(5, args.steps // 4))
+    tiny = measure_tiny(dev, stream, 200)
 
     # ---- end to end through the C ABI with pinned host buffers
     h_qa, h_sa = qa.cpu().pin_memory(), sa.cpu().pin_memory()
@@ -613,6 +649,7 @@ def run_ours(args):
             "dtype": "e4m3 x e4m3 -> f32", "data": "synthetic",
             "config": workload_config(w, ks), "fp8_peak_frac": tflops / fp8_peak,
             "roofline": roof, "pipeline": pipeline, "nt": nt, "casts": casts, "dgrad": dgrad,
+            "tiny": tiny,
             "e2e": e2e,
             "cpu_baseline": cpu,
             "clocks": clk.summary(),
@@ -636,6 +673,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile", action="store_true",
                     help="device-timed leg only (for ncu captures)")
+    ap.add_argument("--profile-tiny", action="store_true",
+                    help="time the tiny in-place workload's call latency alone")
     ap.add_argument("--profile-dgrad", action="store_true",
                     help="time the M-grouped data-gradient leg alone (for kernel captures)")
     ap.add_argument("--profile-casts", action="store_true",
