@@ -316,6 +316,17 @@ def measure_dgrad(dev, stream, pk, steps):
         call()
     ms = time_events(call, steps, stream)
     dg.dg_sync_check()
+    # the same with the weights stored K-major, [G, N, K]
+    wt_k = wt.transpose(1, 2).contiguous()
+
+    def call_nt():
+        dg.dg_m_grouped_fp8_dgrad_nt(a, sfa, wt_k, sfw, d, ms_, ms_dev, 128)
+
+    for _ in range(3):
+        call_nt()
+    ms_nt = time_events(call_nt, steps, stream)
+    dg.dg_sync_check()
+    del wt_k
     live = sum(1 for m in ms_ if m > 0)
     K, N, T = w.M, w.N, w.sum_k
     nbytes = T * K + T * (K // 128) + live * K * N + live * (K // 128) * N + T * N * 2
@@ -328,7 +339,10 @@ def measure_dgrad(dev, stream, pk, steps):
             "shape": {"G": w.G, "K": K, "N": N, "sum_m": T, "experts_with_tokens": live},
             "launches_per_step": 3, "bound": "tensor", "achieved": tflops, "peak": fp8_peak,
             "frac": tflops / fp8_peak, "algorithmic_bytes": nbytes,
-            "hbm_frac": nbytes / (ms * 1e-3) / 1e9 / pk["hbm_gbs"]}
+            "hbm_frac": nbytes / (ms * 1e-3) / 1e9 / pk["hbm_gbs"],
+            "kmajor_weights": {"ms": ms_nt, "value": flops / (ms_nt * 1e-3) / 1e12,
+                               "frac": flops / (ms_nt * 1e-3) / 1e12 / fp8_peak,
+                               "entry": "dg_m_grouped_fp8_dgrad_nt (W [G, N, K])"}}
 
 
 def profile_inplace(w, args, dev, pk, rank):

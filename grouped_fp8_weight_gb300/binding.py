@@ -36,6 +36,8 @@ SIGNATURES = {
     "dg_k_grouped_bf16_wgrad": (_I, [_VP, _VP, _VP, _I, _FP, _I, _I, _I, _I64, _IP, _IP, _VP]),
     "dg_m_grouped_fp8_dgrad": (_I, [_VP, _U8P, _VP, _U8P, _VP, _I, _I, _I, _I, _I64, _IP, _IP,
                                     _I, _VP]),
+    "dg_m_grouped_fp8_dgrad_nt": (_I, [_VP, _U8P, _VP, _U8P, _VP, _I, _I, _I, _I, _I64, _IP,
+                                       _IP, _I, _VP]),
     "dg_quant_transpose_fp8": (_I, [_VP, _I64, _I, _VP, _U8P, _I, _I, _VP]),
     "dg_requant_transpose_fp8": (_I, [_VP, _U8P, _I64, _I, _VP, _U8P, _I, _I, _VP]),
     "dg_quant_moe_layout_fp8": (_I, [_VP, _U8P, _I64, _I, _IP, _I64, _VP, _U8P, _I, _I, _VP]),
@@ -181,7 +183,7 @@ def dg_k_grouped_bf16_wgrad(a, b, d, c, ks_host, ks_dev, stream=None):
 
 
 def dg_m_grouped_fp8_dgrad(a, sfa, w, sfw, d, ms_host, ms_dev, gran_k: int = 128,
-                           stream=None):
+                           stream=None, w_kmajor: bool = False):
     """D[t] = dy[t] W_e for the token rows t of expert e (M-grouped, contiguous).
 
     a: E4M3 [sum_m, K] (or uint8 codes), sfa: uint8 [sum_m, K / gran_k];
@@ -197,20 +199,31 @@ def dg_m_grouped_fp8_dgrad(a, sfa, w, sfw, d, ms_host, ms_dev, gran_k: int = 128
     _need(sfw, torch.uint8, "sfw", 3)
     if d.dim() != 2 or d.dtype not in (torch.float32, torch.bfloat16) or not d.is_contiguous():
         raise ValueError("d: expected contiguous float32/bfloat16 [sum_m, N]")
-    G, K, N = w8.shape
+    if w_kmajor:
+        G, N, K = w8.shape
+    else:
+        G, K, N = w8.shape
     sum_m = a8.shape[0]
     if a8.shape[1] != K or tuple(d.shape) != (sum_m, N):
-        raise ValueError("operand shapes do not match: a [sum_m, K], w [G, K, N], d [sum_m, N]")
+        raise ValueError("operand shapes do not match: a [sum_m, K], w [G, K, N] (or [G, N, K] "
+                         "K-major), d [sum_m, N]")
     if tuple(sfa.shape) != (sum_m, K // gran_k) or tuple(sfw.shape) != (G, K // gran_k, N):
         raise ValueError("scale shapes: sfa [sum_m, K / gran_k], sfw [G, K / gran_k, N]")
     _need(ms_dev, torch.int32, "ms_dev", 1)
     mh, g = _ks_host(ms_host)
     if g != G or ms_dev.numel() != G:
         raise ValueError("ms must have G entries")
-    _check(lib().dg_m_grouped_fp8_dgrad(
-        _dptr(a8), _dptr(sfa), _dptr(w8), _dptr(sfw), _dptr(d),
-        DG_BF16 if d.dtype == torch.bfloat16 else DG_F32,
-        G, K, N, sum_m, mh, _dptr(ms_dev), gran_k, _stream(stream)))
+    fn = lib().dg_m_grouped_fp8_dgrad_nt if w_kmajor else lib().dg_m_grouped_fp8_dgrad
+    _check(fn(_dptr(a8), _dptr(sfa), _dptr(w8), _dptr(sfw), _dptr(d),
+              DG_BF16 if d.dtype == torch.bfloat16 else DG_F32,
+              G, K, N, sum_m, mh, _dptr(ms_dev), gran_k, _stream(stream)))
+
+
+def dg_m_grouped_fp8_dgrad_nt(a, sfa, w, sfw, d, ms_host, ms_dev, gran_k: int = 128,
+                              stream=None):
+    """As dg_m_grouped_fp8_dgrad with the weights stored K-major: w [G, N, K]
+    (scales still sfw [G, K / gran_k, N])."""
+    dg_m_grouped_fp8_dgrad(a, sfa, w, sfw, d, ms_host, ms_dev, gran_k, stream, w_kmajor=True)
 
 
 def dg_quant_transpose_fp8(x, q, sf, layout: str = "token", gran_k: int = 128, stream=None):

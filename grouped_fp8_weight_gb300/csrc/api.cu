@@ -441,8 +441,9 @@ dg_status run_grouped(const GroupedArgs &x) {
 // tokens), tensor maps, the two scale-pack passes and the GEMM launch.
 dg_status run_mgrouped(const void *a, const uint8_t *sfa, const void *w, const uint8_t *sfw,
                        void *d, dg_dtype d_dtype, int G, int K, int N, int64_t sum_m,
-                       const int *ms_host, const int *ms_dev, int gran_k, cudaStream_t stream) {
-  const char *fn = "dg_m_grouped_fp8_dgrad";
+                       const int *ms_host, const int *ms_dev, int gran_k, cudaStream_t stream,
+                       bool w_kmajor) {
+  const char *fn = w_kmajor ? "dg_m_grouped_fp8_dgrad_nt" : "dg_m_grouped_fp8_dgrad";
   if (G < 0) return fail(DG_ERR_INVALID_ARG, "%s: G = %d < 0", fn, G);
   if (G > DG_MAX_GROUPS) return fail(DG_ERR_UNSUPPORTED, "%s: G = %d above DG_MAX_GROUPS", fn, G);
   if (K <= 0 || K % 128)
@@ -456,8 +457,8 @@ dg_status run_mgrouped(const void *a, const uint8_t *sfa, const void *w, const u
   if (sum_m < 0) return fail(DG_ERR_INVALID_ARG, "%s: sum_m < 0", fn);
   if (sum_m > (int64_t)0x7FFFFF00)
     return fail(DG_ERR_UNSUPPORTED, "%s: sum_m above 2^31 - 256", fn);
-  if (static_cast<int64_t>(G) * K > 0x7FFFFFFFll)
-    return fail(DG_ERR_UNSUPPORTED, "%s: G * K above 2^31 - 1", fn);
+  if (static_cast<int64_t>(G) * K > 0x7FFFFFFFll || static_cast<int64_t>(G) * N > 0x7FFFFFFFll)
+    return fail(DG_ERR_UNSUPPORTED, "%s: G * K or G * N above 2^31 - 1", fn);
   if (G == 0) {
     if (sum_m != 0) return fail(DG_ERR_INVALID_ARG, "%s: G = 0 but sum_m = %lld", fn, (long long)sum_m);
     return ok();
@@ -503,7 +504,7 @@ dg_status run_mgrouped(const void *a, const uint8_t *sfa, const void *w, const u
     if (m > 0) {
       dg::SchedEntry &se = p.sched[n_ent];
       se.expert = e;
-      se.k_off = e * K;
+      se.k_off = w_kmajor ? e * N : e * K;   // the expert's first row of W
       se.k_len = K;
       se.g_off = n_ent * NGK;
       se.k_exp = m;
@@ -546,11 +547,16 @@ dg_status run_mgrouped(const void *a, const uint8_t *sfa, const void *w, const u
   // ---- tensor maps: dy as {K, sum_m} (K-major boxes of 128 x 128), the
   // weights as {N, G K} (MN-major boxes of bn / 2 x 128), D as {N, sum_m, 1}
   const uint64_t SM = static_cast<uint64_t>(sum_m), UK = K, UN = N, GK = static_cast<uint64_t>(G) * K;
+  const uint64_t GN = static_cast<uint64_t>(G) * N;
   {
     const uint64_t da[2] = {UK, SM}, sa[1] = {UK};
-    const uint64_t db[2] = {UN, GK}, sb[1] = {UN};
+    // W [G, K, N] as {N, G K} with boxes of bn / 2 x 128 rows; K-major W
+    // [G, N, K] as {K, G N} with boxes of 128 bytes of K x bn / 2 rows
+    const uint64_t db[2] = {w_kmajor ? UK : UN, w_kmajor ? GN : GK};
+    const uint64_t sb[1] = {w_kmajor ? UK : UN};
     const uint32_t boxa[2] = {128, 128};
-    const uint32_t boxb[2] = {static_cast<uint32_t>(std::min(128, bn / 2)), 128};
+    const uint32_t boxb[2] = {w_kmajor ? 128u : static_cast<uint32_t>(std::min(128, bn / 2)),
+                              w_kmajor ? static_cast<uint32_t>(bn / 2) : 128u};
     if ((s = encode(&p.tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, a, 2, da, sa, boxa,
                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "a")) ||
         (s = encode(&p.tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, 2, db, sb, boxb,
@@ -619,7 +625,8 @@ dg_status run_mgrouped(const void *a, const uint8_t *sfa, const void *w, const u
   }
   dg::set_derived(p, n_ent);
   const int pairs = static_cast<int>(std::min<int64_t>(dev->sms / 2, tiles));
-  e = dg::launch_mgrouped_fp8(p, bn, pairs, stream);
+  e = w_kmajor ? dg::launch_mgrouped_fp8_nt(p, bn, pairs, stream)
+               : dg::launch_mgrouped_fp8(p, bn, pairs, stream);
   cudaFreeAsync(scratch, stream);   // after the GEMM in stream order
   if (e != cudaSuccess) return fail(DG_ERR_CUDA, "%s: launch failed: %s", fn, cudaGetErrorString(e));
   return ok();
@@ -731,7 +738,15 @@ dg_status dg_m_grouped_fp8_dgrad(const void *a, const uint8_t *sfa, const void *
                                  int N, int64_t sum_m, const int *ms_host, const int *ms_dev,
                                  int gran_k, dg_stream_t stream) {
   return run_mgrouped(a, sfa, w, sfw, d, d_dtype, G, K, N, sum_m, ms_host, ms_dev, gran_k,
-                      reinterpret_cast<cudaStream_t>(stream));
+                      reinterpret_cast<cudaStream_t>(stream), false);
+}
+
+dg_status dg_m_grouped_fp8_dgrad_nt(const void *a, const uint8_t *sfa, const void *w,
+                                    const uint8_t *sfw, void *d, dg_dtype d_dtype, int G, int K,
+                                    int N, int64_t sum_m, const int *ms_host, const int *ms_dev,
+                                    int gran_k, dg_stream_t stream) {
+  return run_mgrouped(a, sfa, w, sfw, d, d_dtype, G, K, N, sum_m, ms_host, ms_dev, gran_k,
+                      reinterpret_cast<cudaStream_t>(stream), true);
 }
 
 dg_status dg_quant_transpose_fp8(const void *x, int64_t T, int C, void *q, uint8_t *sf,

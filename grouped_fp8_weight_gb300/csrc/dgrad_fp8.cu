@@ -14,4 +14,14 @@ cudaError_t launch_mgrouped_fp8(const WgradParams &p, int block_n, int pairs,
   return cudaErrorInvalidValue;
 }
 
+// The same with the weights stored K-major, W [G, N, K] (tmB maps them as {K, G * N}).
+cudaError_t launch_mgrouped_fp8_nt(const WgradParams &p, int block_n, int pairs,
+                                   cudaStream_t stream) {
+  switch (block_n) {
+    case 224: return launch_mgrouped_bn<224, true>(p, pairs, stream);
+    case 128: return launch_mgrouped_bn<128, true>(p, pairs, stream);
+  }
+  return cudaErrorInvalidValue;
+}
+
 }  // namespace dg

@@ -64,10 +64,11 @@ struct WgradCfg {
   static constexpr int EPI_WARPS = kTransD ? 8 : 4;
   static constexpr int THREADS = 32 * (3 + EPI_WARPS);
   static_assert(!kKMajor || kFP8, "K-major operands: FP8 only");
-  static_assert(!kMG || (kFP8 && !kKMajor), "M-grouped: FP8, K-major A with MN-major B");
+  static_assert(!kMG || kFP8, "M-grouped: FP8");
   // Operand majorness: kKMajor makes both operands K-major (NT weight
-  // gradient); the M-grouped data gradient has a K-major A (token rows of dy)
-  // and an MN-major B (the expert weight [K, N]).
+  // gradient; the data gradient with the weight stored [N, K]); the M-grouped
+  // data gradient otherwise has a K-major A (token rows of dy) and an
+  // MN-major B (the expert weight [K, N]).
   static constexpr bool A_KM = kKMajor || kMG;
   static constexpr bool B_KM = kKMajor;
   static constexpr int BM = 128;                        // rows per CTA (pair: 256)
@@ -466,7 +467,10 @@ __global__ void __launch_bounds__((WgradCfg<kFP8, kBN, kKMajor, kMG, kTransD>::T
                 tma_load_2d_pair(sa + a * Cfg::ATOM_BYTES, &p.tmA, fbar, tc.m0 + a * Cfg::ATOM,
                                  ka, keep);
             }
-            if constexpr (Cfg::B_KM) {
+            if constexpr (Cfg::B_KM && kMG) {
+              // the weight stored [G N, K]: K from 0, rows from the expert's first (k_off = e N)
+              tma_load_2d_pair(sb, &p.tmB, fbar, ka, nb + tc.k_off, keep);
+            } else if constexpr (Cfg::B_KM) {
               tma_load_2d_pair(sb, &p.tmB, fbar, k, nb, keep);
             } else {
 #pragma unroll
@@ -976,13 +980,14 @@ cudaError_t launch_wgrad_bn(const WgradParams &p, int pairs, cudaStream_t stream
 
 // M-grouped FP8 data gradient: A K-major (token rows of dy), B MN-major (the
 // expert weights), direct tiles, FP32 or BF16 output.
-template <int kBN>
+// kKMajor: the weights stored K-major, [G, N, K].
+template <int kBN, bool kKMajor = false>
 cudaError_t launch_mgrouped_bn(const WgradParams &p, int pairs, cudaStream_t stream) {
   switch (p.out_mode) {
     case OUT_F32:
-      return launch_wgrad_variant<true, kBN, OUT_F32, false, false, true>(p, pairs, stream);
+      return launch_wgrad_variant<true, kBN, OUT_F32, kKMajor, false, true>(p, pairs, stream);
     case OUT_BF16:
-      return launch_wgrad_variant<true, kBN, OUT_BF16, false, false, true>(p, pairs, stream);
+      return launch_wgrad_variant<true, kBN, OUT_BF16, kKMajor, false, true>(p, pairs, stream);
   }
   return cudaErrorInvalidValue;
 }

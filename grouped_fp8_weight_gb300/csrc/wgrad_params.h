@@ -153,6 +153,10 @@ cudaError_t launch_kgrouped_fp8_nt_t(const WgradParams &p, int block_n, int pair
 // {N, G * K}, tmD the output as {N, sum_m, 1}).
 cudaError_t launch_mgrouped_fp8(const WgradParams &p, int block_n, int pairs,
                                 cudaStream_t stream);
+// The same with the weights stored K-major, W [G, N, K]: tmB maps them as
+// {K, G * N} and each entry's k_off is e * N (its first row of W).
+cudaError_t launch_mgrouped_fp8_nt(const WgradParams &p, int block_n, int pairs,
+                                   cudaStream_t stream);
 // Column-block casts (quant.cu).  x is BF16 [T_src, C], or, with x_sf set,
 // E4M3 codes [T_src, C] with one UE8M0 scale per token per 128 channels
 // (x_sf [T_src, C / 128]).  With src_rows set, output row t takes source row

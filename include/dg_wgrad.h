@@ -220,6 +220,25 @@ dg_status dg_m_grouped_fp8_dgrad(const void *a, const uint8_t *sfa,
                                  int gran_k, dg_stream_t stream);
 
 /*
+ * dg_m_grouped_fp8_dgrad_nt -- dg_m_grouped_fp8_dgrad with the weights stored
+ * K-major: w is E4M3 [G, N, K] (row n of expert e holds W_e[:, n], K
+ * contiguous), the layout of a transposed weight copy.  The scales keep the
+ * layout sfw [G, K / gran_k, N] (one per column n per gran_k rows of K), and
+ * a, sfa, d, ms, gran_k, the result, errors and scratch are as for
+ * dg_m_grouped_fp8_dgrad.  G * N < 2^31.
+ *
+ * Source: as dg_m_grouped_fp8_dgrad; "How to Use DeepGEMM Weight Gradient
+ * Kernels for Training Backward Passes", section "API Entry Points" (the NT
+ * operand form: the second operand transposed, K contiguous).
+ */
+dg_status dg_m_grouped_fp8_dgrad_nt(const void *a, const uint8_t *sfa,
+                                    const void *w, const uint8_t *sfw,
+                                    void *d, dg_dtype d_dtype,
+                                    int G, int K, int N, int64_t sum_m,
+                                    const int *ms_host, const int *ms_dev,
+                                    int gran_k, dg_stream_t stream);
+
+/*
  * dg_quant_transpose_fp8 -- the cast a weight-gradient GEMM needs: per column,
  * per gran_k-token block, one power-of-two scale, values to E4M3.
  *

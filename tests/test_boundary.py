@@ -133,6 +133,16 @@ def test_dgrad_invalid_arguments(L, kw, why):
     assert why in L.dg_last_error().decode()
 
 
+def test_dgrad_nt_invalid_arguments(L):
+    st = L.dg_m_grouped_fp8_dgrad_nt(FAKE, FAKE, FAKE, FAKE, FAKE, B.DG_BF16, 2, 192, 224, 384,
+                                     _ks([128, 256]), FAKE, 128, None)
+    assert st == B.DG_ERR_INVALID_ARG
+    assert "dg_m_grouped_fp8_dgrad_nt" in L.dg_last_error().decode()
+    st = L.dg_m_grouped_fp8_dgrad_nt(FAKE, FAKE, FAKE, FAKE, FAKE, B.DG_BF16, 2, 256, 2 ** 30,
+                                     384, _ks([128, 256]), FAKE, 128, None)
+    assert st == B.DG_ERR_UNSUPPORTED      # G * N >= 2^31
+
+
 def test_dgrad_limits_and_empty_problems_without_device(L):
     ms = [0] * (B.DG_MAX_GROUPS + 1)
     assert _dgrad(L, G=len(ms), ms=ms, sm=0) == B.DG_ERR_UNSUPPORTED

@@ -1,5 +1,6 @@
-"""GPU parity of dg_m_grouped_fp8_dgrad (the M-grouped FP8 data gradient
-dx_e = dy_e W_e) against the float64 oracle, with the weight gradient's
+"""GPU parity of dg_m_grouped_fp8_dgrad and dg_m_grouped_fp8_dgrad_nt (the
+M-grouped FP8 data gradient dx_e = dy_e W_e, weights [G, K, N] or K-major
+[G, N, K]) against the float64 oracle, with the weight gradient's
 tolerances (FP32 |D_gpu - D| <= 1e-5 S + 1e-6; BF16 2^-7 |D| + 1e-5 S + 1e-6;
 integer-valued problems bit-exact).  Cases span several tiles, ragged N
 tiles, experts whose token count is an odd multiple of 128 (the second half
@@ -28,47 +29,57 @@ def _case(ms, K, N, seed, gran_k=128):
     return a, sfa, w, sfw
 
 
-def run_dgrad(a, sfa, w, sfw, ms, gran_k=128, out="bf16"):
+def run_dgrad(a, sfa, w, sfw, ms, gran_k=128, out="bf16", w_kmajor=False):
+    """w is the oracle's [G, K, N]; with w_kmajor it is passed as [G, N, K]
+    to the K-major entry point."""
     dt = torch.float32 if out == "f32" else torch.bfloat16
     d = torch.full((a.shape[0], w.shape[2]), float("nan"), dtype=dt, device=DEV)
     ms_dev = torch.tensor(ms, dtype=torch.int32, device=DEV)
     t = lambda x: torch.from_numpy(np.ascontiguousarray(x)).to(DEV)
-    dg.dg_m_grouped_fp8_dgrad(t(a), t(sfa), t(w), t(sfw), d, ms, ms_dev, gran_k)
+    if w_kmajor:
+        dg.dg_m_grouped_fp8_dgrad_nt(t(a), t(sfa), t(np.swapaxes(w, 1, 2)), t(sfw), d, ms, ms_dev,
+                                     gran_k)
+    else:
+        dg.dg_m_grouped_fp8_dgrad(t(a), t(sfa), t(w), t(sfw), d, ms, ms_dev, gran_k)
     dg.dg_sync_check()
     return d
 
 
+@pytest.mark.parametrize("w_kmajor", [False, True])
 @pytest.mark.parametrize("gran_k", [128, 32])
 @pytest.mark.parametrize("out", ["f32", "bf16"])
-def test_dgrad_modes(gran_k, out):
+def test_dgrad_modes(gran_k, out, w_kmajor):
     ms, K, N = [256, 0, 384, 128], 512, 448
     a, sfa, w, sfw = _case(ms, K, N, 31, gran_k)
-    d = run_dgrad(a, sfa, w, sfw, ms, gran_k, out)
+    d = run_dgrad(a, sfa, w, sfw, ms, gran_k, out, w_kmajor)
     D, S = oracle.mgrouped_fp8_dgrad(a, sfa, w, sfw, ms, gran_k)
-    assert_close(d, D, S, out, what=f"dgrad {out}/g{gran_k}")
+    assert_close(d, D, S, out, what=f"dgrad {out}/g{gran_k}/kmajor={w_kmajor}")
 
 
+@pytest.mark.parametrize("w_kmajor", [False, True])
 @pytest.mark.parametrize("K,N", [(128, 240), (384, 16), (640, 224 * 3 + 16), (1280, 96)])
-def test_dgrad_ragged_shapes(K, N):
+def test_dgrad_ragged_shapes(K, N, w_kmajor):
     ms = [128, 384, 0, 256, 128]
     a, sfa, w, sfw = _case(ms, K, N, K + N)
-    d = run_dgrad(a, sfa, w, sfw, ms, 128, "f32")
+    d = run_dgrad(a, sfa, w, sfw, ms, 128, "f32", w_kmajor)
     D, S = oracle.mgrouped_fp8_dgrad(a, sfa, w, sfw, ms, 128)
-    assert_close(d, D, S, "f32", what=f"dgrad K={K} N={N}")
+    assert_close(d, D, S, "f32", what=f"dgrad K={K} N={N} kmajor={w_kmajor}")
 
 
+@pytest.mark.parametrize("w_kmajor", [False, True])
 @pytest.mark.parametrize("gran_k", [128, 32])
-def test_dgrad_many_tiles_and_long_k_loops(gran_k):
+def test_dgrad_many_tiles_and_long_k_loops(gran_k, w_kmajor):
     """More tiles than CTA pairs (both lanes busy), 16-stage k loops, one
     expert of a single 128-row half."""
     ms, K, N = [128 * 21, 128 * 7, 0, 128 * 3, 128], 2048, 896
     a, sfa, w, sfw = _case(ms, K, N, 41, gran_k)
-    d = run_dgrad(a, sfa, w, sfw, ms, gran_k, "bf16")
+    d = run_dgrad(a, sfa, w, sfw, ms, gran_k, "bf16", w_kmajor)
     D, S = oracle.mgrouped_fp8_dgrad(a, sfa, w, sfw, ms, gran_k)
-    assert_close(d, D, S, "bf16", what=f"dgrad lanes g{gran_k}")
+    assert_close(d, D, S, "bf16", what=f"dgrad lanes g{gran_k} kmajor={w_kmajor}")
 
 
-def test_dgrad_integer_valued_is_bit_exact():
+@pytest.mark.parametrize("w_kmajor", [False, True])
+def test_dgrad_integer_valued_is_bit_exact(w_kmajor):
     """E4M3 integers in [-8, 8] with unit scales: every partial sum is an
     integer below 2^24, so the FP32 result is exact."""
     rng = np.random.default_rng(2)
@@ -78,7 +89,7 @@ def test_dgrad_integer_valued_is_bit_exact():
     w = oracle.e4m3_encode(rng.integers(-8, 9, size=(len(ms), K, N)).astype(np.float64))
     sfa = np.full((sm, K // 128), 127, np.uint8)
     sfw = np.full((len(ms), K // 128, N), 127, np.uint8)
-    d = run_dgrad(a, sfa, w, sfw, ms, 128, "f32").cpu().numpy()
+    d = run_dgrad(a, sfa, w, sfw, ms, 128, "f32", w_kmajor).cpu().numpy()
     D, _ = oracle.mgrouped_fp8_dgrad(a, sfa, w, sfw, ms, 128)
     assert np.array_equal(d.astype(np.float64), D)
 
