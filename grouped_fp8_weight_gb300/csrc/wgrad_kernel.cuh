@@ -42,6 +42,16 @@
 //
 // Operands are MN-major (the token axis is K and is the slow axis in memory):
 // an operand tile for one stage is BK token rows x 128-byte swizzle atoms.
+// With kKMajor both are K-major (rows of BK bytes of K).
+//
+// M-grouped mode (kMG, the FP8 data gradient dx_e = dy_e W_e): the schedule
+// entries are the experts with tokens, a tile is (256-token chunk, BN columns)
+// of one expert, A is K-major (dy's token rows, [sum_m, K]) and B the expert's
+// weight, MN-major [K, N] or, with kKMajor, K-major [N, K]; every tile runs
+// the same K, so both lanes take tiles in order and k loops are not rotated.
+//
+// Every role reads the schedule table once per chunk; it is copied into
+// shared memory at kernel start when it fits.
 //
 // Building with -DDG_KERNEL_TIMERS adds per-role cycle counters written to
 // WgradParams::timers (profiling builds only).
