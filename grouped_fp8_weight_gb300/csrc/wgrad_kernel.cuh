@@ -942,6 +942,8 @@ template <bool kFP8, int kBN, int kOut, bool kKMajor, bool kTransD, bool kMG = f
 cudaError_t launch_wgrad_variant(const WgradParams &p, int pairs, cudaStream_t stream) {
   using Cfg = WgradCfg<kFP8, kBN, kKMajor, kMG, kTransD>;
   auto kern = kgrouped_wgrad_kernel<kFP8, kBN, kOut, kKMajor, kTransD, kMG>;
+  // the schedule length and the division constants come from set_derived()
+  if (p.num_tiles > 0 && (p.n_sched <= 0 || p.n_sched > kMaxGroups)) return cudaErrorInvalidValue;
   static bool attr_set = false;
   static int max_pairs = 0;
   cudaLaunchAttribute attr[1];
