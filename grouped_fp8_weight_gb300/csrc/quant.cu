@@ -589,17 +589,17 @@ __global__ void __launch_bounds__(256, 3) gather_cast_kernel(const __grid_consta
 
 template <int kGran>
 cudaError_t launch_gather_tma(const CastArgs &a, cudaStream_t stream) {
-  static bool attr_set = false;
-  if (!attr_set) {
+  // attributes set once per process (thread-safe static initialisation)
+  static const cudaError_t setup = [] {
     cudaError_t e = cudaFuncSetAttribute(gather_cast_kernel<kGran>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kGtSmem);
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(gather_cast_kernel<kGran>,
                                cudaFuncAttributePreferredSharedMemoryCarveout,
                                cudaSharedmemCarveoutMaxShared);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+    return e;
+  }();
+  if (setup != cudaSuccess) return setup;
   const dim3 grid(static_cast<unsigned>((a.T + kTileT - 1) / kTileT),
                   static_cast<unsigned>((a.C + kTileC - 1) / kTileC));
   gather_cast_kernel<kGran><<<grid, 256, kGtSmem, stream>>>(a);
@@ -628,16 +628,15 @@ template <bool kGather>
 cudaError_t launch_requant_tm(const CastArgs &a, int gran_k, cudaStream_t stream) {
   const dim3 grid(static_cast<unsigned>((a.T + kTileT - 1) / kTileT),
                   static_cast<unsigned>((a.C + kRqTileC - 1) / kRqTileC));
-  static bool attr_set = false;
-  if (!attr_set) {
+  static const cudaError_t setup = [] {
     cudaError_t e = cudaFuncSetAttribute(requant_tm_kernel<128, kGather>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kRqSmem);
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(requant_tm_kernel<32, kGather>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, kRqSmem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+    return e;
+  }();
+  if (setup != cudaSuccess) return setup;
   if (gran_k == 128)
     requant_tm_kernel<128, kGather><<<grid, 256, kRqSmem, stream>>>(a);
   else

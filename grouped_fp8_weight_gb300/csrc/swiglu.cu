@@ -227,13 +227,10 @@ __global__ void __launch_bounds__(256, 2) swiglu_bwd_cast_kernel(const SwigluArg
 
 template <int kGran, bool kWithA>
 cudaError_t launch_sg(const SwigluArgs &p, cudaStream_t stream) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(swiglu_bwd_cast_kernel<kGran, kWithA>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSgSmem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  // attribute set once per process (thread-safe static initialisation)
+  static const cudaError_t setup = cudaFuncSetAttribute(
+      swiglu_bwd_cast_kernel<kGran, kWithA>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSgSmem);
+  if (setup != cudaSuccess) return setup;
   const dim3 grid(static_cast<unsigned>((p.T + kSgT - 1) / kSgT),
                   static_cast<unsigned>((p.I + kSgC - 1) / kSgC));
   swiglu_bwd_cast_kernel<kGran, kWithA><<<grid, 256, kSgSmem, stream>>>(p);

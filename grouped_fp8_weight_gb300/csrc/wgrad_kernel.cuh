@@ -944,8 +944,6 @@ cudaError_t launch_wgrad_variant(const WgradParams &p, int pairs, cudaStream_t s
   auto kern = kgrouped_wgrad_kernel<kFP8, kBN, kOut, kKMajor, kTransD, kMG>;
   // the schedule length and the division constants come from set_derived()
   if (p.num_tiles > 0 && (p.n_sched <= 0 || p.n_sched > kMaxGroups)) return cudaErrorInvalidValue;
-  static bool attr_set = false;
-  static int max_pairs = 0;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
@@ -957,18 +955,23 @@ cudaError_t launch_wgrad_variant(const WgradParams &p, int pairs, cudaStream_t s
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (!attr_set) {
-    cudaError_t err =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
-    if (err != cudaSuccess) return err;
-    cfg.gridDim = dim3(2 * pairs, 1, 1);
-    int n = 0;
-    err = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
-    if (err != cudaSuccess) return err;
-    max_pairs = n;
-    attr_set = true;
-  }
-  if (max_pairs > 0) pairs = min(pairs, max_pairs);
+  // Shared-memory attribute and the number of co-resident pairs, once per
+  // process (thread-safe static initialisation).
+  struct Setup {
+    cudaError_t err;
+    int max_pairs;
+  };
+  static const Setup setup = [&] {
+    Setup st{cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  Cfg::SMEM_BYTES), 0};
+    if (st.err != cudaSuccess) return st;
+    cudaLaunchConfig_t c = cfg;
+    c.gridDim = dim3(2 * (pairs > 0 ? pairs : 1), 1, 1);
+    st.err = cudaOccupancyMaxActiveClusters(&st.max_pairs, kern, &c);
+    return st;
+  }();
+  if (setup.err != cudaSuccess) return setup.err;
+  if (setup.max_pairs > 0) pairs = min(pairs, setup.max_pairs);
   cfg.gridDim = dim3(2 * pairs, 1, 1);
   return cudaLaunchKernelEx(&cfg, kern, p);
 }
