@@ -368,7 +368,6 @@ def profile_inplace(w, args, dev, pk, rank):
         sb = torch.empty(w.sum_k // 128, w.N, dtype=torch.uint8, device=dev)
         dg.dg_quant_transpose_fp8(A, qa, sa)
         dg.dg_quant_transpose_fp8(B, qb, sb)
-        del A, B
         ops = w.sum_k * (w.M + w.N) + (w.sum_k // 128) * (w.M + w.N)
 
         def step():
@@ -382,12 +381,30 @@ def profile_inplace(w, args, dev, pk, rank):
     dg.dg_sync_check()
     alg = ops + ne * w.M * w.N * 4 * 2          # D read and written for non-empty experts
     tf = w.flops / (ms * 1e-3) / 1e12
+    out = {"profile_only": True, "workload": w.name, "ms_per_step": ms,
+           "tflops": tf, "tensor_frac": tf / peak_t, "kernel": kname,
+           "algorithmic_bytes": alg, "hbm_gbs": alg / (ms * 1e-3) / 1e9,
+           "hbm_frac": alg / (ms * 1e-3) / 1e9 / pk["hbm_gbs"],
+           "nonempty_experts": ne}
+    if w.kind == "pipeline":
+        # the pipeline's other steps: the cast of dY and X, and cast + GEMM
+        def cast_pair():
+            dg.dg_quant_transpose_fp8(A, qa, sa)
+            dg.dg_quant_transpose_fp8(B, qb, sb)
+
+        for _ in range(3):
+            cast_pair()
+        n = max(3, args.steps)
+        ms_cast = time_events(cast_pair, n, torch.cuda.current_stream())
+        ms_pipe = time_events(lambda: (cast_pair(), step()), n, torch.cuda.current_stream())
+        dg.dg_sync_check()
+        cast_bytes = w.sum_k * (w.M + w.N) * 3 + (w.sum_k // 128) * (w.M + w.N)
+        out["cast"] = {"ms": ms_cast, "bound": "hbm", "algorithmic_bytes": cast_bytes,
+                       "achieved": cast_bytes / (ms_cast * 1e-3) / 1e9, "unit": "GB/s",
+                       "frac": cast_bytes / (ms_cast * 1e-3) / 1e9 / pk["hbm_gbs"]}
+        out["cast_plus_gemm"] = {"ms": ms_pipe, "tflops": w.flops / (ms_pipe * 1e-3) / 1e12}
     if rank == 0:
-        print(json.dumps({"profile_only": True, "workload": w.name, "ms_per_step": ms,
-                          "tflops": tf, "tensor_frac": tf / peak_t, "kernel": kname,
-                          "algorithmic_bytes": alg, "hbm_gbs": alg / (ms * 1e-3) / 1e9,
-                          "hbm_frac": alg / (ms * 1e-3) / 1e9 / pk["hbm_gbs"],
-                          "nonempty_experts": ne}), flush=True)
+        print(json.dumps(out), flush=True)
     return 0
 
 
