@@ -205,7 +205,7 @@ cudaError_t launch_moe_layout_plan(const MoePlanArgs &a, int sms, cudaStream_t s
 constexpr int kPairM = 256;
 // Stages of a long tile issued per turn before the MMA stream switches to the
 // other accumulator's tile (FP8 stages are 128 tokens, BF16 64).
-constexpr int kFp8Chunk = 40;
+constexpr int kFp8Chunk = 16;
 static_assert(kFp8Chunk % 4 == 0, "lane chunks must start on a scale group (four k-blocks)");
 // Epilogue chunk: output columns per staged TMA store box (32 rows high).
 constexpr int kEpiCols = 32;
