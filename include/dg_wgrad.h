@@ -2,7 +2,8 @@
  * dg_wgrad.h -- C ABI of the GB300 (sm_103a) K-grouped weight-gradient library.
  *
  * Mixture-of-Experts weight gradient, one GEMM per expert, all experts in one
- * launch:  D[e] (+)= A_e^T B_e.  The operands are concatenated along tokens:
+ * launch:  D[e] (+)= A_e^T B_e  (with the casts that produce its FP8 operands,
+ * and the M-grouped data gradient dx_e = dy_e W_e that pairs with it).  The operands are concatenated along tokens:
  * A is [sum_k, M] (upstream gradients dy, M = h_out), B is [sum_k, N] (input
  * activations x, N = h_in), and expert e owns the contiguous rows
  * [off_e, off_e + K_e), off_e = K_0 + ... + K_{e-1}.  The GEMM's reduction
@@ -15,10 +16,10 @@
  *
  * Conventions shared by every entry point
  * ---------------------------------------
- *  - Every pointer argument named a, b, sfa, sfb, d, c, x, x_sf, q_in, sf_in,
- *    src_rows, pair_rows, topk_idx, ks, h, da, q_dh, sf_dh, q_a, sf_a, q, sf,
- *    ks_dev is a
- *    DEVICE pointer on the current CUDA device; ks_host is a HOST pointer.
+ *  - Every pointer argument named a, b, w, sfa, sfb, sfw, d, c, x, x_sf, q_in,
+ *    sf_in, src_rows, pair_rows, topk_idx, ks, h, da, q_dh, sf_dh, q_a, sf_a,
+ *    q, sf, ks_dev, ms_dev is a DEVICE pointer on the current CUDA device;
+ *    ks_host and ms_host are HOST pointers.
  *  - All matrices are dense row-major with the last index contiguous (no
  *    padding between rows).  Device pointers must be 16-byte aligned.
  *  - The caller owns every buffer.  The first call on a device allocates one
@@ -27,11 +28,12 @@
  *    memory pool the library creates per device: allocated and freed in
  *    stream order on `stream` (cudaMallocFromPoolAsync / cudaFreeAsync), so
  *    calls on different streams never share it; the pool keeps freed blocks
- *    for reuse.  dg_moe_layout_plan takes its counters from the same pool.
+ *    for reuse.  The data-gradient calls and dg_moe_layout_plan take their
+ *    scratch from the same pool.
  *    The BF16 GEMM and the casts allocate nothing per call.
  *  - Work is enqueued on `stream` (NULL = legacy default stream) and runs
- *    asynchronously.  ks_host is read during the call only; device buffers
- *    must stay valid until the enqueued work completes.
+ *    asynchronously.  ks_host / ms_host are read during the call only;
+ *    device buffers must stay valid until the enqueued work completes.
  *  - Argument errors are returned before anything is enqueued; the output is
  *    then untouched.  dg_last_error() gives a message for the calling thread.
  *  - DG_LOG=1 in the environment makes each GEMM call print its plan (tile
