@@ -17,14 +17,18 @@ The same JSON line also carries:
   casts         the re-quantisation of stored FP8 operands, the cast fused
                 with the MoE layout and the cast fused with the SwiGLU
                 backward, each against the HBM roofline;
+  dgrad         the M-grouped FP8 data gradient of the up/gate projection
+                (dg_m_grouped_fp8_dgrad, and _nt with K-major weights)
+                against the FP8 peak;
+  tiny          host and device time per call of the tiny in-place workload;
   e2e           the same metric through the C ABI with pinned host buffers:
                 H2D of the step's operands and D2H of the result D in the
                 timed region;
   cpu_baseline  the float64 CPU oracle timed on a bounded sample;
   clocks        nvidia-smi samples taken during warm-up + timed region.
 
-``--impl reference`` times the oracle (the reference arm of this build) on a
-bounded sample of the same workload.  Under torchrun each rank runs its own
+``--impl reference`` times the float64 oracle (the reference arm: the pages
+hold no runnable code) on a bounded sample of the same workload.  Under torchrun each rank runs its own
 replica of the workload (weak scaling, no data-path collective); rank 0
 prints the line.
 """
