@@ -127,16 +127,23 @@ def test_dgrad_ms_dev_mismatch_is_reported():
     dg.dg_sync_check()                      # the status word was cleared
 
 
-def test_dgrad_full_size_upgate_sampled():
+@pytest.mark.parametrize("w_kmajor", [False, True])
+def test_dgrad_full_size_upgate_sampled(w_kmajor):
     """The bench's data-gradient workload (G = 32, K = 4096, N = 7168, 32768
-    tokens, BF16 out) in the bench's launch configuration; eight experts (the
-    largest, the smallest non-empty, six seeded others) checked on 24 seeded
-    rows each plus the smallest non-empty expert's rows in full."""
+    tokens, BF16 out) in the bench's launch configuration, weights [G, K, N]
+    or K-major [G, N, K]; eight experts (the largest, the smallest non-empty,
+    six seeded others) checked on 24 seeded rows each plus the smallest
+    non-empty expert's rows in full."""
     name = "moe_upgate_dgrad_fp8_g32"
     ms, a, sfa, w, sfw = workloads.draw_dgrad_operands(name)
     d = torch.empty(a.shape[0], w.shape[2], dtype=torch.bfloat16, device=DEV)
     ms_dev = torch.tensor(ms, dtype=torch.int32, device=DEV)
-    dg.dg_m_grouped_fp8_dgrad(a.to(DEV), sfa.to(DEV), w.to(DEV), sfw.to(DEV), d, ms, ms_dev, 128)
+    if w_kmajor:
+        dg.dg_m_grouped_fp8_dgrad_nt(a.to(DEV), sfa.to(DEV), w.to(DEV).transpose(1, 2).contiguous(),
+                                     sfw.to(DEV), d, ms, ms_dev, 128)
+    else:
+        dg.dg_m_grouped_fp8_dgrad(a.to(DEV), sfa.to(DEV), w.to(DEV), sfw.to(DEV), d, ms, ms_dev,
+                                  128)
     dg.dg_sync_check()
     a, sfa, w, sfw = a.numpy(), sfa.numpy(), w.numpy(), sfw.numpy()
     off = oracle.expert_offsets(ms)
