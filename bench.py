@@ -9,9 +9,16 @@ is 2*M*N*sum(K) / step time in TFLOP/s.
 The same JSON line also carries:
   roofline      the GEMM kernel's algorithmic bytes / CUDA-event launch time
                 against the measured HBM copy bandwidth, plus its tensor
-                fraction against the FP8 peak (2 x measured BF16);
+                fraction against the dense FP8 peak, measured in the same run
+                (cuBLASLt e4m3 8192^3 through torch._scaled_mm, best of 10);
+  configs       every workload of the path, each device-resident and timed
+                on its own: the tiny in-place case (see `tiny`), the up/gate
+                headline, the down-projection (BF16 output, 1 % outliers),
+                the fine-grained BF16 case (D += in place) and the pipeline
+                (the cast of dY [131072, 4096] and X [131072, 7168], the
+                in-place GEMM onto C, and cast + GEMM), each with its roofline;
   pipeline      the cast-inclusive step (BF16 dY, X -> dg_quant_transpose_fp8
-                x2 -> GEMM) on the same shapes, and the cast's own roofline;
+                x2 -> GEMM) on the headline's shapes, and the cast's roofline;
   nt            the same GEMM with K-major operands (dg_k_grouped_fp8_wgrad_nt)
                 fed by the channel-major cast;
   casts         the re-quantisation of stored FP8 operands, the cast fused
@@ -139,6 +146,55 @@ class ClockSampler:
                           if v.lower() == "active"})
         return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": rows[0][1],
                 "reasons": reasons, "samples": len(rows)}
+
+
+def measure_fp8_peak(dev, sustained_s: float = 0.0):
+    """Dense FP8 (E4M3 x E4M3 -> BF16, FP32 accumulation) throughput of
+    cuBLASLt through torch._scaled_mm on 8192^3 with per-tensor scales: the
+    best of 10 timed calls (burst) and, if sustained_s > 0, the mean rate of
+    back-to-back calls over that many seconds (sustained).  This is the
+    library's dense FP8 rate on this GPU, the denominator of every FP8
+    tensor fraction."""
+    n = 8192
+    gen = torch.Generator(device=dev).manual_seed(7)
+    a = torch.randn(n, n, generator=gen, device=dev).to(torch.float8_e4m3fn)
+    b = torch.randn(n, n, generator=gen, device=dev).to(torch.float8_e4m3fn).t()
+    one = torch.ones((), dtype=torch.float32, device=dev)
+
+    def mm():
+        return torch._scaled_mm(a, b, one, one, out_dtype=torch.bfloat16)
+
+    for _ in range(5):
+        mm()
+    torch.cuda.synchronize()
+    best = float("inf")
+    for _ in range(10):
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        mm()
+        e.record()
+        e.synchronize()
+        best = min(best, s.elapsed_time(e))
+    flops = 2.0 * n ** 3
+    out = {"burst_tflops": flops / (best * 1e-3) / 1e12, "shape": [n, n, n],
+           "how": "torch._scaled_mm e4m3 x e4m3 -> bf16, per-tensor scales, best of 10"}
+    if sustained_s > 0:
+        calls, t_ms = 0, 0.0
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0 = time.perf_counter()
+        s.record()
+        while time.perf_counter() - t0 < sustained_s:
+            for _ in range(20):
+                mm()
+            calls += 20
+            torch.cuda.synchronize()
+        e.record()
+        e.synchronize()
+        t_ms = s.elapsed_time(e)
+        out["sustained_tflops"] = calls * flops / (t_ms * 1e-3) / 1e12
+        out["sustained_seconds"] = t_ms / 1e3
+    del a, b
+    return out
 
 
 def make_inputs(w, dev):
@@ -301,7 +357,7 @@ def measure_tiny(dev, stream, steps):
             "note": "back-to-back calls; the device time includes the scale-pack launch"}
 
 
-def measure_dgrad(dev, stream, pk, steps):
+def measure_dgrad(dev, stream, pk, steps, fp8p):
     """The M-grouped FP8 data gradient of the up/gate projection (dx = dh W_e,
     K = 4096, N = 7168, the headline's token counts law), device-resident,
     CUDA events; one dg_m_grouped_fp8_dgrad call = two scale-packing passes +
@@ -335,36 +391,38 @@ def measure_dgrad(dev, stream, pk, steps):
     K, N, T = w.M, w.N, w.sum_k
     nbytes = T * K + T * (K // 128) + live * K * N + live * (K // 128) * N + T * N * 2
     flops = 2.0 * T * K * N
-    fp8_peak = 2.0 * pk["bf16_tflops"]
+    fp8_peak = fp8p["tflops"]
     tflops = flops / (ms * 1e-3) / 1e12
     del a, sfa, wt, sfw, d
     return {"ms": ms, "value": tflops, "unit": "TFLOP/s", "workload": name,
             "kernel": "kgrouped_wgrad_kernel<fp8, 224, bf16, M-grouped>",
             "shape": {"G": w.G, "K": K, "N": N, "sum_m": T, "experts_with_tokens": live},
             "launches_per_step": 3, "bound": "tensor", "achieved": tflops, "peak": fp8_peak,
-            "frac": tflops / fp8_peak, "algorithmic_bytes": nbytes,
+            "frac": tflops / fp8_peak, "peak_source": fp8p["source"], "algorithmic_bytes": nbytes,
             "hbm_frac": nbytes / (ms * 1e-3) / 1e9 / pk["hbm_gbs"],
             "kmajor_weights": {"ms": ms_nt, "value": flops / (ms_nt * 1e-3) / 1e12,
                                "frac": flops / (ms_nt * 1e-3) / 1e12 / fp8_peak,
                                "entry": "dg_m_grouped_fp8_dgrad_nt (W [G, N, K])"}}
 
 
-def profile_inplace(w, args, dev, pk, rank):
-    """Device-timed leg of the in-place workloads: the BF16 fine-grained GEMM
-    (BF16 operands, D += A^T B) or the pipeline's FP8 GEMM (operands cast from
-    BF16 draws by the library's cast, D += A^T B), inputs drawn on the device."""
+def measure_inplace(w, dev, pk, fp8_peak, steps, warmup=5):
+    """The in-place workloads, device-resident, CUDA events: the fine-grained
+    BF16 GEMM (BF16 operands, D += A^T B) or the pipeline (BF16 dY and X cast
+    by dg_quant_transpose_fp8, then the FP8 GEMM D += A^T B); for the pipeline
+    also the cast pair alone and cast + GEMM."""
     import grouped_fp8_weight_gb300 as dg
     ks, A, B, C = workloads.draw_operands(w.name, device=str(dev))
     ks_dev = torch.tensor(ks, dtype=torch.int32, device=dev)
     d = C
     ne = sum(1 for k in ks if k > 0)
+    stream = torch.cuda.current_stream()
     if w.kind == "bf16":
         ops = w.sum_k * (w.M + w.N) * 2
 
         def step():
             dg.dg_k_grouped_bf16_wgrad(A, B, d, d, ks, ks_dev)
         kname = "kgrouped_wgrad_kernel<bf16, 256, f32 reduce>"
-        peak_t = pk["bf16_tflops"]
+        peak_t, peak_name = pk["bf16_tflops"], "bf16 (measured cuBLAS burst)"
     else:
         qa = torch.empty(w.sum_k, w.M, dtype=torch.uint8, device=dev)
         sa = torch.empty(w.sum_k // 128, w.M, dtype=torch.uint8, device=dev)
@@ -377,19 +435,22 @@ def profile_inplace(w, args, dev, pk, rank):
         def step():
             dg.dg_k_grouped_fp8_wgrad(qa, sa, qb, sb, d, d, ks, ks_dev, 128)
         kname = "kgrouped_wgrad_kernel<fp8, 224, f32 reduce>"
-        peak_t = 2.0 * pk["bf16_tflops"]
-    for _ in range(args.warmup):
+        peak_t, peak_name = fp8_peak["tflops"], fp8_peak["source"]
+    for _ in range(warmup):
         step()
     torch.cuda.synchronize()
-    ms = time_events(step, args.steps, torch.cuda.current_stream())
+    ms = time_events(step, steps, stream)
     dg.dg_sync_check()
     alg = ops + ne * w.M * w.N * 4 * 2          # D read and written for non-empty experts
     tf = w.flops / (ms * 1e-3) / 1e12
-    out = {"profile_only": True, "workload": w.name, "ms_per_step": ms,
-           "tflops": tf, "tensor_frac": tf / peak_t, "kernel": kname,
-           "algorithmic_bytes": alg, "hbm_gbs": alg / (ms * 1e-3) / 1e9,
-           "hbm_frac": alg / (ms * 1e-3) / 1e9 / pk["hbm_gbs"],
-           "nonempty_experts": ne}
+    gbs = alg / (ms * 1e-3) / 1e9
+    out = {"workload": w.name, "ms": ms, "value": tf, "unit": "TFLOP/s", "kernel": kname,
+           "launches_per_step": 1 if w.kind == "bf16" else 2,
+           "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                        "frac": gbs / pk["hbm_gbs"], "algorithmic_bytes": alg},
+           "tensor_frac": tf / peak_t, "tensor_peak": peak_name,
+           "nonempty_experts": ne, "steps": steps,
+           "shape": {"G": w.G, "M": w.M, "N": w.N, "sum_k": w.sum_k, "max_k": max(ks)}}
     if w.kind == "pipeline":
         # the pipeline's other steps: the cast of dY and X, and cast + GEMM
         def cast_pair():
@@ -398,18 +459,69 @@ def profile_inplace(w, args, dev, pk, rank):
 
         for _ in range(3):
             cast_pair()
-        n = max(3, args.steps)
-        ms_cast = time_events(cast_pair, n, torch.cuda.current_stream())
-        ms_pipe = time_events(lambda: (cast_pair(), step()), n, torch.cuda.current_stream())
+        ms_cast = time_events(cast_pair, steps, stream)
+        ms_pipe = time_events(lambda: (cast_pair(), step()), steps, stream)
         dg.dg_sync_check()
         cast_bytes = w.sum_k * (w.M + w.N) * 3 + (w.sum_k // 128) * (w.M + w.N)
-        out["cast"] = {"ms": ms_cast, "bound": "hbm", "algorithmic_bytes": cast_bytes,
-                       "achieved": cast_bytes / (ms_cast * 1e-3) / 1e9, "unit": "GB/s",
-                       "frac": cast_bytes / (ms_cast * 1e-3) / 1e9 / pk["hbm_gbs"]}
-        out["cast_plus_gemm"] = {"ms": ms_pipe, "tflops": w.flops / (ms_pipe * 1e-3) / 1e12}
-    if rank == 0:
-        print(json.dumps(out), flush=True)
-    return 0
+        out["cast"] = {"ms": ms_cast, "kernel": "cast_colblock_kernel<128, token-major> x2",
+                       "roofline": {"bound": "hbm", "achieved": cast_bytes / (ms_cast * 1e-3) / 1e9,
+                                    "peak": pk["hbm_gbs"], "unit": "GB/s",
+                                    "frac": cast_bytes / (ms_cast * 1e-3) / 1e9 / pk["hbm_gbs"],
+                                    "algorithmic_bytes": cast_bytes},
+                       "shapes": {"dY": [w.sum_k, w.M], "X": [w.sum_k, w.N]}}
+        out["cast_plus_gemm"] = {"ms": ms_pipe, "value": w.flops / (ms_pipe * 1e-3) / 1e12,
+                                 "unit": "TFLOP/s", "launches_per_step": 4}
+        del qa, sa, qb, sb
+    del A, B, C, d
+    torch.cuda.empty_cache()
+    return out
+
+
+def measure_fp8_config(name, dev, pk, fp8_peak, steps):
+    """A device-resident FP8 weight-gradient workload other than the headline
+    (the down-projection: BF16 output, outliers): operands drawn on the device
+    and cast by the library's own cast, CUDA events over `steps` calls."""
+    import grouped_fp8_weight_gb300 as dg
+    w = workloads.WORKLOADS[name]
+    ks, a_raw, b_raw, qa, sa, qb, sb = make_inputs(w, dev)
+    del a_raw, b_raw
+    ks_dev = torch.tensor(ks, dtype=torch.int32, device=dev)
+    out_dt = torch.float32 if w.out_dtype == "f32" else torch.bfloat16
+    d = torch.empty(w.G, w.M, w.N, dtype=out_dt, device=dev)
+
+    def step():
+        dg.dg_k_grouped_fp8_wgrad(qa, sa, qb, sb, d, None, ks, ks_dev, 128)
+
+    for _ in range(5):
+        step()
+    torch.cuda.synchronize()
+    ms = time_events(step, steps, torch.cuda.current_stream())
+    dg.dg_sync_check()
+    tf = w.flops / (ms * 1e-3) / 1e12
+    alg = algorithmic_bytes(w, ks)
+    del qa, sa, qb, sb, d
+    torch.cuda.empty_cache()
+    return {"workload": name, "ms": ms, "value": tf, "unit": "TFLOP/s", "steps": steps,
+            "kernel": "kgrouped_wgrad_kernel<fp8, 224, bf16, transposed tiles>"
+                      if w.out_dtype == "bf16" else "kgrouped_wgrad_kernel<fp8, 224, f32>",
+            "launches_per_step": 2,
+            "roofline": {"bound": "tensor", "achieved": tf, "peak": fp8_peak["tflops"],
+                         "unit": "TFLOP/s", "frac": tf / fp8_peak["tflops"],
+                         "peak_source": fp8_peak["source"]},
+            "hbm_frac": alg / (ms * 1e-3) / 1e9 / pk["hbm_gbs"], "algorithmic_bytes": alg,
+            "shape": {"G": w.G, "M": w.M, "N": w.N, "sum_k": w.sum_k, "max_k": max(ks),
+                      "empty_experts": sum(1 for k in ks if k == 0), "out": w.out_dtype}}
+
+
+def fp8_peak_for(dev, pk):
+    """The dense FP8 denominator: cuBLASLt's e4m3 8192^3 rate measured now on
+    this GPU (best of 10), or 2 x the measured BF16 burst if that fails."""
+    try:
+        r = measure_fp8_peak(dev)
+        return {"tflops": r["burst_tflops"], "source": "measured: " + r["how"]}
+    except Exception as exc:  # noqa: BLE001 - reported, not hidden
+        return {"tflops": 2.0 * pk["bf16_tflops"],
+                "source": f"assumed 2 x measured BF16 burst (FP8 measurement failed: {exc})"}
 
 
 def cpu_oracle_sample(w, ks, qa, sa, qb, sb, n_rows=16):
@@ -518,11 +630,14 @@ def run_ours(args):
         tdist.init_process_group("nccl", device_id=dev)
     w = workloads.WORKLOADS[args.workload]
     pk, pk_kind = peaks()
-    if w.kind != "fp8":
+    if w.kind not in ("fp8",):
         if not args.profile:
-            raise SystemExit("the full bench line runs the FP8 workloads; the BF16 and "
-                             "pipeline workloads have the device-timed --profile leg only")
-        return profile_inplace(w, args, dev, pk, rank)
+            raise SystemExit("the full bench line runs with the headline FP8 workload and "
+                             "times the others inside it; --workload X --profile times X alone")
+        out = measure_inplace(w, dev, pk, fp8_peak_for(dev, pk), args.steps, args.warmup)
+        if rank == 0:
+            print(json.dumps({"profile_only": True, **out}), flush=True)
+        return 0
     if args.profile_tiny:
         out = measure_tiny(dev, torch.cuda.current_stream(), max(args.steps, 50))
         if rank == 0:
@@ -530,7 +645,8 @@ def run_ours(args):
         return 0
     if args.profile_dgrad:
         # the data-gradient leg alone, for kernel captures
-        out = measure_dgrad(dev, torch.cuda.current_stream(), pk, args.steps)
+        out = measure_dgrad(dev, torch.cuda.current_stream(), pk, args.steps,
+                            fp8_peak_for(dev, pk))
         if rank == 0:
             print(json.dumps({"profile_only": True, "dgrad": out}), flush=True)
         return 0
@@ -543,6 +659,7 @@ def run_ours(args):
             print(json.dumps({"profile_only": True, "config": workload_config(w, ks),
                               "casts": casts}), flush=True)
         return 0
+    fp8p = fp8_peak_for(dev, pk)
     ks, a_raw, b_raw, qa, sa, qb, sb = make_inputs(w, dev)
     ks_dev = torch.tensor(ks, dtype=torch.int32, device=dev)
     out_dt = torch.float32 if w.out_dtype == "f32" else torch.bfloat16
@@ -575,7 +692,7 @@ def run_ours(args):
     # ---- roofline of the GEMM kernel (the only kernel of the step)
     alg = algorithmic_bytes(w, ks)
     gbs = alg / (ms * 1e-3) / 1e9
-    fp8_peak = 2.0 * pk["bf16_tflops"]
+    fp8_peak = fp8p["tflops"]
     tflops = flops / (ms * 1e-3) / 1e12
     t_hbm = alg / (pk["hbm_gbs"] * 1e9)
     t_tc = flops / (fp8_peak * 1e12)
@@ -592,7 +709,7 @@ def run_ours(args):
                  "tensor_peak_tflops": fp8_peak, "tensor_frac": tflops / fp8_peak,
                  "attainable_frac": max(t_hbm, t_tc) / (ms * 1e-3),
                  "timed": "one dg_k_grouped_fp8_wgrad call: scale-packing pass + GEMM kernel",
-                 "note": "FP8 peak = 2 x measured BF16 burst (nominal fp8/bf16 ratio)"})
+                 "tensor_peak_source": fp8p["source"]})
 
     if args.profile:
         if rank == 0:
@@ -647,8 +764,20 @@ def run_ours(args):
 
     casts = measure_casts(w, ks, dev, stream, pk, max(5, args.steps // 4))
     dg.dg_sync_check()
-    dgrad = measure_dgrad(dev, stream, pk, max(5, args.steps // 4))
+    dgrad = measure_dgrad(dev, stream, pk, max(5, args.steps // 4), fp8p)
     tiny = measure_tiny(dev, stream, 200)
+    # ---- the other workloads, each device-resident and timed on its own
+    configs = {
+        "fp8_tiny_g4": {"see": "tiny"},
+        "moe_upgate_fp8_g32": {"see": "value / roofline", "ms": ms, "value": tflops,
+                               "tensor_frac": tflops / fp8_peak},
+        "moe_down_fp8_g32": measure_fp8_config("moe_down_fp8_g32", dev, pk, fp8p,
+                                               max(20, args.steps // 4)),
+        "bf16_fine_g256": measure_inplace(workloads.WORKLOADS["bf16_fine_g256"], dev, pk, fp8p,
+                                          max(20, args.steps // 4)),
+        "pipeline_fp8_g64": measure_inplace(workloads.WORKLOADS["pipeline_fp8_g64"], dev, pk,
+                                            fp8p, max(10, args.steps // 20)),
+    }
 
     # ---- end to end through the C ABI with pinned host buffers
     h_qa, h_sa = qa.cpu().pin_memory(), sa.cpu().pin_memory()
@@ -683,8 +812,8 @@ def run_ours(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "e4m3 x e4m3 -> f32", "data": "synthetic",
             "config": workload_config(w, ks), "fp8_peak_frac": tflops / fp8_peak,
-            "roofline": roof, "pipeline": pipeline, "nt": nt, "casts": casts, "dgrad": dgrad,
-            "tiny": tiny,
+            "roofline": roof, "configs": configs, "pipeline": pipeline, "nt": nt,
+            "casts": casts, "dgrad": dgrad, "tiny": tiny,
             "e2e": e2e,
             "cpu_baseline": cpu,
             "clocks": clk.summary(),
@@ -714,9 +843,18 @@ def main():
                     help="time the M-grouped data-gradient leg alone (for kernel captures)")
     ap.add_argument("--profile-casts", action="store_true",
                     help="the cast legs only, `--steps` launches each (for ncu captures)")
+    ap.add_argument("--fp8-peak", action="store_true",
+                    help="measure the dense FP8 peak (burst and 4-s sustained) and exit")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.fp8_peak:
+        dev = torch.device("cuda", 0)
+        with ClockSampler(0) as clk:
+            r = measure_fp8_peak(dev, sustained_s=4.0)
+        r["clocks"] = clk.summary()
+        print(json.dumps(r), flush=True)
+        return 0
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

@@ -17,6 +17,7 @@
 #include <cuda_runtime.h>
 
 #include "dg_wgrad.h"
+#include "grouped_plan.h"
 #include "wgrad_params.h"
 
 static_assert(DG_MAX_GROUPS == dg::kMaxGroups, "group limit mismatch");
@@ -59,13 +60,14 @@ struct DeviceState {
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
-PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 dg_status device_state(DeviceState **out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return fail(DG_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
   if (dev < 0 || dev >= kMaxDevices) return fail(DG_ERR_UNSUPPORTED, "device index %d", dev);
+  if (dg::tensor_map_encoder() == nullptr)
+    return fail(DG_ERR_CUDA, "cuTensorMapEncodeTiled not available");
   std::lock_guard<std::mutex> lock(g_mu);
   DeviceState &st = g_dev[dev];
   if (!st.init) {
@@ -92,15 +94,6 @@ dg_status device_state(DeviceState **out) {
               cudaSuccess)
         return fail(DG_ERR_CUDA, "memory pool: %s", cudaGetErrorString(e));
     }
-    if (g_encode == nullptr) {
-      void *fn = nullptr;
-      cudaDriverEntryPointQueryResult q{};
-      e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
-                                           cudaEnableDefault, &q);
-      if (e != cudaSuccess || fn == nullptr || q != cudaDriverEntryPointSuccess)
-        return fail(DG_ERR_CUDA, "cuTensorMapEncodeTiled not available");
-      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-    }
     st.init = true;
   }
   if (!st.arch_ok)
@@ -108,17 +101,6 @@ dg_status device_state(DeviceState **out) {
                 st.major, st.minor);
   *out = &st;
   return DG_OK;
-}
-
-uint64_t wait_limit_ns() {
-  const char *s = std::getenv("DG_WAIT_LIMIT_MS");
-  long ms = 4000;
-  if (s != nullptr && *s) {
-    char *end = nullptr;
-    long v = std::strtol(s, &end, 10);
-    if (end != s && v > 0) ms = v;
-  }
-  return static_cast<uint64_t>(ms) * 1000000ull;
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -144,42 +126,82 @@ dg_status encode(CUtensorMap *m, CUtensorMapDataType dt, const void *ptr, int ra
     es[i] = 1;
   }
   for (int i = 0; i + 1 < rank; ++i) gs[i] = strides_bytes[i];
-  CUresult r = g_encode(m, dt, static_cast<cuuint32_t>(rank), const_cast<void *>(ptr), gd, gs,
-                        bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, l2,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  PFN_cuTensorMapEncodeTiled_v12000 enc = dg::tensor_map_encoder();
+  if (enc == nullptr) return fail(DG_ERR_CUDA, "cuTensorMapEncodeTiled not available");
+  CUresult r = enc(m, dt, static_cast<cuuint32_t>(rank), const_cast<void *>(ptr), gd, gs, bx, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, sw, l2, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(DG_ERR_CUDA, "tensor map for %s failed (%d)", what, (int)r);
   return DG_OK;
 }
 
-struct GroupedArgs {
-  bool fp8;
-  bool kmajor;   // FP8 only: a [M, sum_k], b [N, sum_k] (NT) instead of [sum_k, M], [sum_k, N]
-  const void *a, *b;
-  const uint8_t *sfa, *sfb;
-  void *d;
-  dg_dtype d_dtype;
-  const float *c;
-  int G, M, N;
-  int64_t sum_k;
-  const int *ks_host, *ks_dev;
-  int gran_k;
-  cudaStream_t stream;
-};
+}  // namespace
 
-dg_status run_grouped(const GroupedArgs &x) {
-  const char *fn = !x.fp8 ? "dg_k_grouped_bf16_wgrad"
-                   : x.kmajor ? "dg_k_grouped_fp8_wgrad_nt" : "dg_k_grouped_fp8_wgrad";
-  // ---- validation (nothing is enqueued on failure)
+namespace dg {
+
+cudaError_t noalloc_take_status(DevStatus *out, bool *present);   // noalloc.cu
+
+dg_status failf(dg_status s, const char *fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return s;
+}
+
+// Lets the allocation-free entry point (noalloc.cu) report through dg_last_error.
+void set_last_error(const char *msg) { g_err = (msg != nullptr) ? msg : ""; }
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static const PFN_cuTensorMapEncodeTiled_v12000 enc = [] {
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    const cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                           cudaEnableDefault, &q);
+    return (e == cudaSuccess && q == cudaDriverEntryPointSuccess)
+               ? reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn)
+               : nullptr;
+  }();
+  return enc;
+}
+
+uint64_t wait_limit_ns() {
+  // DG_WAIT_LIMIT_US (microseconds) takes precedence over DG_WAIT_LIMIT_MS.
+  const char *us = std::getenv("DG_WAIT_LIMIT_US");
+  if (us != nullptr && *us) {
+    char *end = nullptr;
+    const long long v = std::strtoll(us, &end, 10);
+    if (end != us && v > 0) return static_cast<uint64_t>(v) * 1000ull;
+  }
+  const char *s = std::getenv("DG_WAIT_LIMIT_MS");
+  long long ms = 4000;
+  if (s != nullptr && *s) {
+    char *end = nullptr;
+    const long long v = std::strtoll(s, &end, 10);
+    if (end != s && v > 0) ms = v;
+  }
+  return static_cast<uint64_t>(ms) * 1000000ull;
+}
+
+bool deterministic_requested() {
+  const char *v = std::getenv("DG_DETERMINISTIC");
+  return v != nullptr && *v != '\0' && *v != '0';
+}
+
+dg_status grouped_validate(const GroupedArgs &x) {
+  const char *fn = x.fn;
   if (x.G < 0) return fail(DG_ERR_INVALID_ARG, "%s: G = %d < 0", fn, x.G);
   if (x.G > DG_MAX_GROUPS)
-    return fail(DG_ERR_UNSUPPORTED, "%s: G = %d above DG_MAX_GROUPS", fn, x.G);
+    return fail(DG_ERR_UNSUPPORTED, "%s: G = %d above the maximum of %d experts", fn, x.G,
+                DG_MAX_GROUPS);
   const int mult = x.fp8 ? 16 : 8;
   if (x.M <= 0 || x.N <= 0 || x.M % mult || x.N % mult)
     return fail(DG_ERR_INVALID_ARG, "%s: M = %d, N = %d must be positive multiples of %d", fn,
                 x.M, x.N, mult);
   if (x.sum_k < 0) return fail(DG_ERR_INVALID_ARG, "%s: sum_k < 0", fn);
   if (x.sum_k > (int64_t)0x7FFFFF00)
-    return fail(DG_ERR_UNSUPPORTED, "%s: sum_k above 2^31 - 256", fn);
+    return fail(DG_ERR_UNSUPPORTED, "%s: sum_k above the maximum of 2^31 - 256", fn);
   if (x.fp8 && x.gran_k != 32 && x.gran_k != 128)
     return fail(DG_ERR_INVALID_ARG, "%s: gran_k = %d (must be 32 or 128)", fn, x.gran_k);
   if (x.d_dtype != DG_F32 && x.d_dtype != DG_BF16)
@@ -189,7 +211,7 @@ dg_status run_grouped(const GroupedArgs &x) {
   if (x.G == 0) {
     if (x.sum_k != 0)
       return fail(DG_ERR_INVALID_ARG, "%s: G = 0 but sum_k = %lld", fn, (long long)x.sum_k);
-    return ok();
+    return DG_OK;
   }
   if (x.ks_host == nullptr || x.ks_dev == nullptr)
     return fail(DG_ERR_INVALID_ARG, "%s: ks_host and ks_dev are required", fn);
@@ -216,76 +238,84 @@ dg_status run_grouped(const GroupedArgs &x) {
       return fail(DG_ERR_INVALID_ARG, "%s: sfa and sfb must be 16-byte aligned device pointers",
                   fn);
   }
-  DeviceState *dev = nullptr;
-  dg_status s = device_state(&dev);
-  if (s != DG_OK) return s;
+  return DG_OK;
+}
 
-  // ---- schedule: longest entries first, then output-only (fill) experts
-  std::unique_ptr<dg::WgradParams> hold(new dg::WgradParams);   // ~21 KB: off the stack
-  dg::WgradParams &p = *hold;
+void grouped_schedule(const GroupedArgs &x, int sms, WgradParams &p, PackParams &pk,
+                      GroupedPlan &g) {
   std::memset(&p, 0, sizeof(p));
+  std::memset(&pk, 0, sizeof(pk));
   // FP8 with N not a multiple of 224 but M one (the down-projection's 7168 x
   // 2048): compute D^T tiles instead, so that the 224-wide tile runs along M
   // with no ragged edge and the 256-row side along N.
-  const bool trans = x.fp8 && (x.N % 224 != 0) && (x.M % 224 == 0);
-  const int Mk = trans ? x.N : x.M, Nk = trans ? x.M : x.N;   // the kernel's M and N
-  const void *ka = trans ? x.b : x.a;
-  const void *kb = trans ? x.a : x.b;
-  const uint8_t *ksfa = trans ? x.sfb : x.sfa;
-  const uint8_t *ksfb = trans ? x.sfa : x.sfb;
-  const int bn = x.fp8 ? dg::fp8_pick_block_n(Nk) : dg::bf16_pick_block_n(Nk);
-  const int tpg = ((Mk + dg::kPairM - 1) / dg::kPairM) * ((Nk + bn - 1) / bn);
+  g.trans = x.fp8 && (x.N % 224 != 0) && (x.M % 224 == 0);
+  const int Mk = g.trans ? x.N : x.M, Nk = g.trans ? x.M : x.N;   // the kernel's M and N
+  g.ksfa = g.trans ? x.sfb : x.sfa;
+  g.ksfb = g.trans ? x.sfa : x.sfb;
+  g.bn = x.fp8 ? fp8_pick_block_n(Nk) : bf16_pick_block_n(Nk);
+  const int bn = g.bn;
+  const int tpg = ((Mk + kPairM - 1) / kPairM) * ((Nk + bn - 1) / bn);
   const bool reduce = (x.c == x.d) && x.d_dtype == DG_F32;   // D += acc in place
 
+  // Entries: (expert, first token, tokens); fixed-size per-thread storage, so
+  // that planning takes no heap memory.
   struct Entry {
     int expert;
     int64_t k_off;
     int k_len;
   };
-  std::vector<int64_t> off(x.G + 1, 0);
+  static thread_local Entry ents[2 * kMaxGroups];
+  static thread_local Entry split[kMaxGroups];
+  static thread_local int64_t off[kMaxGroups + 1];
+  int n = 0;
+  off[0] = 0;
   for (int e = 0; e < x.G; ++e) off[e + 1] = off[e] + x.ks_host[e];
-  std::vector<Entry> ents;
   for (int e = 0; e < x.G; ++e)
-    if (x.ks_host[e] > 0) ents.push_back(Entry{e, off[e], x.ks_host[e]});
+    if (x.ks_host[e] > 0) ents[n++] = Entry{e, off[e], x.ks_host[e]};
   // In-place accumulation: experts much longer than a CTA pair's fair share of
   // the work are split along K into several entries, each adding its part
   // into D (exact by linearity; the order of the FP32 additions then depends
   // on timing).  A pair's fair share is (stages x tiles) / pairs; entries are
   // capped at a quarter of it, in whole scale groups for FP8.
-  if (reduce && !ents.empty()) {
+  if (reduce && n > 0 && sms > 0 && !deterministic_requested()) {
     const int bk = x.fp8 ? 128 : 64;            // tokens per stage
     const int unit = x.fp8 ? 4 : 1;             // stages per split unit
     int64_t total = 0;
-    for (const Entry &en : ents) total += (en.k_len + bk - 1) / bk;
-    const int64_t share = total * tpg / std::max(1, dev->sms / 2);
+    for (int i = 0; i < n; ++i) total += (ents[i].k_len + bk - 1) / bk;
+    const int64_t share = total * tpg / std::max(1, sms / 2);
     const int64_t cap = std::max<int64_t>(8, share / 4);   // stages per entry
-    std::vector<Entry> split;
-    for (const Entry &en : ents) {
+    int ns = 0;
+    bool fits = true;
+    for (int i = 0; i < n && fits; ++i) {
+      const Entry &en = ents[i];
       const int64_t st = (en.k_len + bk - 1) / bk;
       if (st <= cap) {
-        split.push_back(en);
+        if (ns == kMaxGroups) { fits = false; break; }
+        split[ns++] = en;
         continue;
       }
       const int64_t parts = (st + cap - 1) / cap;
       int64_t per = (st + parts - 1) / parts;
       per = (per + unit - 1) / unit * unit;
       for (int64_t s0 = 0; s0 < st; s0 += per) {
+        if (ns == kMaxGroups) { fits = false; break; }
         const int64_t t0 = s0 * bk;
         const int64_t t1 = std::min<int64_t>(en.k_len, (s0 + per) * bk);
-        split.push_back(Entry{en.expert, en.k_off + t0, static_cast<int>(t1 - t0)});
+        split[ns++] = Entry{en.expert, en.k_off + t0, static_cast<int>(t1 - t0)};
       }
     }
-    if (static_cast<int>(split.size()) <= dg::kMaxGroups) ents.swap(split);
+    if (fits) {
+      for (int i = 0; i < ns; ++i) ents[i] = split[i];
+      n = ns;
+    }
   }
-  std::stable_sort(ents.begin(), ents.end(),
-                   [](const Entry &u, const Entry &v) { return u.k_len > v.k_len; });
-  const int n_mma = static_cast<int>(ents.size());
-  const bool fill_empty = (x.c != x.d);    // no accumulator, or a separate one
-  if (fill_empty)
+  std::stable_sort(ents, ents + n, [](const Entry &u, const Entry &v) { return u.k_len > v.k_len; });
+  g.n_mma = n;
+  if (x.c != x.d)   // no accumulator, or a separate one: empty experts still write D
     for (int e = 0; e < x.G; ++e)
-      if (x.ks_host[e] == 0) ents.push_back(Entry{e, off[e], 0});
-  const int n_groups = static_cast<int>(ents.size());
-  for (int i = 0; i < n_groups; ++i) {
+      if (x.ks_host[e] == 0) ents[n++] = Entry{e, off[e], 0};
+  g.n_sched = n;
+  for (int i = 0; i < n; ++i) {
     p.sched[i].expert = ents[i].expert;
     p.sched[i].k_off = static_cast<int>(ents[i].k_off);
     p.sched[i].k_len = ents[i].k_len;
@@ -294,56 +324,40 @@ dg_status run_grouped(const GroupedArgs &x) {
   p.M = Mk;
   p.N = Nk;
   p.G = x.G;
-  p.m_tiles = (Mk + dg::kPairM - 1) / dg::kPairM;
+  p.m_tiles = (Mk + kPairM - 1) / kPairM;
   p.n_tiles = (Nk + bn - 1) / bn;
   p.tiles_per_group = p.m_tiles * p.n_tiles;
-  p.num_mma_tiles = n_mma * p.tiles_per_group;
-  p.num_tiles = n_groups * p.tiles_per_group;
+  p.num_mma_tiles = g.n_mma * p.tiles_per_group;
+  p.num_tiles = n * p.tiles_per_group;
   p.gran_k = x.fp8 ? x.gran_k : 0;
-  p.chunk = x.fp8 ? dg::kFp8Chunk : dg::kBf16Chunk;
+  p.chunk = !x.fp8                  ? kBf16Chunk
+            : x.d_dtype == DG_BF16    ? kFp8ChunkBf16Out
+            : (x.c == x.d)            ? kFp8ChunkInPlace
+                                      : kFp8Chunk;
+  if (const char *v = std::getenv("DG_LANE_CHUNK")) {   // tuning override (multiple of 4)
+    const int c = std::atoi(v);
+    if (c > 0 && (!x.fp8 || c % 4 == 0)) p.chunk = c;
+  }
   // Sweep the smaller operand's tiles fastest: the concurrently running tiles
   // then share the larger operand's slices, and the smaller one stays in L2
   // from one sweep to the next.
   p.m_fastest = (Mk <= Nk) ? 1 : 0;
-  p.out_mode = (x.d_dtype == DG_BF16) ? dg::OUT_BF16
-               : (x.c == nullptr)     ? dg::OUT_F32
-               : (x.c == x.d)         ? dg::OUT_F32_REDUCE
-                                      : dg::OUT_F32_C;
-  p.wait_limit_ns = wait_limit_ns();
-  p.status = dev->status;
+  p.out_mode = (x.d_dtype == DG_BF16) ? OUT_BF16
+               : (x.c == nullptr)     ? OUT_F32
+               : (x.c == x.d)         ? OUT_F32_REDUCE
+                                      : OUT_F32_C;
   p.ks_dev = x.ks_dev;
-#ifdef DG_KERNEL_TIMERS
-  p.timers = g_timers;
-#endif
-  if (log_enabled()) {
-    int empty = 0, max_k = 0;
-    for (int e = 0; e < x.G; ++e) {
-      empty += (x.ks_host[e] == 0);
-      max_k = std::max(max_k, x.ks_host[e]);
-    }
-    std::fprintf(stderr,
-                 "[dg] %s: G=%d M=%d N=%d sum_k=%lld (%d empty, max K %d) | %s operands, %s tiles "
-                 "256 x %d, %d x %d per expert | %d GEMM entries (+%d from splits along K), "
-                 "%d GEMM tiles + %d output-only | out=%s | pairs=%d\n",
-                 fn, x.G, x.M, x.N, static_cast<long long>(x.sum_k), empty, max_k,
-                 x.kmajor ? "K-major" : "token-major", trans ? "transposed" : "direct", bn,
-                 p.m_tiles, p.n_tiles, n_mma, n_mma - (x.G - empty), p.num_mma_tiles,
-                 p.num_tiles - p.num_mma_tiles,
-                 p.out_mode == dg::OUT_BF16        ? "bf16"
-                 : p.out_mode == dg::OUT_F32       ? "f32"
-                 : p.out_mode == dg::OUT_F32_REDUCE ? "f32 += (reduce-add)"
-                                                    : "f32 = C +",
-                 std::min(dev->sms / 2, p.num_tiles));
-  }
-  if (p.num_tiles == 0) return ok();     // every expert empty and D accumulates in place
-  std::unique_ptr<dg::PackParams> pk_hold(new dg::PackParams);   // ~12 KB
-  dg::PackParams &pk = *pk_hold;
-  std::memset(&pk, 0, sizeof(pk));
-  const size_t sf_bytes = (x.fp8 && n_mma > 0) ? dg::plan_scale_pack(p, pk, n_mma, x.gran_k, bn) : 0;
+  g.sf_bytes = (x.fp8 && g.n_mma > 0) ? plan_scale_pack(p, pk, g.n_mma, x.gran_k, bn) : 0;
+  set_derived(p, n);
+}
 
-  // ---- tensor maps (operands in the kernel's roles; D and C as the caller's)
+dg_status grouped_maps(const GroupedArgs &x, const GroupedPlan &g, WgradParams &p) {
+  dg_status s = DG_OK;
   const uint64_t M = x.M, N = x.N, G = x.G, SK = x.sum_k;
-  const uint64_t MK = Mk, NK = Nk;
+  const uint64_t MK = p.M, NK = p.N;
+  const void *ka = g.trans ? x.b : x.a;
+  const void *kb = g.trans ? x.a : x.b;
+  const int bn = g.bn;
   if (p.num_mma_tiles > 0) {
     if (x.fp8 && x.kmajor) {
       // K-major: rows of sum_k bytes; one box = 128 tokens x 128 rows (A) or
@@ -363,13 +377,10 @@ dg_status run_grouped(const GroupedArgs &x) {
       // B: one box per CTA covers its bn / 2 columns (<= one 128-byte atom)
       const uint32_t boxb[2] = {static_cast<uint32_t>(std::min(128, bn / 2)), 128};
       if ((s = encode(&p.tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, ka, 2, da, sa, box,
-                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "a")))
+                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "a")) ||
+          (s = encode(&p.tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, kb, 2, db, sb, boxb,
+                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "b")))
         return s;
-      s = encode(&p.tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, kb, 2, db, sb, boxb,
-                 CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "b");
-      if (s) return s;
-      // The packed scale records are mapped (and the scratch taken) below,
-      // once every other map has been encoded.
     } else {
       const uint64_t da[2] = {M, SK}, sa[1] = {2 * M};
       const uint64_t db[2] = {N, SK}, sb[1] = {2 * N};
@@ -382,38 +393,105 @@ dg_status run_grouped(const GroupedArgs &x) {
         return s;
     }
   }
-  {
-    const bool bf = (x.d_dtype == DG_BF16);
-    const uint64_t es = bf ? 2 : 4;
-    const uint64_t dd[3] = {N, M, G}, sd[2] = {es * N, es * N * M};
-    const uint32_t box[3] = {dg::kEpiCols, 32, 1};
-    if ((s = encode(&p.tmD,
-                    bf ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, x.d,
-                    3, dd, sd, box, dg::epi_swizzle(bf ? 2 : 4),
-                    CU_TENSOR_MAP_L2_PROMOTION_NONE, "d")))
-      return s;
-    if (p.out_mode == dg::OUT_F32_C &&
-        (s = encode(&p.tmC, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, x.c, 3, dd, sd, box,
-                    dg::epi_swizzle(4), CU_TENSOR_MAP_L2_PROMOTION_NONE, "c")))
-      return s;
+  const bool bf = (x.d_dtype == DG_BF16);
+  const uint64_t es = bf ? 2 : 4;
+  const uint64_t dd[3] = {N, M, G}, sd[2] = {es * N, es * N * M};
+  const uint32_t box[3] = {kEpiCols, 32, 1};
+  if ((s = encode(&p.tmD, bf ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                  x.d, 3, dd, sd, box, epi_swizzle(bf ? 2 : 4), CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                  "d")))
+    return s;
+  if (p.out_mode == OUT_F32_C &&
+      (s = encode(&p.tmC, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, x.c, 3, dd, sd, box, epi_swizzle(4),
+                  CU_TENSOR_MAP_L2_PROMOTION_NONE, "c")))
+    return s;
+  return DG_OK;
+}
+
+dg_status grouped_scale_maps(const GroupedArgs &x, const GroupedPlan &g, void *scratch,
+                             WgradParams &p, PackParams &pk) {
+  (void)x;
+  bind_scale_pack(pk, scratch, g.ksfa, g.ksfb);
+  const uint64_t rec[1] = {512};
+  const uint64_t dpa[2] = {128, static_cast<uint64_t>(pk.n_groups) * pk.MC};
+  const uint64_t dpb[2] = {128, static_cast<uint64_t>(pk.n_groups) * pk.NT * pk.CB};
+  const uint32_t bpa[2] = {128, 1}, bpb[2] = {128, static_cast<uint32_t>(pk.CB)};
+  dg_status s;
+  if ((s = encode(&p.tmSFA, CU_TENSOR_MAP_DATA_TYPE_UINT32, pk.sfa_p, 2, dpa, rec, bpa,
+                  CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE, "sfa records")) ||
+      (s = encode(&p.tmSFB, CU_TENSOR_MAP_DATA_TYPE_UINT32, pk.sfb_p, 2, dpb, rec, bpb,
+                  CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE, "sfb records")))
+    return s;
+  return DG_OK;
+}
+
+cudaError_t grouped_launch(const GroupedArgs &x, const GroupedPlan &g, WgradParams &p, int sms) {
+  const int pairs = std::min(sms / 2, p.num_tiles);
+  return !x.fp8               ? launch_kgrouped_bf16(p, g.bn, pairs, x.stream)
+         : x.kmajor && g.trans ? launch_kgrouped_fp8_nt_t(p, g.bn, pairs, x.stream)
+         : x.kmajor           ? launch_kgrouped_fp8_nt(p, g.bn, pairs, x.stream)
+         : g.trans            ? launch_kgrouped_fp8_t(p, g.bn, pairs, x.stream)
+                              : launch_kgrouped_fp8(p, g.bn, pairs, x.stream);
+}
+
+}  // namespace dg
+
+namespace {
+
+using dg::GroupedArgs;
+using dg::wait_limit_ns;
+
+dg_status run_grouped(const GroupedArgs &x) {
+  const char *fn = x.fn;
+  dg_status s = dg::grouped_validate(x);
+  if (s != DG_OK) return s;
+  if (x.G == 0) return ok();
+  DeviceState *dev = nullptr;
+  if ((s = device_state(&dev)) != DG_OK) return s;
+
+  // ---- schedule: longest entries first, then output-only (fill) experts
+  std::unique_ptr<dg::WgradParams> hold(new dg::WgradParams);   // ~29 KB: off the stack
+  std::unique_ptr<dg::PackParams> pk_hold(new dg::PackParams);  // ~12 KB
+  dg::WgradParams &p = *hold;
+  dg::PackParams &pk = *pk_hold;
+  dg::GroupedPlan g{};
+  dg::grouped_schedule(x, dev->sms, p, pk, g);
+  p.wait_limit_ns = wait_limit_ns();
+  p.status = dev->status;
+#ifdef DG_KERNEL_TIMERS
+  p.timers = g_timers;
+#endif
+  if (log_enabled()) {
+    int empty = 0, max_k = 0;
+    for (int e = 0; e < x.G; ++e) {
+      empty += (x.ks_host[e] == 0);
+      max_k = std::max(max_k, x.ks_host[e]);
+    }
+    std::fprintf(stderr,
+                 "[dg] %s: G=%d M=%d N=%d sum_k=%lld (%d empty, max K %d) | %s operands, %s tiles "
+                 "256 x %d, %d x %d per expert | %d GEMM entries (+%d from splits along K), "
+                 "%d GEMM tiles + %d output-only | out=%s | pairs=%d\n",
+                 fn, x.G, x.M, x.N, static_cast<long long>(x.sum_k), empty, max_k,
+                 x.kmajor ? "K-major" : "token-major", g.trans ? "transposed" : "direct", g.bn,
+                 p.m_tiles, p.n_tiles, g.n_mma, g.n_mma - (x.G - empty), p.num_mma_tiles,
+                 p.num_tiles - p.num_mma_tiles,
+                 p.out_mode == dg::OUT_BF16        ? "bf16"
+                 : p.out_mode == dg::OUT_F32       ? "f32"
+                 : p.out_mode == dg::OUT_F32_REDUCE ? "f32 += (reduce-add)"
+                                                    : "f32 = C +",
+                 std::min(dev->sms / 2, p.num_tiles));
   }
+  if (p.num_tiles == 0) return ok();     // every expert empty and D accumulates in place
+  if ((s = dg::grouped_maps(x, g, p)) != DG_OK) return s;
 
   // ---- FP8 scale records: scratch from the pool, their tensor maps, the pack pass
   void *scratch = nullptr;
   cudaError_t e = cudaSuccess;
-  if (sf_bytes > 0) {
-    if ((e = cudaMallocFromPoolAsync(&scratch, sf_bytes, dev->pool, x.stream)) != cudaSuccess)
-      return fail(DG_ERR_CUDA, "%s: scale scratch (%zu bytes): %s", fn, sf_bytes,
+  if (g.sf_bytes > 0) {
+    if ((e = cudaMallocFromPoolAsync(&scratch, g.sf_bytes, dev->pool, x.stream)) != cudaSuccess)
+      return fail(DG_ERR_CUDA, "%s: scale scratch (%zu bytes): %s", fn, g.sf_bytes,
                   cudaGetErrorString(e));
-    dg::bind_scale_pack(pk, scratch, ksfa, ksfb);
-    const uint64_t rec[1] = {512};
-    const uint64_t dpa[2] = {128, static_cast<uint64_t>(pk.n_groups) * pk.MC};
-    const uint64_t dpb[2] = {128, static_cast<uint64_t>(pk.n_groups) * pk.NT * pk.CB};
-    const uint32_t bpa[2] = {128, 1}, bpb[2] = {128, static_cast<uint32_t>(pk.CB)};
-    if ((s = encode(&p.tmSFA, CU_TENSOR_MAP_DATA_TYPE_UINT32, pk.sfa_p, 2, dpa, rec, bpa,
-                    CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE, "sfa records")) ||
-        (s = encode(&p.tmSFB, CU_TENSOR_MAP_DATA_TYPE_UINT32, pk.sfb_p, 2, dpb, rec, bpb,
-                    CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE, "sfb records"))) {
+    if ((s = dg::grouped_scale_maps(x, g, scratch, p, pk)) != DG_OK) {
       cudaFreeAsync(scratch, x.stream);
       return s;
     }
@@ -424,13 +502,7 @@ dg_status run_grouped(const GroupedArgs &x) {
   }
 
   // ---- launch: one persistent CTA pair per two SMs (or per tile when fewer)
-  dg::set_derived(p, n_groups);
-  const int pairs = std::min(dev->sms / 2, p.num_tiles);
-  e = !x.fp8              ? dg::launch_kgrouped_bf16(p, bn, pairs, x.stream)
-      : x.kmajor && trans  ? dg::launch_kgrouped_fp8_nt_t(p, bn, pairs, x.stream)
-      : x.kmajor           ? dg::launch_kgrouped_fp8_nt(p, bn, pairs, x.stream)
-      : trans              ? dg::launch_kgrouped_fp8_t(p, bn, pairs, x.stream)
-                           : dg::launch_kgrouped_fp8(p, bn, pairs, x.stream);
+  e = dg::grouped_launch(x, g, p, dev->sms);
   if (scratch != nullptr) cudaFreeAsync(scratch, x.stream);   // after the GEMM in stream order
   if (e != cudaSuccess)
     return fail(DG_ERR_CUDA, "%s: launch failed: %s", fn, cudaGetErrorString(e));
@@ -699,19 +771,14 @@ dg_status run_cast(const char *fn, dg::CastArgs a, dg_layout q_layout, int gran_
 
 }  // namespace
 
-namespace dg {
-// Lets the allocation-free entry point (noalloc.cu) report through dg_last_error.
-void set_last_error(const char *msg) { g_err = (msg != nullptr) ? msg : ""; }
-}  // namespace dg
-
 extern "C" {
 
 dg_status dg_k_grouped_fp8_wgrad(const void *a, const uint8_t *sfa, const void *b,
                                  const uint8_t *sfb, void *d, dg_dtype d_dtype, const float *c,
                                  int G, int M, int N, int64_t sum_k, const int *ks_host,
                                  const int *ks_dev, int gran_k, dg_stream_t stream) {
-  GroupedArgs x{true, false, a, b, sfa, sfb, d, d_dtype, c, G, M, N, sum_k, ks_host, ks_dev,
-                gran_k, reinterpret_cast<cudaStream_t>(stream)};
+  GroupedArgs x{"dg_k_grouped_fp8_wgrad", true, false, a, b, sfa, sfb, d, d_dtype, c, G, M, N,
+                sum_k, ks_host, ks_dev, gran_k, reinterpret_cast<cudaStream_t>(stream)};
   return run_grouped(x);
 }
 
@@ -720,16 +787,16 @@ dg_status dg_k_grouped_fp8_wgrad_nt(const void *a, const uint8_t *sfa, const voi
                                     const float *c, int G, int M, int N, int64_t sum_k,
                                     const int *ks_host, const int *ks_dev, int gran_k,
                                     dg_stream_t stream) {
-  GroupedArgs x{true, true, a, b, sfa, sfb, d, d_dtype, c, G, M, N, sum_k, ks_host, ks_dev,
-                gran_k, reinterpret_cast<cudaStream_t>(stream)};
+  GroupedArgs x{"dg_k_grouped_fp8_wgrad_nt", true, true, a, b, sfa, sfb, d, d_dtype, c, G, M,
+                N, sum_k, ks_host, ks_dev, gran_k, reinterpret_cast<cudaStream_t>(stream)};
   return run_grouped(x);
 }
 
 dg_status dg_k_grouped_bf16_wgrad(const void *a, const void *b, void *d, dg_dtype d_dtype,
                                   const float *c, int G, int M, int N, int64_t sum_k,
                                   const int *ks_host, const int *ks_dev, dg_stream_t stream) {
-  GroupedArgs x{false, false, a, b, nullptr, nullptr, d, d_dtype, c, G, M, N, sum_k, ks_host,
-                ks_dev, 0, reinterpret_cast<cudaStream_t>(stream)};
+  GroupedArgs x{"dg_k_grouped_bf16_wgrad", false, false, a, b, nullptr, nullptr, d, d_dtype, c,
+                G, M, N, sum_k, ks_host, ks_dev, 0, reinterpret_cast<cudaStream_t>(stream)};
   return run_grouped(x);
 }
 
@@ -853,17 +920,37 @@ dg_status dg_swiglu_backward_quant_fp8(const void *h, const void *da, int64_t T,
 const char *dg_last_error(void) { return g_err.c_str(); }
 
 dg_status dg_sync_check(dg_stream_t stream) {
-  DeviceState *dev = nullptr;
-  dg_status s = device_state(&dev);
-  if (s != DG_OK) return s;
-  cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+  // Reads the records that exist; allocates nothing (a device on which no
+  // allocating entry point has run has no ordinary record yet).
+  int devi = 0;
+  cudaError_t e = cudaGetDevice(&devi);
+  if (e != cudaSuccess) return fail(DG_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  dg::DevStatus *rec = nullptr;
+  if (devi >= 0 && devi < kMaxDevices) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (g_dev[devi].init) {
+      if (!g_dev[devi].arch_ok)
+        return fail(DG_ERR_UNSUPPORTED, "device is sm_%d%d; this library is built for sm_103a only",
+                    g_dev[devi].major, g_dev[devi].minor);
+      rec = g_dev[devi].status;
+    }
+  }
+  e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(DG_ERR_CUDA, "stream synchronise: %s", cudaGetErrorString(e));
   dg::DevStatus st{};
-  if ((e = cudaMemcpy(&st, dev->status, sizeof(st), cudaMemcpyDeviceToHost)) != cudaSuccess)
+  if (rec != nullptr) {
+    if ((e = cudaMemcpy(&st, rec, sizeof(st), cudaMemcpyDeviceToHost)) != cudaSuccess)
+      return fail(DG_ERR_CUDA, "status read: %s", cudaGetErrorString(e));
+    if (st.code != dg::DEV_OK && (e = cudaMemset(rec, 0, sizeof(st))) != cudaSuccess)
+      return fail(DG_ERR_CUDA, "status reset: %s", cudaGetErrorString(e));
+  }
+  // The allocation-free entry point's record (read and cleared likewise).
+  dg::DevStatus na{};
+  bool present = false;
+  if ((e = dg::noalloc_take_status(&na, &present)) != cudaSuccess)
     return fail(DG_ERR_CUDA, "status read: %s", cudaGetErrorString(e));
+  if (st.code == dg::DEV_OK && present) st = na;
   if (st.code == dg::DEV_OK) return ok();
-  if ((e = cudaMemset(dev->status, 0, sizeof(st))) != cudaSuccess)
-    return fail(DG_ERR_CUDA, "status reset: %s", cudaGetErrorString(e));
   if (st.code == dg::DEV_TIMEOUT)
     return fail(DG_ERR_TIMEOUT, "device wait timed out (site 0x%x, block %d, detail %d)",
                 st.where, st.block, st.detail);

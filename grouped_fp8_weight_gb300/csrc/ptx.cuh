@@ -44,6 +44,45 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// The same with cluster-scope acquire: for a phase completed by a
+// cluster-scope release from the other CTA of the pair (its generic writes
+// to its own shared memory must be seen by work this thread starts next).
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// try_wait whose suspension ends after at most about `hint_ns` nanoseconds
+// (the thread sleeps until the phase completes or the hint expires).
+template <bool kClusterScope>
+__device__ __forceinline__ bool mbar_try_wait_hint(uint64_t *bar, uint32_t parity,
+                                                   uint32_t hint_ns) {
+  uint32_t ok;
+  if constexpr (kClusterScope) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+  }
+  return ok != 0;
+}
 
 // Status words a kernel may record (first writer wins), read back by the host.
 enum : int { DEV_OK = 0, DEV_KS_MISMATCH = 1, DEV_BAD_ROW = 2, DEV_BAD_ROUTE = 3, DEV_TIMEOUT = 4 };
@@ -58,16 +97,26 @@ struct DevStatus {
 // Bounded wait on an mbarrier phase.  Returns false if the CTA-wide abort flag
 // is (or becomes) set (unless honor_abort is false: drains before exit), or if
 // the wait exceeds limit_ns; in the latter case the abort flag is set and the
-// status word records DEV_TIMEOUT.
+// status word records DEV_TIMEOUT.  After a first plain try_wait, the thread
+// sleeps in try_waits whose suspension is capped at a quarter of the limit
+// (250 ns to 250 us), checking the clock after each, so that the limit is
+// honoured to that granularity however long the hardware's own suspension
+// window is.
+template <bool kClusterScope = false>
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
                                           uint64_t limit_ns, DevStatus *st, int where,
                                           int detail, bool honor_abort = true) {
-  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t q = limit_ns / 4;
+  const uint32_t hint = static_cast<uint32_t>(q < 250 ? 250 : (q > 250000 ? 250000 : q));
+  // (a limit below 1 ms -- tests of the timeout path -- caps the first
+  // suspension too; production limits are seconds)
+  if (limit_ns < 1000000ull ? mbar_try_wait_hint<kClusterScope>(bar, parity, hint)
+      : kClusterScope       ? mbar_try_wait_cluster(bar, parity)
+                            : mbar_try_wait(bar, parity))
+    return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
-#pragma unroll 1
-    for (int i = 0; i < 32; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_hint<kClusterScope>(bar, parity, hint)) return true;
     if (honor_abort && *abort_flag) return false;
     if (globaltimer_ns() - t0 > limit_ns) {
       *abort_flag = 1;
@@ -80,6 +129,26 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
       return false;
     }
   }
+}
+
+// One lane of the (fully active) warp: the lowest.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t e;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "elect.sync _|p, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(e));
+  return e != 0;
+}
+
+// Limit of the waits a CTA makes before it exits, for copies it started
+// itself (drains): at least 2 s whatever the call's wait limit, so that a
+// kernel ended early by a short limit still lets every copy in flight land
+// before its shared memory is released.  After one such wait gives up, the
+// copies have long landed and the remaining drain waits are skipped.
+__host__ __device__ constexpr uint64_t drain_limit_ns(uint64_t limit_ns) {
+  return limit_ns > 2000000000ull ? limit_ns : 2000000000ull;
 }
 
 // ---------------------------------------------------------------- cluster

@@ -523,7 +523,8 @@ __global__ void __launch_bounds__(256, 3) gather_cast_kernel(const __grid_consta
   }
   if (!mbar_wait(bar, 0, abort_flag, a.wait_limit_ns, a.status, 0x41, blockIdx.x)) {
     // gave up: let the copies in flight land (bounded) before the CTA exits
-    mbar_wait(bar, 0, abort_flag, a.wait_limit_ns, a.status, 0x42, blockIdx.x, false);
+    mbar_wait(bar, 0, abort_flag, drain_limit_ns(a.wait_limit_ns), a.status, 0x42, blockIdx.x,
+              false);
     return;
   }
 

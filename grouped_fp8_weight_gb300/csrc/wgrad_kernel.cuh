@@ -23,8 +23,9 @@
 //               (BF16) tokens; both CTAs' bytes complete on the even CTA's
 //               `full` barrier.
 //   warp 1      tensor-memory allocation (collective over the pair); in the
-//               even CTA one thread issues tcgen05.cp per scale group and four
-//               tcgen05.mma per stage, committing to both CTAs' barriers.
+//               even CTA the warp walks the schedule and one elected lane
+//               issues tcgen05.cp per scale group and four tcgen05.mma per
+//               stage, committing to both CTAs' barriers.
 //   warps 2..5  epilogue, one warp per tensor-memory lane quadrant (32 rows),
 //               each on its own: tensor memory -> registers -> swizzled
 //               shared-memory staging -> TMA store (or TMA reduce-add for
@@ -59,6 +60,13 @@
 
 #include <cuda_bf16.h>
 
+// The MMA issuer runs as a whole warp with warp-uniform control flow; one
+// lane, elected once, issues every tcgen05 instruction, and every wait result
+// is made warp-uniform (a single thread issuing from divergent code kept the
+// tensor pipe less than half busy).
+#define DG_ISSUE if (mma_el)
+#define DG_MMA_OK(x) (__all_sync(0xffffffffu, (x)))
+
 #include "wgrad_params.h"
 
 namespace dg {
@@ -71,7 +79,14 @@ struct WgradCfg {
   // 32-column chunk with one staging buffer, which releases an accumulator in
   // about half the time.  Roles: warp 0 producer, 1 MMA, 6 scale loader /
   // BF16 gate, the rest epilogue.
-  static constexpr int EPI_WARPS = kTransD ? 8 : 4;
+  // Register-held drain (weight gradient): each of two warps per quadrant
+  // reads its whole share of a finished accumulator (every other 32-column
+  // chunk) into registers, releases the accumulator at once, and only then
+  // stages and stores those chunks; the accumulator is busy for the MMAs and
+  // one tensor-memory read instead of the whole drain.
+  static constexpr bool REG_EPI = kFP8 && !kMG;
+  static constexpr int EPI_WARPS = (kTransD || REG_EPI) ? 8 : 4;
+  static constexpr int EPI_CH = (kBN / kEpiCols + 1) / 2;   // chunks a warp holds (at most)
   static constexpr int THREADS = 32 * (3 + EPI_WARPS);
   static_assert(!kKMajor || kFP8, "K-major operands: FP8 only");
   static_assert(!kMG || kFP8, "M-grouped: FP8");
@@ -496,19 +511,22 @@ __global__ void __launch_bounds__((WgradCfg<kFP8, kBN, kKMajor, kMG, kTransD>::T
       // Let every load this CTA started land before the pair can exit: the
       // even CTA sees them on `full`; its partner sees the stages released.
       for (uint32_t i = (armed > static_cast<uint32_t>(S) ? armed - S : 0); i < armed; ++i) {
-        if (leader)
-          mbar_wait(&full[i % S], (i / S) & 1, abort_flag, lim, p.status, W_PROD_DRAIN,
-                    static_cast<int>(i), false);
-        else
-          mbar_wait(&empty[i % S], (i / S) & 1, abort_flag, lim, p.status, W_PROD_DRAIN,
-                    static_cast<int>(i), false);
+        const bool landed =
+            leader ? mbar_wait(&full[i % S], (i / S) & 1, abort_flag, drain_limit_ns(lim),
+                               p.status, W_PROD_DRAIN, static_cast<int>(i), false)
+                   : mbar_wait(&empty[i % S], (i / S) & 1, abort_flag, drain_limit_ns(lim),
+                               p.status, W_PROD_DRAIN, static_cast<int>(i), false);
+        if (!landed) break;
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (even CTA)
-    // One thread; per stage only constant-offset descriptor updates and the
-    // four MMAs, so that issue keeps ahead of the tensor pipe.
-    if (lane == 0 && leader) {
+    // The whole warp walks the schedule in lockstep (waits made warp-uniform);
+    // one lane, elected once, issues the copies, MMAs and commits.  Per stage
+    // only constant-offset descriptor updates and the four MMAs, so that issue
+    // keeps ahead of the tensor pipe.
+    const bool mma_el = elect_one();   // the issuing lane
+    if (leader) {
       int s = 0, g = 0;
       uint32_t ph = 0, gph = 0;
       uint32_t sfa_t = 0, sfb_t = 0;
@@ -541,7 +559,7 @@ __global__ void __launch_bounds__((WgradCfg<kFP8, kBN, kKMajor, kMG, kTransD>::T
         if (ch.j0 == 0) {
           // the buffer's previous tile has been drained by both epilogues
           DG_T0(w0);
-          ok = mbar_wait(&acce[b], (uses[b] & 1) ^ 1, abort_flag, lim, p.status, W_MMA_ACCE, t);
+          ok = DG_MMA_OK(mbar_wait(&acce[b], (uses[b] & 1) ^ 1, abort_flag, lim, p.status, W_MMA_ACCE, t));
           DG_TACC(1, w0);
           if (!ok) break;
           tc_fence_after();
@@ -554,19 +572,19 @@ __global__ void __launch_bounds__((WgradCfg<kFP8, kBN, kKMajor, kMG, kTransD>::T
           if constexpr (kFP8) {
             if ((jj & gs_mask) == 0) {
               DG_T0(w1);
-              ok = mbar_wait(&sfr[g], gph, abort_flag, lim, p.status, W_MMA_SFR, t);
+              ok = DG_MMA_OK(mbar_wait(&sfr[g], gph, abort_flag, lim, p.status, W_MMA_SFR, t));
               DG_TACC(2, w1);
               if (!ok) break;
               tc_fence_after();
               sfa_t = tmem_base + Cfg::SF_COL0 + g * Cfg::SF_COLS;
               sfb_t = sfa_t + 4;
-              tmem_cp_32x128b_warpx4_pair(sfa_t, uta_desc0 + static_cast<uint64_t>(g * (Cfg::UT_A >> 4)));
+              DG_ISSUE tmem_cp_32x128b_warpx4_pair(sfa_t, uta_desc0 + static_cast<uint64_t>(g * (Cfg::UT_A >> 4)));
 #pragma unroll
               for (int c = 0; c < Cfg::SF_CHUNKS_B; ++c)
-                tmem_cp_32x128b_warpx4_pair(
+                DG_ISSUE tmem_cp_32x128b_warpx4_pair(
                     sfb_t + 4 * c,
                     utb_desc0 + static_cast<uint64_t>(g * (Cfg::UT_B >> 4) + c * (512 >> 4)));
-              mma_commit_pair(&sfe[g], 0x3);
+              DG_ISSUE mma_commit_pair(&sfe[g], 0x3);
               if (++g == NS) { g = 0; gph ^= 1; }
             }
           }
@@ -575,8 +593,11 @@ __global__ void __launch_bounds__((WgradCfg<kFP8, kBN, kKMajor, kMG, kTransD>::T
           // expert's last, partial BF16 stage once warp 6 has also masked the
           // rows past the slice in both CTAs (`gate`, used by tail stages only).
           const bool tail = !kFP8 && jj == ch.nk - 1 && tcm.k_len - jj * Cfg::BK < Cfg::BK;
-          ok = mbar_wait(tail ? &gate[s] : &full[s], tail ? (gate_ph >> s) & 1u : ph, abort_flag,
-                         lim, p.status, W_MMA_FULL, t);
+          // (the gate's phase is completed by a cluster-scope release from the
+          // odd CTA, whose zeroed rows the MMA reads: cluster-scope acquire)
+          ok = DG_MMA_OK(tail ? mbar_wait<true>(&gate[s], (gate_ph >> s) & 1u, abort_flag, lim,
+                                                p.status, W_MMA_FULL, t)
+                              : mbar_wait(&full[s], ph, abort_flag, lim, p.status, W_MMA_FULL, t));
           if (tail) gate_ph ^= 1u << s;
           DG_TACC(2, w2);
           if (!ok) break;
@@ -590,12 +611,12 @@ __global__ void __launch_bounds__((WgradCfg<kFP8, kBN, kKMajor, kMG, kTransD>::T
             const uint64_t bd = b_desc + static_cast<uint64_t>(ks * (Cfg::B_KSTEP >> 4));
             if constexpr (kFP8) {
               const uint32_t idesc = (gs == 4) ? idesc_j : (kIdescBase | (static_cast<uint32_t>(ks) * 0x20000010u));
-              mma_mxf8_pair(d_tmem, ad, bd, idesc, sfa_t, sfb_t, (j | ks) != 0);
+              DG_ISSUE mma_mxf8_pair(d_tmem, ad, bd, idesc, sfa_t, sfb_t, (j | ks) != 0);
             } else {
-              mma_bf16_pair(d_tmem, ad, bd, kIdescBase, (j | ks) != 0);
+              DG_ISSUE mma_bf16_pair(d_tmem, ad, bd, kIdescBase, (j | ks) != 0);
             }
           }
-          mma_commit_pair(&empty[s], 0x3);
+          DG_ISSUE mma_commit_pair(&empty[s], 0x3);
           if (++s == S) {
             s = 0;
             ph ^= 1;
@@ -608,14 +629,14 @@ __global__ void __launch_bounds__((WgradCfg<kFP8, kBN, kKMajor, kMG, kTransD>::T
         }
         if (!ok) break;
         if (ch.j1 == ch.nk) {
-          mma_commit_pair(&accf[b], 0x3);
+          DG_ISSUE mma_commit_pair(&accf[b], 0x3);
           ++uses[b];
         }
       }
       // Drain: every tcgen05 op issued here completes before tensor memory
       // is released.
-      mma_commit_pair(drain, 0x1);
-      mbar_wait(drain, 0, abort_flag, lim, p.status, W_MMA_DRAIN, 0, false);
+      DG_ISSUE mma_commit_pair(drain, 0x1);
+      mbar_wait(drain, 0, abort_flag, drain_limit_ns(lim), p.status, W_MMA_DRAIN, 0, false);
     }
   } else if (warp == 6) {
     if constexpr (!kFP8) {
@@ -743,15 +764,189 @@ __global__ void __launch_bounds__((WgradCfg<kFP8, kBN, kKMajor, kMG, kTransD>::T
         // the even CTA sees them on `sfr`; its partner sees the slots' copies
         // complete.
         for (uint32_t i = (ig > static_cast<uint32_t>(NS) ? ig - NS : 0); i < ig; ++i) {
-          if (leader)
-            mbar_wait(&sfr[i % NS], (i / NS) & 1, abort_flag, lim, p.status, W_PROD_DRAIN,
-                      static_cast<int>(i), false);
-          else
-            mbar_wait(&sfe[i % NS], (i / NS) & 1, abort_flag, lim, p.status, W_PROD_DRAIN,
-                      static_cast<int>(i), false);
+          const bool landed =
+              leader ? mbar_wait(&sfr[i % NS], (i / NS) & 1, abort_flag, drain_limit_ns(lim),
+                                 p.status, W_PROD_DRAIN, static_cast<int>(i), false)
+                     : mbar_wait(&sfe[i % NS], (i / NS) & 1, abort_flag, drain_limit_ns(lim),
+                                 p.status, W_PROD_DRAIN, static_cast<int>(i), false);
+          if (!landed) break;
         }
       }
     }
+  } else if constexpr (Cfg::REG_EPI) {
+    // ------------------------------------------------------------ epilogue (register-held)
+    // Two warps per tensor-memory lane quadrant; each takes every other
+    // 32-column chunk of a finished tile (the two swap sets from tile to tile,
+    // so each stores half the columns on average).  A warp reads up to three
+    // of its chunks into registers with one tcgen05.wait (a fourth after its
+    // first chunk is staged) and releases the accumulator as soon as every
+    // read of it has completed, then stages and stores the chunks from
+    // registers: the accumulator is held for the MMAs and its read-out, not
+    // for the whole drain.
+    const int q = warp & 3;
+    const int ew = warp < 6 ? warp - 2 : warp - 3;
+    const int half = ew >> 2;
+    uint32_t uses[2] = {0, 0};
+    uint32_t cuse = 0, ntile = 0;
+    bool stg_busy = false;
+    constexpr bool kHasC = (kOut == OUT_F32_C);
+    constexpr int EC = Cfg::EC;
+    constexpr int NCH = Cfg::EPI_CH;           // chunks of this warp per tile (at most)
+    constexpr int H = NCH < 2 ? NCH : 2;       // chunks held in registers at once
+    static_assert(Cfg::EPI_BUFS == 1, "one staging buffer per warp");
+    const uint64_t stream_out = l2_policy_evict_first();
+    const uint32_t acce_leader = mapa_shared(smem_u32(&acce[0]), 0);
+    uint8_t *stg = smem + Cfg::OFF_STG + ew * Cfg::WSTG_BYTES;
+    uint64_t *wcbar = cbar + ew;
+    uint32_t r[H][EC];
+    LaneSched L;
+    lane_init(L, p, pid, R, sched);
+    Chunk ch;
+    bool ok = true;
+    // Stage chunk c of the current tile from registers rr and store it.
+    auto emit = [&](uint32_t(&rr)[EC], int c, int row0, int n0, int expert, int t) -> bool {
+      DG_T0(w1);
+      if (lane == 0 && stg_busy) bulk_wait_read<0>();   // the previous store has read stg
+      __syncwarp();
+      DG_TACC(2, w1);
+      const int bx = kTransD ? row0 : n0 + EC * c;
+      const int by = kTransD ? n0 + EC * c : row0;
+      if constexpr (kHasC) {
+        if (lane == 0) {
+          mbar_arrive_expect_tx(wcbar, 32 * EC * 4);
+          tma_load_3d(stg, &p.tmC, wcbar, bx, by, expert);
+        }
+        bool got = mbar_wait(wcbar, cuse & 1, abort_flag, lim, p.status, W_EPI_C, t);
+        ++cuse;
+        if (!__all_sync(0xffffffffu, got)) return false;
+        if constexpr (kTransD) {
+#pragma unroll
+          for (int j = 0; j < EC; ++j)
+            rr[j] = __float_as_uint(__uint_as_float(rr[j]) + *reinterpret_cast<const float *>(
+                stg + j * (32 * 4) + (swz_chunk<32 * 4>(lane >> 2, j) << 4) + (lane & 3) * 4));
+        } else {
+          const uint8_t *rowp = stg + lane * (EC * 4);
+#pragma unroll
+          for (int j = 0; j < EC / 4; ++j) {
+            const float4 cv = *reinterpret_cast<const float4 *>(rowp + (swz_chunk<EC * 4>(j, lane) << 4));
+            rr[4 * j + 0] = __float_as_uint(__uint_as_float(rr[4 * j + 0]) + cv.x);
+            rr[4 * j + 1] = __float_as_uint(__uint_as_float(rr[4 * j + 1]) + cv.y);
+            rr[4 * j + 2] = __float_as_uint(__uint_as_float(rr[4 * j + 2]) + cv.z);
+            rr[4 * j + 3] = __float_as_uint(__uint_as_float(rr[4 * j + 3]) + cv.w);
+          }
+        }
+        __syncwarp();   // every lane has read the C box before it is overwritten
+      }
+      if constexpr (kTransD) {
+        static_assert(EC == 32, "transposed boxes are 32 x 32");
+        if constexpr (kOut == OUT_BF16) {
+#pragma unroll
+          for (int j = 0; j < EC; ++j)
+            *reinterpret_cast<__nv_bfloat16 *>(stg + j * 64 + (swz_chunk<64>(lane >> 3, j) << 4) +
+                                               (lane & 7) * 2) =
+                __float2bfloat16_rn(__uint_as_float(rr[j]));
+        } else {
+#pragma unroll
+          for (int j = 0; j < EC; ++j)
+            *reinterpret_cast<uint32_t *>(stg + j * 128 + (swz_chunk<128>(lane >> 2, j) << 4) +
+                                          (lane & 3) * 4) = rr[j];
+        }
+      } else if constexpr (kOut == OUT_BF16) {
+        uint8_t *rowp = stg + lane * (EC * 2);
+#pragma unroll
+        for (int j = 0; j < EC / 8; ++j) {
+          uint32_t w[4];
+#pragma unroll
+          for (int h = 0; h < 4; ++h) {
+            const __nv_bfloat162 pr = __floats2bfloat162_rn(__uint_as_float(rr[8 * j + 2 * h]),
+                                                            __uint_as_float(rr[8 * j + 2 * h + 1]));
+            w[h] = *reinterpret_cast<const uint32_t *>(&pr);
+          }
+          *reinterpret_cast<uint4 *>(rowp + (swz_chunk<EC * 2>(j, lane) << 4)) =
+              make_uint4(w[0], w[1], w[2], w[3]);
+        }
+      } else {
+        uint8_t *rowp = stg + lane * (EC * 4);
+#pragma unroll
+        for (int j = 0; j < EC / 4; ++j)
+          *reinterpret_cast<uint4 *>(rowp + (swz_chunk<EC * 4>(j, lane) << 4)) =
+              make_uint4(rr[4 * j], rr[4 * j + 1], rr[4 * j + 2], rr[4 * j + 3]);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        if constexpr (kOut == OUT_F32_REDUCE)
+          tma_reduce_add_3d_hint(&p.tmD, stg, bx, by, expert, stream_out);
+        else
+          tma_store_3d_hint(&p.tmD, stg, bx, by, expert, stream_out);
+        bulk_commit();
+      }
+      stg_busy = true;
+      return true;
+    };
+    while (ok && lane_next(L, p, pid, R, Cfg::BK, ch)) {
+      if (ch.nk > 0 && ch.j1 != ch.nk) continue;   // only tile completions
+      const int t = ch.u;
+      const TileCoord tc = tile_coord<kMG>(p, sched, ch.u, kBN, rank);
+      const bool mma_tile = ch.nk > 0;
+      const int b = ch.lane;
+      const int sel = half ^ static_cast<int>(ntile & 1);   // this tile's chunk set
+      ++ntile;
+      const int ncols = min(kBN, p.N - tc.n0);
+      const int nch = (ncols + EC - 1) / EC;
+      const int mine = nch > sel ? (nch - sel + 1) / 2 : 0;   // chunks sel, sel + 2, ...
+      const int row0 = tc.m0 + 32 * q;
+      const uint32_t tmem_row = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + b * kBN;
+      if (mma_tile) {
+        DG_T0(w0);
+        bool got = mbar_wait(&accf[b], uses[b] & 1, abort_flag, lim, p.status, W_EPI_ACCF, t);
+        DG_TACC(1, w0);
+        if (!__all_sync(0xffffffffu, got)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int i = 0; i < H; ++i)
+          if (i < mine) tmem_ld_row<EC>(tmem_row + EC * (sel + 2 * i), r[i]);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < H; ++i) tmem_reg_fence_n<EC>(r[i]);
+        if (mine <= H) {
+          // every read of this buffer has completed: release it (CTA-scope arrive)
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_remote(acce_leader + 8 * b);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < H; ++i)
+#pragma unroll
+          for (int j = 0; j < EC; ++j) r[i][j] = 0u;
+      }
+      // chunk i sits in slot i % H; once it is stored, the slot takes chunk
+      // i + H, and the accumulator is released after its last chunk's read
+#pragma unroll
+      for (int i = 0; i < NCH; ++i) {
+        if (!ok || i >= mine) break;
+        ok = emit(r[i % H], sel + 2 * i, row0, tc.n0, tc.expert, t);
+        if (ok && i + H < NCH && i + H < mine) {
+          if (mma_tile) {
+            tmem_ld_row<EC>(tmem_row + EC * (sel + 2 * (i + H)), r[i % H]);
+            tmem_wait_ld();
+            tmem_reg_fence_n<EC>(r[i % H]);
+            if (i + H == mine - 1) {
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive_remote(acce_leader + 8 * b);
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < EC; ++j) r[i % H][j] = 0u;
+          }
+        }
+      }
+      if (!ok) break;
+      if (mma_tile) ++uses[b];
+    }
+    if (lane == 0) bulk_wait<0>();
   } else {
     // ------------------------------------------------------------ epilogue
     // Each warp owns one tensor-memory lane quadrant (32 rows of this CTA's

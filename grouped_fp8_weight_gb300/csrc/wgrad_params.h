@@ -204,9 +204,15 @@ cudaError_t launch_moe_layout_plan(const MoePlanArgs &a, int sms, cudaStream_t s
 // columns of N.
 constexpr int kPairM = 256;
 // Stages of a long tile issued per turn before the MMA stream switches to the
-// other accumulator's tile (FP8 stages are 128 tokens, BF16 64).
-constexpr int kFp8Chunk = 16;
-static_assert(kFp8Chunk % 4 == 0, "lane chunks must start on a scale group (four k-blocks)");
+// other accumulator's tile (FP8 stages are 128 tokens, BF16 64).  FP32 output
+// (4 bytes per element to store) drains a tile in about as long as 48 MMA
+// stages take; BF16 output in half that, and its tiles interleave best in
+// short turns; in-place accumulation (reduce-add) was measured best at 16.
+constexpr int kFp8Chunk = 48;
+constexpr int kFp8ChunkBf16Out = 8;
+constexpr int kFp8ChunkInPlace = 16;
+static_assert(kFp8Chunk % 4 == 0 && kFp8ChunkBf16Out % 4 == 0 && kFp8ChunkInPlace % 4 == 0,
+              "lane chunks must start on a scale group (four k-blocks)");
 // Epilogue chunk: output columns per staged TMA store box (32 rows high).
 constexpr int kEpiCols = 32;
 // Staging row of kEpiCols elements of `bytes` each is stored with the TMA
