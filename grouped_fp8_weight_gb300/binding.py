@@ -78,16 +78,39 @@ def _check(status: int):
         raise DGError(status, lib().dg_last_error().decode())
 
 
-def _stream(stream):
+_RAW_STREAM = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
+def _stream(stream, t=None):
+    """The CUDA stream handle to launch on: `stream`'s, or the current stream of
+    tensor t's device (of the current device when t is None)."""
     if stream is None:
+        if _RAW_STREAM is not None:
+            idx = t.device.index if t is not None and t.device.index is not None \
+                else torch.cuda.current_device()
+            return _RAW_STREAM(idx)
         return torch.cuda.current_stream().cuda_stream
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
 
+_KS_CACHE = {}
+
+
 def _ks_host(ks):
+    """ks as a ctypes int array (the host copy the C call reads), with its
+    length.  Arrays of recently seen count lists are reused (they are only
+    read by the call)."""
     if isinstance(ks, torch.Tensor):
         ks = ks.tolist()
-    return (ctypes.c_int * max(1, len(ks)))(*[int(k) for k in ks]), len(ks)
+    key = tuple(ks)
+    hit = _KS_CACHE.get(key)
+    if hit is not None:
+        return hit
+    arr = (ctypes.c_int * max(1, len(key)))(*[int(k) for k in key])
+    if len(_KS_CACHE) >= 64:
+        _KS_CACHE.clear()
+    _KS_CACHE[key] = (arr, len(key))
+    return arr, len(key)
 
 
 def _dptr(t):
@@ -131,7 +154,7 @@ def dg_k_grouped_fp8_wgrad(a, sfa, b, sfb, d, c, ks_host, ks_dev, gran_k: int = 
     _check(lib().dg_k_grouped_fp8_wgrad(
         _dptr(a8), _dptr(sfa), _dptr(b8), _dptr(sfb), _dptr(d),
         DG_BF16 if d.dtype == torch.bfloat16 else DG_F32,
-        _dptr(c), G, M, N, a8.shape[0], kh, _dptr(ks_dev), gran_k, _stream(stream)))
+        _dptr(c), G, M, N, a8.shape[0], kh, _dptr(ks_dev), gran_k, _stream(stream, d)))
 
 
 def dg_k_grouped_fp8_wgrad_nt(a, sfa, b, sfb, d, c, ks_host, ks_dev, gran_k: int = 128,
@@ -159,7 +182,7 @@ def dg_k_grouped_fp8_wgrad_nt(a, sfa, b, sfb, d, c, ks_host, ks_dev, gran_k: int
     _check(lib().dg_k_grouped_fp8_wgrad_nt(
         _dptr(a8), _dptr(sfa), _dptr(b8), _dptr(sfb), _dptr(d),
         DG_BF16 if d.dtype == torch.bfloat16 else DG_F32,
-        _dptr(c), G, M, N, a8.shape[1], kh, _dptr(ks_dev), gran_k, _stream(stream)))
+        _dptr(c), G, M, N, a8.shape[1], kh, _dptr(ks_dev), gran_k, _stream(stream, d)))
 
 
 def dg_k_grouped_bf16_wgrad(a, b, d, c, ks_host, ks_dev, stream=None):
@@ -179,7 +202,7 @@ def dg_k_grouped_bf16_wgrad(a, b, d, c, ks_host, ks_dev, stream=None):
         raise ValueError("ks must have G entries")
     _check(lib().dg_k_grouped_bf16_wgrad(
         _dptr(a), _dptr(b), _dptr(d), DG_BF16 if d.dtype == torch.bfloat16 else DG_F32,
-        _dptr(c), G, M, N, a.shape[0], kh, _dptr(ks_dev), _stream(stream)))
+        _dptr(c), G, M, N, a.shape[0], kh, _dptr(ks_dev), _stream(stream, d)))
 
 
 def dg_m_grouped_fp8_dgrad(a, sfa, w, sfw, d, ms_host, ms_dev, gran_k: int = 128,

@@ -4,6 +4,7 @@
 // from a memory pool this library owns (returned to the pool on the same
 // stream once the GEMM is queued; the pool keeps it for the next call).
 #include <algorithm>
+#include <cstddef>
 #include <cstdarg>
 #include <cstdio>
 #include <cstdlib>
@@ -243,8 +244,10 @@ dg_status grouped_validate(const GroupedArgs &x) {
 
 void grouped_schedule(const GroupedArgs &x, int sms, WgradParams &p, PackParams &pk,
                       GroupedPlan &g) {
-  std::memset(&p, 0, sizeof(p));
-  std::memset(&pk, 0, sizeof(pk));
+  // Clear everything but the per-entry tables; the entries in use are written
+  // below and the kernels and the pack pass read no others.
+  std::memset(&p, 0, offsetof(WgradParams, sched));
+  std::memset(&pk, 0, offsetof(PackParams, g_off));
   // FP8 with N not a multiple of 224 but M one (the down-projection's 7168 x
   // 2048): compute D^T tiles instead, so that the 224-wide tile runs along M
   // with no ragged edge and the 256-row side along N.
@@ -450,10 +453,11 @@ dg_status run_grouped(const GroupedArgs &x) {
   if ((s = device_state(&dev)) != DG_OK) return s;
 
   // ---- schedule: longest entries first, then output-only (fill) experts
-  std::unique_ptr<dg::WgradParams> hold(new dg::WgradParams);   // ~29 KB: off the stack
-  std::unique_ptr<dg::PackParams> pk_hold(new dg::PackParams);  // ~12 KB
-  dg::WgradParams &p = *hold;
-  dg::PackParams &pk = *pk_hold;
+  // ~29 KB and ~12 KB: per-thread storage rather than the stack or the heap
+  static thread_local dg::WgradParams t_p;
+  static thread_local dg::PackParams t_pk;
+  dg::WgradParams &p = t_p;
+  dg::PackParams &pk = t_pk;
   dg::GroupedPlan g{};
   dg::grouped_schedule(x, dev->sms, p, pk, g);
   p.wait_limit_ns = wait_limit_ns();
