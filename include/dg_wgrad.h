@@ -39,10 +39,16 @@
  *  - DG_LOG=1 in the environment makes each GEMM call print its plan (tile
  *    orientation and width, tiles, entries split along K, output mode) to
  *    stderr.
- *  - Device-side waits are bounded (default 4 s, environment variable
- *    DG_WAIT_LIMIT_MS).  A wait that runs out makes the kernel stop early and
- *    record DG_ERR_TIMEOUT in the device status word, which dg_sync_check()
- *    reports; the output is then unspecified.
+ *  - Device-side waits are bounded (default 4 s; environment variable
+ *    DG_WAIT_LIMIT_US, else DG_WAIT_LIMIT_MS, read at each call).  A wait that
+ *    runs out makes the kernel stop early and record DG_ERR_TIMEOUT in the
+ *    device status word, which dg_sync_check() reports; the output is then
+ *    unspecified.  Waits for copies already in flight, on the way out, keep a
+ *    limit of at least 2 s so that no copy outlives the kernel.
+ *  - DG_DETERMINISTIC=1 in the environment (read at each call) keeps every
+ *    expert of an in-place FP8 or BF16 GEMM in one piece (no split along K;
+ *    see c under dg_k_grouped_fp8_wgrad), making in-place results bitwise
+ *    reproducible at some cost in balance.
  */
 #ifndef DG_WGRAD_H
 #define DG_WGRAD_H
@@ -98,8 +104,8 @@ typedef enum {
  *           Only with d_dtype == DG_F32.  In place, an expert much longer than
  *           the others is split along K into parts that each add into D, so
  *           the order of the FP32 additions (and the last bits of D) may vary
- *           from run to run; every other mode writes each element once and is
- *           bitwise reproducible.
+ *           from run to run (unless DG_DETERMINISTIC is set); every other mode
+ *           writes each element once and is bitwise reproducible.
  *   G       number of experts, 0 <= G <= DG_MAX_GROUPS.
  *   M, N    positive multiples of 16.
  *   sum_k   total tokens; must equal ks_host[0] + ... + ks_host[G-1].
@@ -116,9 +122,14 @@ typedef enum {
  * group of four scale rows (four 128-token blocks at gran_k 128, the four
  * 32-token blocks of one 128-token block at gran_k 32) of each expert into
  * 512-byte records laid out as the tensor core reads scales, so the GEMM loads
- * them with TMA.  Scratch: (scale groups) x (2 * ceil(M / 256) +
- * ceil(N / BN) * ceil(BN / 128)) x 512 bytes, BN = 224 if N % 224 == 0 else
- * 128 -- about 3.9 MB for G = 32, M = 4096, N = 7168, sum_k = 32768.
+ * them with TMA.  Scratch: (scale groups) x (2 * ceil(M' / 256) +
+ * ceil(N' / BN) * ceil(BN / 128)) x 512 bytes, where (M', N') = (N, M) when
+ * N % 224 != 0 and M % 224 == 0 (the kernel then computes tiles of D^T) and
+ * (M, N) otherwise, BN = 224 if N' % 224 == 0 else 128, and the scale groups
+ * are ceil(K_e / 512) per expert at gran_k 128 and K_e / 128 at gran_k 32
+ * (about four times as many; an in-place expert split along K counts each
+ * part's groups) -- about 3.9 MB for G = 32, M = 4096, N = 7168,
+ * sum_k = 32768 at gran_k 128.
  * Errors: DG_ERR_INVALID_ARG for any violated condition above (including
  * NULL pointers where data is needed and misaligned pointers),
  * DG_ERR_UNSUPPORTED off sm_103, DG_ERR_CUDA on a failed launch or scratch
@@ -418,22 +429,26 @@ dg_status dg_swiglu_backward_quant_fp8(const void *h, const void *da,
  * caching allocator, or that must not take the device synchronisation
  * cudaMalloc can cause, cannot accept that.  This entry point computes exactly
  * what dg_k_grouped_fp8_wgrad computes, with the same arguments and errors,
- * and allocates nothing: the status record and the packed scale records live
- * in one file-scope device array of the library, 256 bytes + 32 MiB (every GPU
- * that loads this part of the library holds it until the process exits).
+ * by the same host steps (validation, schedule with its tile orientation and
+ * split along K, tensor maps, scale packing, launch), and allocates nothing:
+ * the status record and the packed scale records live in one file-scope
+ * device array of the library, 256 bytes + 32 MiB (every GPU that loads this
+ * part of the library holds it until the process exits).
  *  - The first call on a device does the set-up (device queries, the
  *    array's device address via cudaGetSymbolAddress); make that first call
  *    before any stream capture.
  *  - Each call clears the record and rewrites the scale records on `stream`
  *    before its GEMM; calls that overlap on the GPU (on different streams)
  *    share the array and race on it.
- *  - It never synchronises, so device-side timeouts and ks_dev mismatches are
- *    not reported (waits stay bounded: the kernel ends early, D unspecified).
+ *  - It never synchronises.  dg_sync_check() reads and clears this entry
+ *    point's record as well as the ordinary one, so device-side timeouts and
+ *    ks_dev mismatches are reported there.
  *  - Limits: the packed scale records must fit 32 MiB (their size is given
  *    under dg_k_grouped_fp8_wgrad; G = 64, M = 4096, N = 7168,
- *    sum_k = 131072 needs 14 MB); larger problems, and sizes above the
- *    kernel's own limits (G > DG_MAX_GROUPS, sum_k >= 2^31 - 256), are
- *    rejected with DG_ERR_UNSUPPORTED and a message.
+ *    sum_k = 131072 needs 14 MB at gran_k 128 and about four times that,
+ *    above the limit, at gran_k 32); larger problems, and sizes above the kernel's own limits
+ *    (G > DG_MAX_GROUPS, sum_k > 2^31 - 256), are rejected with
+ *    DG_ERR_UNSUPPORTED and a message before any CUDA call.
  */
 dg_status dg_k_grouped_fp8_wgrad_noalloc(const void *a, const uint8_t *sfa,
                                          const void *b, const uint8_t *sfb,
@@ -446,8 +461,10 @@ dg_status dg_k_grouped_fp8_wgrad_noalloc(const void *a, const uint8_t *sfa,
 const char *dg_last_error(void);
 
 /*
- * Synchronise `stream`, then read and clear the current device's status word.
- * Returns DG_ERR_TIMEOUT if a kernel gave up on a bounded wait,
+ * Synchronise `stream`, then read and clear the current device's status words
+ * (the ordinary entry points' record and dg_k_grouped_fp8_wgrad_noalloc's).
+ * Allocates nothing.  Returns DG_ERR_TIMEOUT if a kernel gave up on a bounded
+ * wait,
  * DG_ERR_INVALID_ARG if a kernel found ks_dev different from ks_host, a
  * src_rows entry or a topk_idx entry out of range,
  * DG_ERR_CUDA if the synchronisation failed, else DG_OK.
