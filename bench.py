@@ -85,6 +85,17 @@ def kernel_source_sha() -> str:
     return h.hexdigest()[:16]
 
 
+def fp8_tiles(M: int, N: int) -> str:
+    """Tile widths of the token-major FP8 weight gradient for an M x N output:
+    the kernel's N is N, or M when its tiles are transposed (N % 224 != 0 and
+    M % 224 == 0); a kernel N that is a multiple of 1792 (of 256 and of 224)
+    runs mixed 256 / 224-column tiles unless DG_MIXED_TILES=0."""
+    nk = M if (N % 224 and M % 224 == 0) else N
+    if nk % 1792 == 0 and os.environ.get("DG_MIXED_TILES", "") != "0":
+        return "256 | 224 mixed"
+    return "224" if nk % 224 == 0 else "128"
+
+
 def recorded_traffic(kernel: str, workload: str):
     """Per-launch DRAM bytes for (kernel, workload) from the committed ncu
     summary, or None if absent or taken on a different kernel source."""
@@ -434,7 +445,7 @@ def measure_inplace(w, dev, pk, fp8_peak, steps, warmup=5):
 
         def step():
             dg.dg_k_grouped_fp8_wgrad(qa, sa, qb, sb, d, d, ks, ks_dev, 128)
-        kname = "kgrouped_wgrad_kernel<fp8, 224, f32 reduce>"
+        kname = f"kgrouped_wgrad_kernel<fp8, {fp8_tiles(w.M, w.N)}, f32 reduce>"
         peak_t, peak_name = fp8_peak["tflops"], fp8_peak["source"]
     for _ in range(warmup):
         step()
@@ -502,8 +513,8 @@ def measure_fp8_config(name, dev, pk, fp8_peak, steps):
     del qa, sa, qb, sb, d
     torch.cuda.empty_cache()
     return {"workload": name, "ms": ms, "value": tf, "unit": "TFLOP/s", "steps": steps,
-            "kernel": "kgrouped_wgrad_kernel<fp8, 224, bf16, transposed tiles>"
-                      if w.out_dtype == "bf16" else "kgrouped_wgrad_kernel<fp8, 224, f32>",
+            "kernel": f"kgrouped_wgrad_kernel<fp8, {fp8_tiles(w.M, w.N)}, "
+                      + ("bf16, transposed tiles>" if w.out_dtype == "bf16" else "f32>"),
             "launches_per_step": 2,
             "roofline": {"bound": "tensor", "achieved": tf, "peak": fp8_peak["tflops"],
                          "unit": "TFLOP/s", "frac": tf / fp8_peak["tflops"],
@@ -704,7 +715,8 @@ def run_ours(args):
     else:
         roof = {"bound": "tensor", "achieved": tflops, "peak": fp8_peak, "unit": "TFLOP/s",
                 "frac": tflops / fp8_peak, "traffic": traffic}
-    roof.update({"kernel": "kgrouped_wgrad_kernel<fp8, 224, f32>", "peak_source": pk_kind,
+    roof.update({"kernel": f"kgrouped_wgrad_kernel<fp8, {fp8_tiles(w.M, w.N)}, f32>",
+                 "peak_source": pk_kind,
                  "algorithmic_bytes": alg, "tensor_tflops": tflops,
                  "tensor_peak_tflops": fp8_peak, "tensor_frac": tflops / fp8_peak,
                  "attainable_frac": max(t_hbm, t_tc) / (ms * 1e-3),

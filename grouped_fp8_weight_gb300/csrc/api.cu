@@ -106,13 +106,11 @@ dg_status device_state(DeviceState **out) {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// DG_LOG=1 in the environment: each GEMM call prints its plan to stderr.
+// DG_LOG=1 in the environment (read at each call): each GEMM call prints its
+// plan to stderr.
 bool log_enabled() {
-  static const bool on = [] {
-    const char *v = std::getenv("DG_LOG");
-    return v != nullptr && *v != '\0' && *v != '0';
-  }();
-  return on;
+  const char *v = std::getenv("DG_LOG");
+  return v != nullptr && *v != '\0' && *v != '0';
 }
 
 dg_status encode(CUtensorMap *m, CUtensorMapDataType dt, const void *ptr, int rank,
@@ -188,6 +186,17 @@ uint64_t wait_limit_ns() {
 bool deterministic_requested() {
   const char *v = std::getenv("DG_DETERMINISTIC");
   return v != nullptr && *v != '\0' && *v != '0';
+}
+
+// DG_MIXED_TILES in the environment (read at each call): 0 keeps every FP8
+// tile 224 columns wide; a positive number is the percentage of the narrow
+// tiles' count that the wide tiles' lane-0 turns may reach (default 100; see
+// grouped_schedule).
+static int mixed_tiles_percent() {
+  const char *v = std::getenv("DG_MIXED_TILES");
+  if (v == nullptr || *v == '\0') return 100;
+  const int pct = std::atoi(v);
+  return pct < 0 ? 0 : pct;
 }
 
 dg_status grouped_validate(const GroupedArgs &x) {
@@ -350,6 +359,38 @@ void grouped_schedule(const GroupedArgs &x, int sms, WgradParams &p, PackParams 
                : (x.c == x.d)         ? OUT_F32_REDUCE
                                       : OUT_F32_C;
   p.ks_dev = x.ks_dev;
+  // Mixed tile widths (FP8, token-major operands, kernel N a multiple of both
+  // 256 and 224): the longest entries are cut into 256-column tiles, which
+  // load 12.5 % fewer operand bytes per multiply-add than 224-column ones
+  // (B's 128-byte rows fill whole 32-byte sectors).  Only the first
+  // accumulator holds 256 columns, so only lane 0 takes wide tiles, and each
+  // of its turns on them pairs with a narrow tile of lane 1: entries become
+  // wide, longest first, while the narrow tiles left still cover the lane-0
+  // turns that the wide ones take.
+  const int mix_pct = mixed_tiles_percent();
+  if (x.fp8 && !x.kmajor && bn == kNarrowBN && Nk % kWideBN == 0 && g.n_mma > 0 && mix_pct > 0) {
+    const int ntw = Nk / kWideBN;
+    const int64_t tpg_w = static_cast<int64_t>(p.m_tiles) * ntw;
+    int64_t narrow = static_cast<int64_t>(n) * tpg;   // narrow tiles with no wide entry
+    int64_t turns = 0;                                // lane-0 turns of the wide tiles
+    int nw = 0;
+    for (; nw < g.n_mma; ++nw) {
+      const int64_t nk = (ents[nw].k_len + 127) / 128;
+      const int64_t t = tpg_w * ((nk + p.chunk - 1) / p.chunk);
+      if ((turns + t) * 100 > (narrow - tpg) * mix_pct) break;
+      turns += t;
+      narrow -= tpg;
+    }
+    if (nw > 0) {
+      g.bn = kWideBN;
+      p.n_wide = nw;
+      p.n_tiles_w = ntw;
+      p.tpg_w = static_cast<int>(tpg_w);
+      p.wide_tiles = static_cast<int>(nw * tpg_w);
+      p.num_mma_tiles = p.wide_tiles + (g.n_mma - nw) * tpg;
+      p.num_tiles = p.wide_tiles + (n - nw) * tpg;
+    }
+  }
   g.sf_bytes = (x.fp8 && g.n_mma > 0) ? plan_scale_pack(p, pk, g.n_mma, x.gran_k, bn) : 0;
   set_derived(p, n);
 }
@@ -377,11 +418,17 @@ dg_status grouped_maps(const GroupedArgs &x, const GroupedPlan &g, WgradParams &
       const uint64_t da[2] = {MK, SK}, sa[1] = {MK};
       const uint64_t db[2] = {NK, SK}, sb[1] = {NK};
       const uint32_t box[2] = {128, 128};
-      // B: one box per CTA covers its bn / 2 columns (<= one 128-byte atom)
+      // B: one box per CTA covers its bn / 2 columns (<= one 128-byte atom);
+      // mixed widths: tmB for the wide tiles, tmBn for the narrow ones
       const uint32_t boxb[2] = {static_cast<uint32_t>(std::min(128, bn / 2)), 128};
+      const uint32_t boxn[2] = {static_cast<uint32_t>(kNarrowBN / 2), 128};
       if ((s = encode(&p.tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, ka, 2, da, sa, box,
                       CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "a")) ||
           (s = encode(&p.tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, kb, 2, db, sb, boxb,
+                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "b")))
+        return s;
+      if (bn == kWideBN &&
+          (s = encode(&p.tmBn, CU_TENSOR_MAP_DATA_TYPE_UINT8, kb, 2, db, sb, boxn,
                       CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "b")))
         return s;
     } else {
@@ -417,7 +464,8 @@ dg_status grouped_scale_maps(const GroupedArgs &x, const GroupedPlan &g, void *s
   bind_scale_pack(pk, scratch, g.ksfa, g.ksfb);
   const uint64_t rec[1] = {512};
   const uint64_t dpa[2] = {128, static_cast<uint64_t>(pk.n_groups) * pk.MC};
-  const uint64_t dpb[2] = {128, static_cast<uint64_t>(pk.n_groups) * pk.NT * pk.CB};
+  const uint64_t dpb[2] = {128, (static_cast<uint64_t>(pk.GW) * pk.NTW +
+                                static_cast<uint64_t>(pk.n_groups - pk.GW) * pk.NT) * pk.CB};
   const uint32_t bpa[2] = {128, 1}, bpb[2] = {128, static_cast<uint32_t>(pk.CB)};
   dg_status s;
   if ((s = encode(&p.tmSFA, CU_TENSOR_MAP_DATA_TYPE_UINT32, pk.sfa_p, 2, dpa, rec, bpa,
@@ -473,11 +521,13 @@ dg_status run_grouped(const GroupedArgs &x) {
     }
     std::fprintf(stderr,
                  "[dg] %s: G=%d M=%d N=%d sum_k=%lld (%d empty, max K %d) | %s operands, %s tiles "
-                 "256 x %d, %d x %d per expert | %d GEMM entries (+%d from splits along K), "
+                 "256 x %d, %d x %d per expert (%d entries of 256 x 256 tiles, %d x %d) | "
+                 "%d GEMM entries (+%d from splits along K), "
                  "%d GEMM tiles + %d output-only | out=%s | pairs=%d\n",
                  fn, x.G, x.M, x.N, static_cast<long long>(x.sum_k), empty, max_k,
-                 x.kmajor ? "K-major" : "token-major", g.trans ? "transposed" : "direct", g.bn,
-                 p.m_tiles, p.n_tiles, g.n_mma, g.n_mma - (x.G - empty), p.num_mma_tiles,
+                 x.kmajor ? "K-major" : "token-major", g.trans ? "transposed" : "direct",
+                 g.bn == dg::kWideBN ? dg::kNarrowBN : g.bn, p.m_tiles, p.n_tiles, p.n_wide,
+                 p.m_tiles, p.n_tiles_w, g.n_mma, g.n_mma - (x.G - empty), p.num_mma_tiles,
                  p.num_tiles - p.num_mma_tiles,
                  p.out_mode == dg::OUT_BF16        ? "bf16"
                  : p.out_mode == dg::OUT_F32       ? "f32"

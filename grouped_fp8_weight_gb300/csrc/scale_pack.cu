@@ -11,7 +11,10 @@
 // Records:
 //   SFA_p[gp][mc]      : rows m = 128 mc + 32 q + l of A's scales, mc < MC
 //   SFB_p[gp][nt][c]   : columns n = nt * BN + 128 c + 32 q + l of B's scales,
-//                        c < CB; columns outside the tile or past N are 0
+//                        c < CB; columns outside the tile or past N are 0.
+//                        With mixed tile widths the first GW groups (those of
+//                        the wide entries) have NTW tiles of BNW columns and
+//                        come first; the others follow with NT tiles of BN.
 // where gp runs over the scale groups of all experts with K_e > 0 in schedule
 // order: group j of schedule entry s is gp = g_off[s] + j and covers scale
 // rows k_off[s] / gran_k + 4j .. + 3 (rows past the expert's end are 0).
@@ -39,6 +42,9 @@ __global__ void __launch_bounds__(128) pack_scales_kernel(const __grid_constant_
   const int l = t >> 2, q = t & 3;
   const int col_in = 32 * q + l;       // column within a 128-column chunk
   const int r = blockIdx.y;            // record of this group: A chunks, then B (tile, chunk)
+  const bool wide = gp < p.GW;
+  const int NT = wide ? p.NTW : p.NT, BN = wide ? p.BNW : p.BN;
+  if (r >= p.MC + NT * p.CB) return;   // the grid covers the larger tile count
   uint32_t w = 0;
   if (r < p.MC) {
     const int m = 128 * r + col_in;
@@ -50,11 +56,14 @@ __global__ void __launch_bounds__(128) pack_scales_kernel(const __grid_constant_
     const int rb = r - p.MC;           // nt * CB + c
     const int nt = rb / p.CB, c = rb - nt * p.CB;
     const int nn = 128 * c + col_in;
-    const int n = nt * p.BN + nn;
-    if (nn < p.BN && n < p.N)
+    const int n = nt * BN + nn;
+    if (nn < BN && n < p.N)
       for (int i = 0; i < rows; ++i)
         w |= static_cast<uint32_t>(p.sfb[(row0 + i) * p.N + n]) << (8 * i);
-    p.sfb_p[(static_cast<int64_t>(gp) * p.NT * p.CB + rb) * 128 + t] = w;
+    const int64_t rec = wide ? static_cast<int64_t>(gp) * p.NTW * p.CB + rb
+                             : static_cast<int64_t>(p.GW) * p.NTW * p.CB +
+                                   static_cast<int64_t>(gp - p.GW) * p.NT * p.CB + rb;
+    p.sfb_p[rec * 128 + t] = w;
   }
 }
 
@@ -84,8 +93,9 @@ cudaError_t launch_pack_token_scales(const TokenPackParams &p, cudaStream_t stre
 
 size_t plan_scale_pack(WgradParams &p, PackParams &pk, int n_mma, int gran_k, int bn) {
   const int gs = (gran_k == 128) ? 4 : 1;   // k-blocks per scale group
-  int gp = 0;
+  int gp = 0, gw = 0;
   for (int i = 0; i < n_mma; ++i) {
+    if (i == p.n_wide) gw = gp;   // the wide entries' groups end here
     const int kb = p.sched[i].k_len / 128;
     const int rows_per_kb = 128 / gran_k;
     p.sched[i].g_off = gp;
@@ -94,16 +104,22 @@ size_t plan_scale_pack(WgradParams &p, PackParams &pk, int n_mma, int gran_k, in
     pk.row_end[i] = pk.row_off[i] + kb * rows_per_kb;
     gp += (kb + gs - 1) / gs;
   }
+  if (p.n_wide >= n_mma) gw = gp;
   pk.M = p.M;
   pk.N = p.N;
   pk.MC = 2 * p.m_tiles;
   pk.NT = p.n_tiles;
   pk.CB = (bn + 127) / 128;
   pk.BN = bn;
+  pk.GW = p.n_wide > 0 ? gw : 0;
+  pk.NTW = p.n_wide > 0 ? p.n_tiles_w : 0;
+  pk.BNW = p.n_wide > 0 ? kWideBN : 0;
   pk.n_entries = n_mma;
   pk.n_groups = gp;
   p.sf_mc = pk.MC;
-  return static_cast<size_t>(gp) * (pk.MC + static_cast<size_t>(pk.NT) * pk.CB) * 512;
+  p.sf_gw = pk.GW;
+  return (static_cast<size_t>(gp) * pk.MC + static_cast<size_t>(pk.GW) * pk.NTW * pk.CB +
+          static_cast<size_t>(gp - pk.GW) * pk.NT * pk.CB) * 512;
 }
 
 void bind_scale_pack(PackParams &pk, void *scratch, const uint8_t *sfa, const uint8_t *sfb) {
@@ -115,7 +131,7 @@ void bind_scale_pack(PackParams &pk, void *scratch, const uint8_t *sfa, const ui
 
 cudaError_t launch_pack_scales(const PackParams &p, cudaStream_t stream) {
   if (p.n_groups <= 0) return cudaSuccess;
-  const dim3 grid(p.n_groups, p.MC + p.NT * p.CB);
+  const dim3 grid(p.n_groups, p.MC + (p.NTW > p.NT ? p.NTW : p.NT) * p.CB);
   pack_scales_kernel<<<grid, 128, 0, stream>>>(p);
   return cudaGetLastError();
 }

@@ -60,6 +60,8 @@
 
 #include <cuda_bf16.h>
 
+#include <type_traits>
+
 // The MMA issuer runs as a whole warp with warp-uniform control flow; one
 // lane, elected once, issues every tcgen05 instruction, and every wait result
 // is made warp-uniform (a single thread issuing from divergent code kept the
@@ -90,6 +92,14 @@ struct WgradCfg {
   static constexpr int THREADS = 32 * (3 + EPI_WARPS);
   static_assert(!kKMajor || kFP8, "K-major operands: FP8 only");
   static_assert(!kMG || kFP8, "M-grouped: FP8");
+  // Mixed tile widths (FP8 weight gradient, token-major operands, block_n
+  // 256): the first accumulator is 256 columns wide and takes the wide tiles
+  // (the longest experts) and narrow ones; the second is BN1 = 224 wide and
+  // takes narrow tiles only.  256 + 224 columns leave room for two scale
+  // slots in tensor memory.
+  static constexpr bool kMixed = kFP8 && !kMG && !kKMajor && kBN == kWideBN;
+  static_assert(!(kFP8 && kBN == kWideBN) || kMixed, "FP8 block_n 256: mixed widths only");
+  static constexpr int BN1 = kMixed ? kNarrowBN : kBN;   // second accumulator's width
   // Operand majorness: kKMajor makes both operands K-major (NT weight
   // gradient; the data gradient with the weight stored [N, K]); the M-grouped
   // data gradient otherwise has a K-major A (token rows of dy) and an
@@ -119,6 +129,7 @@ struct WgradCfg {
   // (its 128-byte swizzled rows keep their 128-byte pitch in shared memory).
   static constexpr int B_BOX_COLS = BN_CTA < ATOM ? BN_CTA : ATOM;
   static constexpr int B_LOAD_BYTES = B_KM ? B_BYTES : B_ATOMS * BK * B_BOX_COLS * ELEM;
+  static constexpr int B_LOAD_BYTES_N = kMixed ? BK * (BN1 / 2) * ELEM : B_LOAD_BYTES;   // narrow tiles
   // Descriptor start-address step of one MMA along K: MN-major, MMA_K token
   // rows of 128 bytes; K-major, MMA_K elements inside the 128-byte row.
   static constexpr int A_KSTEP = A_KM ? MMA_K * ELEM : MMA_K * 128;
@@ -139,12 +150,20 @@ struct WgradCfg {
   static constexpr int UT_A = 512;                      // 32 rows x 16 bytes
   static constexpr int UT_B = 512 * SF_CHUNKS_B;
   static constexpr int SF_COLS = 4 + 4 * SF_CHUNKS_B;   // tensor-memory columns per slot
-  static constexpr int SF_COL0 = NUM_ACC * kBN;
+  static constexpr int SF_COL0 = kBN + BN1;              // after the two accumulators
+  // Tensor-memory scale slots, a ring of SF_TSLOTS (two with mixed widths,
+  // whose accumulators leave room for no more).  The copy of a group's scales
+  // into a slot waits until the MMAs of the group that last read the slot
+  // have completed: the tensor pipe orders a copy before later MMAs, but not
+  // after earlier ones.
+  static constexpr int SF_TSLOTS = kMixed ? 2 : SF_SLOTS;
+  static constexpr int SF_TSLOTS_MAX = 5;
+  static_assert(SF_TSLOTS <= SF_TSLOTS_MAX, "scale-slot barriers");
   static constexpr int EC = kEpiCols;                   // output columns per epilogue chunk
   static constexpr int WSTG_BYTES = 32 * EC * 4;        // per epilogue warp and buffer: 32 FP32 rows
   static constexpr int EPI_BUFS = 8 / EPI_WARPS;        // staging buffers per epilogue warp
   static constexpr int TMEM_COLS = 512;
-  static_assert(SF_COL0 + SF_SLOTS * SF_COLS <= TMEM_COLS, "tmem budget");
+  static_assert(SF_COL0 + SF_TSLOTS * SF_COLS <= TMEM_COLS, "tmem budget");
   static_assert(kBN % 32 == 0 && kBN <= 256, "block N");
 
   static constexpr int OFF_B = 0;
@@ -155,8 +174,8 @@ struct WgradCfg {
   static constexpr int OFF_UTB = OFF_UTA + SF_SLOTS * UT_A;
   static constexpr int OFF_BAR = (OFF_UTB + SF_SLOTS * UT_B + 7) / 8 * 8;
   // barriers: full[S], empty[S], gate[S], tfull[S], accf[2], acce[2],
-  // cbar[4 warps x 2], sfr/sfe[SLOTS], drain
-  static constexpr int NUM_BARS = 4 * STAGES + 2 * NUM_ACC + 8 + 2 * SF_SLOTS + 1;
+  // cbar[4 warps x 2], sfr/sfe[SLOTS], drain, sfd[TSLOTS_MAX]
+  static constexpr int NUM_BARS = 4 * STAGES + 2 * NUM_ACC + 8 + 2 * SF_SLOTS + 1 + SF_TSLOTS_MAX;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   // The schedule table is read once per chunk by every role; indexed reads
   // of the kernel parameters miss the constant cache, so it is copied here
@@ -172,7 +191,7 @@ struct WgradCfg {
 
 // Roles' wait sites, reported in DevStatus::where.
 enum : int { W_PROD_EMPTY = 0x01, W_PROD_DRAIN = 0x02, W_PROD_SFE = 0x03, W_MMA_ACCE = 0x11,
-             W_MMA_FULL = 0x12, W_MMA_DRAIN = 0x13, W_MMA_SFR = 0x14, W_EPI_ACCF = 0x21,
+             W_MMA_FULL = 0x12, W_MMA_DRAIN = 0x13, W_MMA_SFR = 0x14, W_MMA_SFD = 0x15, W_EPI_ACCF = 0x21,
              W_EPI_C = 0x22, W_SF_FULL = 0x31 };
 
 struct TileCoord {
@@ -181,10 +200,13 @@ struct TileCoord {
   int ka_off;                         // A's offset along K (k_off, or 0 when M-grouped)
   int rows;                           // M-grouped: this CTA's rows inside the expert (<= 0: none)
   int k_exp;                          // the entry's k_exp (checked against ks_dev)
+  int bn;                             // the tile's width
 };
 
 // Weight gradient: entry u / tiles_per_group, tiles (M tile, N tile) of the
-// expert's [M, N] output.  M-grouped data gradient: the entry whose tile_off
+// expert's [M, N] output; with mixed widths the first wide_tiles tiles are the
+// wide entries' (kWideBN columns, tpg_w per entry) and the rest follow with
+// width bn.  M-grouped data gradient: the entry whose tile_off
 // range holds u; its tiles are (256-token chunk, N tile) of the expert's rows,
 // N tiles fastest, and A's rows are the tokens (m0 is a row of the [sum_m, K]
 // operand), B's rows the expert's K rows of W.
@@ -204,18 +226,32 @@ __device__ __forceinline__ TileCoord tile_coord(const WgradParams &p, const Sche
     const int r0 = mt * 256 + static_cast<int>(rank) * 128;
     c.expert = se.expert; c.k_off = se.k_off; c.k_len = se.k_len;
     c.m0 = se.row_off + r0; c.n0 = nt * bn; c.mt = mt; c.nt = nt; c.g_off = se.g_off;
-    c.ka_off = 0; c.rows = se.k_exp - r0; c.k_exp = se.k_exp;
+    c.ka_off = 0; c.rows = se.k_exp - r0; c.k_exp = se.k_exp; c.bn = bn;
   } else {
-    const int gi = fast_div(u, p.div_tpg);
-    const int lt = u - gi * p.tiles_per_group;
+    int gi, lt, ntn;
+    FastDiv dnt;
+    if (u < p.wide_tiles) {
+      gi = fast_div(u, p.div_tpg_w);
+      lt = u - gi * p.tpg_w;
+      ntn = p.n_tiles_w;
+      dnt = p.div_nt_w;
+      bn = kWideBN;
+    } else {
+      const int v = u - p.wide_tiles;
+      const int gq = fast_div(v, p.div_tpg);
+      gi = p.n_wide + gq;
+      lt = v - gq * p.tiles_per_group;
+      ntn = p.n_tiles;
+      dnt = p.div_nt;
+    }
     const SchedEntry se = sched[gi];
-    const int q = fast_div(lt, p.m_fastest ? p.div_mt : p.div_nt);
-    const int r = lt - q * (p.m_fastest ? p.m_tiles : p.n_tiles);
+    const int q = fast_div(lt, p.m_fastest ? p.div_mt : dnt);
+    const int r = lt - q * (p.m_fastest ? p.m_tiles : ntn);
     const int mt = p.m_fastest ? r : q;
     const int nt = p.m_fastest ? q : r;
     c.expert = se.expert; c.k_off = se.k_off; c.k_len = se.k_len;
     c.m0 = mt * 256 + static_cast<int>(rank) * 128; c.n0 = nt * bn; c.mt = mt; c.nt = nt;
-    c.g_off = se.g_off; c.ka_off = se.k_off; c.rows = 128; c.k_exp = se.k_exp;
+    c.g_off = se.g_off; c.ka_off = se.k_off; c.rows = 128; c.k_exp = se.k_exp; c.bn = bn;
   }
   return c;
 }
@@ -303,8 +339,15 @@ __device__ __forceinline__ bool lane_turn(LaneSched &L, const WgradParams &p, in
     // in order, so the running tiles share one expert's weight in L2.
     const int i = (l == 0 || p.mgroup) ? L.head++ : L.tail--;
     u = owned_tile(i, pid, R);
+    if (l == 1 && u < p.wide_tiles) {   // a wide tile does not fit the second accumulator
+      ++L.tail;
+      u = -1;
+      return false;
+    }
     // (M-grouped: every entry's K is the same, sched[0].k_len)
-    const int kl = p.mgroup ? L.sched[0].k_len : L.sched[fast_div(u, p.div_tpg)].k_len;
+    const int ei = u < p.wide_tiles ? fast_div(u, p.div_tpg_w)
+                                    : p.n_wide + fast_div(u - p.wide_tiles, p.div_tpg);
+    const int kl = p.mgroup ? L.sched[0].k_len : L.sched[ei].k_len;
     nk = (u < p.num_mma_tiles) ? (kl + bk - 1) / bk : 0;
     j = 0;
     if (nk == 0) {   // output-only tile: a completion without MMAs
@@ -375,6 +418,7 @@ __global__ void __launch_bounds__((WgradCfg<kFP8, kBN, kKMajor, kMG, kTransD>::T
   uint64_t *sfr = cbar + 8;        // even CTA: both CTAs' records of a scale group landed
   uint64_t *sfe = sfr + NS;        // scale slot free (its tcgen05.cp completed)
   uint64_t *drain = sfe + NS;
+  uint64_t *sfd = drain + 1;       // even CTA: MMAs of the scale group in tensor-memory slot i completed
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Cfg::OFF_MISC);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + Cfg::OFF_MISC + 4);
 
@@ -411,6 +455,7 @@ __global__ void __launch_bounds__((WgradCfg<kFP8, kBN, kKMajor, kMG, kTransD>::T
       mbar_init(&sfe[i], 1);
     }
     mbar_init(drain, 1);
+    for (int i = 0; i < Cfg::SF_TSLOTS_MAX; ++i) mbar_init(&sfd[i], 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -437,7 +482,7 @@ __global__ void __launch_bounds__((WgradCfg<kFP8, kBN, kKMajor, kMG, kTransD>::T
     if (lane == 0) {
       prefetch_tmap(&p.tmA);
       prefetch_tmap(&p.tmB);
-      const uint32_t tx = 2 * (Cfg::A_BYTES + Cfg::B_LOAD_BYTES);   // both CTAs' bytes
+      if constexpr (Cfg::kMixed) prefetch_tmap(&p.tmBn);
       const uint64_t keep = l2_policy_evict_last();   // operands are re-read by other tiles
       int s = 0;
       uint32_t ph = 0, armed = 0;
@@ -447,12 +492,16 @@ __global__ void __launch_bounds__((WgradCfg<kFP8, kBN, kKMajor, kMG, kTransD>::T
       Chunk ch;
       while (ok && lane_next(L, p, pid, R, Cfg::BK, ch)) {
         if (ch.nk == 0) continue;
-        const TileCoord tc = tile_coord<kMG>(p, sched, ch.u, kBN, rank);
+        const TileCoord tc = tile_coord<kMG>(p, sched, ch.u, Cfg::BN1, rank);
         const int t = ch.u;
+        // both CTAs' bytes of a stage; a narrow tile's B boxes (mixed widths)
+        const bool narrow = Cfg::kMixed && tc.bn != kBN;
+        const uint32_t tx = 2 * (Cfg::A_BYTES + (narrow ? Cfg::B_LOAD_BYTES_N : Cfg::B_LOAD_BYTES));
+        const CUtensorMap *tmb = narrow ? &p.tmBn : &p.tmB;
         if (leader && ch.j0 == 0 && p.ks_dev != nullptr && tc.mt == 0 && tc.nt == 0 &&
             p.ks_dev[tc.expert] != tc.k_exp)
           atomicCAS(&p.status->code, DEV_OK, DEV_KS_MISMATCH);
-        const int nb = tc.n0 + static_cast<int>(rank) * Cfg::BN_CTA;   // this CTA's B columns
+        const int nb = tc.n0 + static_cast<int>(rank) * (tc.bn / 2);   // this CTA's B columns
         const KRot rot = tile_rot(tc.mt, tc.nt, ch.nk, Cfg::ROT_UNIT);
         for (int j = ch.j0; j < ch.j1; ++j) {
           const int jj = rot_stage(j, rot);   // stage of the tile's k range at position j
@@ -500,8 +549,7 @@ __global__ void __launch_bounds__((WgradCfg<kFP8, kBN, kKMajor, kMG, kTransD>::T
             } else {
 #pragma unroll
               for (int b = 0; b < Cfg::B_ATOMS; ++b)
-                tma_load_2d_pair(sb + b * Cfg::ATOM_BYTES, &p.tmB, fbar, nb + b * Cfg::ATOM, k,
-                                 keep);
+                tma_load_2d_pair(sb + b * Cfg::ATOM_BYTES, tmb, fbar, nb + b * Cfg::ATOM, k, keep);
             }
           }
           ++armed;
@@ -535,6 +583,11 @@ __global__ void __launch_bounds__((WgradCfg<kFP8, kBN, kKMajor, kMG, kTransD>::T
       constexpr uint32_t kIdescBase =
           (kFP8 ? idesc_mxf8(2 * Cfg::BM, kBN, 0, 0) : idesc_bf16(2 * Cfg::BM, kBN)) &
           (Cfg::A_KM ? ~(1u << 15) : ~0u) & (Cfg::B_KM ? ~(1u << 16) : ~0u);
+      // mixed widths: the narrow tiles' MMAs (N = BN1)
+      constexpr uint32_t kIdescNarrow = kFP8 ? idesc_mxf8(2 * Cfg::BM, Cfg::BN1, 0, 0) : kIdescBase;
+      uint32_t ig = 0;             // scale groups issued
+      int ts = 0;                  // tensor-memory slot of the next group (ig mod SF_TSLOTS)
+      uint32_t tw = 0;             // parity of ig / SF_TSLOTS
       // Descriptors of stage 0 / scale slot 0; later stages and k-steps add
       // their byte offset >> 4 to the start-address field (shared addresses
       // stay below 256 KB, so the field never carries out).
@@ -565,67 +618,92 @@ __global__ void __launch_bounds__((WgradCfg<kFP8, kBN, kKMajor, kMG, kTransD>::T
           tc_fence_after();
         }
         const uint32_t d_tmem = tmem_base + b * kBN;
-        const TileCoord tcm = tile_coord<kMG>(p, sched, ch.u, kBN, 0);
+        const TileCoord tcm = tile_coord<kMG>(p, sched, ch.u, Cfg::BN1, 0);
         const KRot rot = tile_rot(tcm.mt, tcm.nt, ch.nk, Cfg::ROT_UNIT);
-        for (int j = ch.j0; j < ch.j1; ++j) {
-          const int jj = rot_stage(j, rot);   // k-block of this position
-          if constexpr (kFP8) {
-            if ((jj & gs_mask) == 0) {
-              DG_T0(w1);
-              ok = DG_MMA_OK(mbar_wait(&sfr[g], gph, abort_flag, lim, p.status, W_MMA_SFR, t));
-              DG_TACC(2, w1);
-              if (!ok) break;
-              tc_fence_after();
-              sfa_t = tmem_base + Cfg::SF_COL0 + g * Cfg::SF_COLS;
-              sfb_t = sfa_t + 4;
-              DG_ISSUE tmem_cp_32x128b_warpx4_pair(sfa_t, uta_desc0 + static_cast<uint64_t>(g * (Cfg::UT_A >> 4)));
-#pragma unroll
-              for (int c = 0; c < Cfg::SF_CHUNKS_B; ++c)
-                DG_ISSUE tmem_cp_32x128b_warpx4_pair(
-                    sfb_t + 4 * c,
-                    utb_desc0 + static_cast<uint64_t>(g * (Cfg::UT_B >> 4) + c * (512 >> 4)));
-              DG_ISSUE mma_commit_pair(&sfe[g], 0x3);
-              if (++g == NS) { g = 0; gph ^= 1; }
-            }
-          }
-          DG_T0(w2);
-          // A stage is complete once both CTAs' bytes land (`full`); an
-          // expert's last, partial BF16 stage once warp 6 has also masked the
-          // rows past the slice in both CTAs (`gate`, used by tail stages only).
-          const bool tail = !kFP8 && jj == ch.nk - 1 && tcm.k_len - jj * Cfg::BK < Cfg::BK;
-          // (the gate's phase is completed by a cluster-scope release from the
-          // odd CTA, whose zeroed rows the MMA reads: cluster-scope acquire)
-          ok = DG_MMA_OK(tail ? mbar_wait<true>(&gate[s], (gate_ph >> s) & 1u, abort_flag, lim,
-                                                p.status, W_MMA_FULL, t)
-                              : mbar_wait(&full[s], ph, abort_flag, lim, p.status, W_MMA_FULL, t));
-          if (tail) gate_ph ^= 1u << s;
-          DG_TACC(2, w2);
-          if (!ok) break;
-          tc_fence_after();
-          // gran_k 128: byte j%4 of each scale word holds this k-block's
-          // scale; gran_k 32: byte ks holds this 32-token sub-block's.
-          const uint32_t idesc_j = kIdescBase | ((gs == 4) ? (static_cast<uint32_t>(jj & 3) * 0x20000010u) : 0u);
-#pragma unroll
-          for (int ks = 0; ks < Cfg::KSTEPS; ++ks) {
-            const uint64_t ad = a_desc + static_cast<uint64_t>(ks * (Cfg::A_KSTEP >> 4));
-            const uint64_t bd = b_desc + static_cast<uint64_t>(ks * (Cfg::B_KSTEP >> 4));
+        // The chunk's stages, with the tile's instruction descriptor as a
+        // compile-time constant: one selected at run time slowed the MMA
+        // stream by about 40 % (measured), so mixed widths run one of two
+        // copies of this loop.
+        auto stages = [&](auto id_c) {
+          constexpr uint32_t idesc_t = decltype(id_c)::value;
+          for (int j = ch.j0; j < ch.j1; ++j) {
+            const int jj = rot_stage(j, rot);   // k-block of this position
             if constexpr (kFP8) {
-              const uint32_t idesc = (gs == 4) ? idesc_j : (kIdescBase | (static_cast<uint32_t>(ks) * 0x20000010u));
-              DG_ISSUE mma_mxf8_pair(d_tmem, ad, bd, idesc, sfa_t, sfb_t, (j | ks) != 0);
+              if ((jj & gs_mask) == 0) {
+                DG_T0(w1);
+                ok = DG_MMA_OK(mbar_wait(&sfr[g], gph, abort_flag, lim, p.status, W_MMA_SFR, t));
+                DG_TACC(2, w1);
+                if (!ok) break;
+                // The MMAs of the previous group are committed to its slot's
+                // sfd; this group's copy overwrites the slot of group
+                // ig - SF_TSLOTS, whose MMAs must have completed.
+                constexpr int T = Cfg::SF_TSLOTS;
+                if (ig >= 1) DG_ISSUE mma_commit_pair(&sfd[ts == 0 ? T - 1 : ts - 1], 0x1);
+                if (ig >= static_cast<uint32_t>(T))
+                  ok = DG_MMA_OK(mbar_wait(&sfd[ts], tw ^ 1, abort_flag, lim, p.status, W_MMA_SFD, t));
+                if (!ok) break;
+                tc_fence_after();
+                sfa_t = tmem_base + Cfg::SF_COL0 + ts * Cfg::SF_COLS;
+                ++ig;
+                if (++ts == T) { ts = 0; tw ^= 1; }
+                sfb_t = sfa_t + 4;
+                DG_ISSUE tmem_cp_32x128b_warpx4_pair(sfa_t, uta_desc0 + static_cast<uint64_t>(g * (Cfg::UT_A >> 4)));
+#pragma unroll
+                for (int c = 0; c < Cfg::SF_CHUNKS_B; ++c)
+                  DG_ISSUE tmem_cp_32x128b_warpx4_pair(
+                      sfb_t + 4 * c,
+                      utb_desc0 + static_cast<uint64_t>(g * (Cfg::UT_B >> 4) + c * (512 >> 4)));
+                DG_ISSUE mma_commit_pair(&sfe[g], 0x3);
+                if (++g == NS) { g = 0; gph ^= 1; }
+              }
+            }
+            DG_T0(w2);
+            // A stage is complete once both CTAs' bytes land (`full`); an
+            // expert's last, partial BF16 stage once warp 6 has also masked the
+            // rows past the slice in both CTAs (`gate`, used by tail stages only).
+            const bool tail = !kFP8 && jj == ch.nk - 1 && tcm.k_len - jj * Cfg::BK < Cfg::BK;
+            // (the gate's phase is completed by a cluster-scope release from the
+            // odd CTA, whose zeroed rows the MMA reads: cluster-scope acquire)
+            ok = DG_MMA_OK(tail ? mbar_wait<true>(&gate[s], (gate_ph >> s) & 1u, abort_flag, lim,
+                                                  p.status, W_MMA_FULL, t)
+                                : mbar_wait(&full[s], ph, abort_flag, lim, p.status, W_MMA_FULL, t));
+            if (tail) gate_ph ^= 1u << s;
+            DG_TACC(2, w2);
+            if (!ok) break;
+            tc_fence_after();
+            // gran_k 128: byte j%4 of each scale word holds this k-block's
+            // scale; gran_k 32: byte ks holds this 32-token sub-block's.
+            const uint32_t idesc_j = idesc_t | ((gs == 4) ? (static_cast<uint32_t>(jj & 3) * 0x20000010u) : 0u);
+#pragma unroll
+            for (int ks = 0; ks < Cfg::KSTEPS; ++ks) {
+              const uint64_t ad = a_desc + static_cast<uint64_t>(ks * (Cfg::A_KSTEP >> 4));
+              const uint64_t bd = b_desc + static_cast<uint64_t>(ks * (Cfg::B_KSTEP >> 4));
+              if constexpr (kFP8) {
+                const uint32_t idesc = (gs == 4) ? idesc_j : (idesc_t | (static_cast<uint32_t>(ks) * 0x20000010u));
+                DG_ISSUE mma_mxf8_pair(d_tmem, ad, bd, idesc, sfa_t, sfb_t, (j | ks) != 0);
+              } else {
+                DG_ISSUE mma_bf16_pair(d_tmem, ad, bd, idesc_t, (j | ks) != 0);
+              }
+            }
+            DG_ISSUE mma_commit_pair(&empty[s], 0x3);
+            if (++s == S) {
+              s = 0;
+              ph ^= 1;
+              a_desc = a_desc0;
+              b_desc = b_desc0;
             } else {
-              DG_ISSUE mma_bf16_pair(d_tmem, ad, bd, kIdescBase, (j | ks) != 0);
+              a_desc += Cfg::A_BYTES >> 4;
+              b_desc += Cfg::B_BYTES >> 4;
             }
           }
-          DG_ISSUE mma_commit_pair(&empty[s], 0x3);
-          if (++s == S) {
-            s = 0;
-            ph ^= 1;
-            a_desc = a_desc0;
-            b_desc = b_desc0;
-          } else {
-            a_desc += Cfg::A_BYTES >> 4;
-            b_desc += Cfg::B_BYTES >> 4;
-          }
+        };
+        if constexpr (Cfg::kMixed) {
+          if (tcm.bn != kBN)
+            stages(std::integral_constant<uint32_t, kIdescNarrow>{});
+          else
+            stages(std::integral_constant<uint32_t, kIdescBase>{});
+        } else {
+          stages(std::integral_constant<uint32_t, kIdescBase>{});
         }
         if (!ok) break;
         if (ch.j1 == ch.nk) {
@@ -662,7 +740,7 @@ __global__ void __launch_bounds__((WgradCfg<kFP8, kBN, kKMajor, kMG, kTransD>::T
           const int t = ch.u;
           const int nk = ch.nk;
           const int tail = sched[fast_div(ch.u, p.div_tpg)].k_len - (nk - 1) * Cfg::BK;
-          const TileCoord tcg = tile_coord<kMG>(p, sched, ch.u, kBN, 0);
+          const TileCoord tcg = tile_coord<kMG>(p, sched, ch.u, Cfg::BN1, 0);
           const KRot rot = tile_rot(tcg.mt, tcg.nt, nk, Cfg::ROT_UNIT);
           for (int j = ch.j0; j < ch.j1; ++j) {
             const int jj = rot_stage(j, rot);
@@ -732,7 +810,7 @@ __global__ void __launch_bounds__((WgradCfg<kFP8, kBN, kKMajor, kMG, kTransD>::T
               have = lane_next(L, p, pid, R, Cfg::BK, ch);
               if (!have) break;
               if (ch.nk == 0) { have = false; continue; }
-              tc = tile_coord<kMG>(p, sched, ch.u, kBN, rank);
+              tc = tile_coord<kMG>(p, sched, ch.u, Cfg::BN1, rank);
               rot = tile_rot(tc.mt, tc.nt, ch.nk, Cfg::ROT_UNIT);
               j = ch.j0;
               continue;
@@ -755,8 +833,11 @@ __global__ void __launch_bounds__((WgradCfg<kFP8, kBN, kKMajor, kMG, kTransD>::T
           const int grp_a = kMG ? (jj >> gs_shift) : grp;
           tma_load_2d_pair(smem + Cfg::OFF_UTA + g * Cfg::UT_A, &p.tmSFA, sfr_leader + 8 * g, 0,
                            grp_a * p.sf_mc + tc.m0 / 128, keep);
+          // B's records: the wide entries' groups (n_tiles_w tiles each) first
+          const int brec = grp < p.sf_gw ? grp * p.n_tiles_w + tc.nt
+                                         : p.sf_gw * p.n_tiles_w + (grp - p.sf_gw) * p.n_tiles + tc.nt;
           tma_load_2d_pair(smem + Cfg::OFF_UTB + g * Cfg::UT_B, &p.tmSFB, sfr_leader + 8 * g, 0,
-                           (grp * p.n_tiles + tc.nt) * Cfg::SF_CHUNKS_B, keep);
+                           brec * Cfg::SF_CHUNKS_B, keep);
           ++ig;
           ++j;
         }
@@ -887,12 +968,12 @@ __global__ void __launch_bounds__((WgradCfg<kFP8, kBN, kKMajor, kMG, kTransD>::T
     while (ok && lane_next(L, p, pid, R, Cfg::BK, ch)) {
       if (ch.nk > 0 && ch.j1 != ch.nk) continue;   // only tile completions
       const int t = ch.u;
-      const TileCoord tc = tile_coord<kMG>(p, sched, ch.u, kBN, rank);
+      const TileCoord tc = tile_coord<kMG>(p, sched, ch.u, Cfg::BN1, rank);
       const bool mma_tile = ch.nk > 0;
       const int b = ch.lane;
       const int sel = half ^ static_cast<int>(ntile & 1);   // this tile's chunk set
       ++ntile;
-      const int ncols = min(kBN, p.N - tc.n0);
+      const int ncols = min(tc.bn, p.N - tc.n0);
       const int nch = (ncols + EC - 1) / EC;
       const int mine = nch > sel ? (nch - sel + 1) / 2 : 0;   // chunks sel, sel + 2, ...
       const int row0 = tc.m0 + 32 * q;
@@ -972,7 +1053,7 @@ __global__ void __launch_bounds__((WgradCfg<kFP8, kBN, kKMajor, kMG, kTransD>::T
     while (lane_next(L, p, pid, R, Cfg::BK, ch)) {
       if (ch.nk > 0 && ch.j1 != ch.nk) continue;   // only tile completions
       const int t = ch.u;
-      const TileCoord tc = tile_coord<kMG>(p, sched, ch.u, kBN, rank);
+      const TileCoord tc = tile_coord<kMG>(p, sched, ch.u, Cfg::BN1, rank);
       const bool mma_tile = ch.nk > 0;
       // M-grouped: a CTA whose 128 rows lie past its expert's last token
       // (the second half of an expert's last 256-row chunk) stores nothing.
@@ -986,7 +1067,7 @@ __global__ void __launch_bounds__((WgradCfg<kFP8, kBN, kKMajor, kMG, kTransD>::T
         if (!__all_sync(0xffffffffu, got)) break;
         tc_fence_after();
       }
-      const int ncols = min(kBN, p.N - tc.n0);
+      const int ncols = min(tc.bn, p.N - tc.n0);
       const int nch = (ncols + EC - 1) / EC;
       const int row0 = tc.m0 + 32 * q;    // first output row of this warp's boxes
       const uint32_t tmem_row = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + b * kBN;

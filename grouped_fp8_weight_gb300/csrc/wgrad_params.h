@@ -64,6 +64,7 @@ enum OutMode : int {
 struct WgradParams {
   CUtensorMap tmA;     // operand A [sum_k, M], 128-byte swizzled tiles
   CUtensorMap tmB;     // operand B [sum_k, N], 128-byte swizzled tiles
+  CUtensorMap tmBn;    // mixed widths: B boxes of the narrow tiles (kNarrowBN / 2 columns)
   CUtensorMap tmSFA;   // FP8: packed scale records of A, 512 bytes each (see PackParams)
   CUtensorMap tmSFB;   // FP8: packed scale records of B, CB x 512 bytes per box
   CUtensorMap tmD;     // output [G, M, N] as 3-D {N, M, G}
@@ -81,6 +82,13 @@ struct WgradParams {
   int n_entries;       // M-grouped: schedule entries
   int n_sched;         // valid entries of sched (copied to shared memory when they fit)
   FastDiv div_tpg, div_mt, div_nt;   // by tiles_per_group, m_tiles, n_tiles
+  // Mixed tile widths (FP8, kernel N a multiple of 256 and of 224): the first
+  // n_wide schedule entries are cut into 256-column tiles (wide_tiles of them,
+  // first in the tile list; n_tiles_w per row), every later entry into
+  // 224-column tiles (n_tiles per row).  Their packed B records come first
+  // (sf_gw scale groups of n_tiles_w tiles each).  Zero otherwise.
+  int n_wide, wide_tiles, n_tiles_w, tpg_w, sf_gw;
+  FastDiv div_tpg_w, div_nt_w;
   uint64_t wait_limit_ns;
   DevStatus *status;
   const int *ks_dev;
@@ -97,6 +105,8 @@ inline void set_derived(WgradParams &p, int n_sched) {
   p.div_tpg = make_fastdiv(static_cast<uint32_t>(p.tiles_per_group > 0 ? p.tiles_per_group : 1));
   p.div_mt = make_fastdiv(static_cast<uint32_t>(p.m_tiles > 0 ? p.m_tiles : 1));
   p.div_nt = make_fastdiv(static_cast<uint32_t>(p.n_tiles > 0 ? p.n_tiles : 1));
+  p.div_tpg_w = make_fastdiv(static_cast<uint32_t>(p.tpg_w > 0 ? p.tpg_w : 1));
+  p.div_nt_w = make_fastdiv(static_cast<uint32_t>(p.n_tiles_w > 0 ? p.n_tiles_w : 1));
 }
 
 // FP8 scale packing (scale_pack.cu): every scale group the GEMM uses, laid
@@ -106,17 +116,20 @@ inline void set_derived(WgradParams &p, int n_sched) {
 struct PackParams {
   const uint8_t *sfa, *sfb;   // [sum_k / gran_k, M] and [sum_k / gran_k, N]
   uint32_t *sfa_p;            // [n_groups][MC][128 words]
-  uint32_t *sfb_p;            // [n_groups][NT][CB][128 words]
+  uint32_t *sfb_p;            // [GW][NTW][CB] then [n_groups - GW][NT][CB], 128 words each
   int M, N, MC, NT, CB, BN;
+  int GW, NTW, BNW;           // mixed widths: the first GW groups use NTW tiles of BNW columns
   int n_entries, n_groups;
   int g_off[kMaxGroups];
   int row_off[kMaxGroups];
   int row_end[kMaxGroups];
 };
 
-// Fills pk's plan (and p.sched[i].g_off, p.sf_mc) from the first n_mma
-// schedule entries of p for block width bn; returns the scratch bytes the
-// packed records need (0 when there is no GEMM work).
+// Fills pk's plan (and p.sched[i].g_off, p.sf_mc, p.sf_gw) from the first
+// n_mma schedule entries of p for block width bn (the narrow width when
+// p.n_wide > 0: the first p.n_wide entries then use p.n_tiles_w tiles of
+// kWideBN columns); returns the scratch bytes the packed records need (0 when
+// there is no GEMM work).
 size_t plan_scale_pack(WgradParams &p, PackParams &pk, int n_mma, int gran_k, int bn);
 // Points pk at `scratch` (16-byte aligned, plan_scale_pack's size).
 void bind_scale_pack(PackParams &pk, void *scratch, const uint8_t *sfa, const uint8_t *sfb);
@@ -144,7 +157,8 @@ cudaError_t launch_kgrouped_bf16(const WgradParams &p, int block_n, int pairs,
 cudaError_t launch_kgrouped_fp8_nt(const WgradParams &p, int block_n, int pairs,
                                    cudaStream_t stream);
 // Transposed output tiles (the kernel's A is the caller's B, its M the
-// caller's N; D and C maps keep the caller's [G, M, N]); block_n 224 only.
+// caller's N; D and C maps keep the caller's [G, M, N]); block_n 224, or 256
+// (mixed widths).
 cudaError_t launch_kgrouped_fp8_t(const WgradParams &p, int block_n, int pairs,
                                   cudaStream_t stream);
 cudaError_t launch_kgrouped_fp8_nt_t(const WgradParams &p, int block_n, int pairs,
@@ -223,6 +237,11 @@ inline CUtensorMapSwizzle epi_swizzle(int elem_bytes) {
                     : row == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
 }
 constexpr int kBf16Chunk = 80;
+// Mixed tile widths: block_n kWideBN selects the FP8 variant whose first
+// accumulator is 256 columns wide and second kNarrowBN (256 + 224 + two
+// 12-column scale slots fit the 512 tensor-memory columns).
+constexpr int kWideBN = 256;
+constexpr int kNarrowBN = 224;
 int fp8_pick_block_n(int N);
 int bf16_pick_block_n(int N);
 

@@ -45,7 +45,8 @@ def _noalloc(ops, d, c, ks, ks_dev, gran_k):
 
 # (ks, M, N, gran_k, output, accumulator): direct 224-wide tiles, 128-wide
 # ragged tiles, transposed tiles (N % 224 != 0, M % 224 == 0), BF16 output,
-# a separate C, in place with an expert long enough to be split along K.
+# a separate C, in place with an expert long enough to be split along K, and
+# mixed 256 / 224 widths (N = 1792) with and without an accumulator.
 CASES = [
     ([256, 0, 384, 128], 256, 448, 128, "f32", "inplace"),
     ([128, 640, 0], 384, 672, 128, "f32", "none"),
@@ -53,6 +54,8 @@ CASES = [
     ([384, 128, 0, 256], 448, 256, 128, "bf16", "none"),
     ([640, 256, 0], 448, 2048, 32, "f32", "inplace"),
     ([128 * 40, 128, 0], 256, 448, 128, "f32", "inplace"),
+    ([128 * 12, 0, 128 * 6, 256], 256, 1792, 128, "f32", "none"),
+    ([128 * 12, 0, 128 * 6, 256], 512, 1792, 32, "f32", "inplace"),
 ]
 
 
