@@ -190,11 +190,11 @@ bool deterministic_requested() {
 
 // DG_MIXED_TILES in the environment (read at each call): 0 keeps every FP8
 // tile 224 columns wide; a positive number is the percentage of the narrow
-// tiles' count that the wide tiles' lane-0 turns may reach (default 100; see
-// grouped_schedule).
+// tiles' count that the wide tiles' lane-0 turns may reach (see
+// grouped_schedule).  -1 when unset: the default for the output mode.
 static int mixed_tiles_percent() {
   const char *v = std::getenv("DG_MIXED_TILES");
-  if (v == nullptr || *v == '\0') return 100;
+  if (v == nullptr || *v == '\0') return -1;
   const int pct = std::atoi(v);
   return pct < 0 ? 0 : pct;
 }
@@ -342,13 +342,20 @@ void grouped_schedule(const GroupedArgs &x, int sms, WgradParams &p, PackParams 
   p.num_mma_tiles = g.n_mma * p.tiles_per_group;
   p.num_tiles = n * p.tiles_per_group;
   p.gran_k = x.fp8 ? x.gran_k : 0;
+  // Mixed tile widths are possible (see below): FP8, token-major operands,
+  // kernel N a multiple of both 256 and 224.
+  const int mix_pct_env = mixed_tiles_percent();
+  const bool mixable = x.fp8 && !x.kmajor && bn == kNarrowBN && Nk % kWideBN == 0 &&
+                       g.n_mma > 0 && mix_pct_env != 0;
   p.chunk = !x.fp8                  ? kBf16Chunk
-            : x.d_dtype == DG_BF16    ? kFp8ChunkBf16Out
+            : x.d_dtype == DG_BF16    ? (mixable ? kFp8ChunkBf16OutMixed : kFp8ChunkBf16Out)
             : (x.c == x.d)            ? kFp8ChunkInPlace
                                       : kFp8Chunk;
-  if (const char *v = std::getenv("DG_LANE_CHUNK")) {   // tuning override (multiple of 4)
-    const int c = std::atoi(v);
+  const char *chunk_env = std::getenv("DG_LANE_CHUNK");
+  if (chunk_env != nullptr) {   // tuning override (multiple of 4)
+    const int c = std::atoi(chunk_env);
     if (c > 0 && (!x.fp8 || c % 4 == 0)) p.chunk = c;
+    else chunk_env = nullptr;
   }
   // Sweep the smaller operand's tiles fastest: the concurrently running tiles
   // then share the larger operand's slices, and the smaller one stays in L2
@@ -367,8 +374,13 @@ void grouped_schedule(const GroupedArgs &x, int sms, WgradParams &p, PackParams 
   // of its turns on them pairs with a narrow tile of lane 1: entries become
   // wide, longest first, while the narrow tiles left still cover the lane-0
   // turns that the wide ones take.
-  const int mix_pct = mixed_tiles_percent();
-  if (x.fp8 && !x.kmajor && bn == kNarrowBN && Nk % kWideBN == 0 && g.n_mma > 0 && mix_pct > 0) {
+  // (the share, unless DG_MIXED_TILES sets it: 50 % for FP32 output without
+  // an accumulator in place, whose heavy drains favour more narrow tiles,
+  // 100 % otherwise; measured)
+  const int mix_pct = mix_pct_env >= 0 ? mix_pct_env
+                      : (p.out_mode == OUT_F32 || p.out_mode == OUT_F32_C) ? kMixPercentF32
+                                                                            : kMixPercent;
+  if (mixable) {
     const int ntw = Nk / kWideBN;
     const int64_t tpg_w = static_cast<int64_t>(p.m_tiles) * ntw;
     int64_t narrow = static_cast<int64_t>(n) * tpg;   // narrow tiles with no wide entry
@@ -389,6 +401,9 @@ void grouped_schedule(const GroupedArgs &x, int sms, WgradParams &p, PackParams 
       p.wide_tiles = static_cast<int>(nw * tpg_w);
       p.num_mma_tiles = p.wide_tiles + (g.n_mma - nw) * tpg;
       p.num_tiles = p.wide_tiles + (n - nw) * tpg;
+    } else if (p.chunk == kFp8ChunkBf16OutMixed && chunk_env == nullptr &&
+               x.d_dtype == DG_BF16) {
+      p.chunk = kFp8ChunkBf16Out;   // no wide entry: the 224-only kernel's chunk
     }
   }
   g.sf_bytes = (x.fp8 && g.n_mma > 0) ? plan_scale_pack(p, pk, g.n_mma, x.gran_k, bn) : 0;

@@ -224,9 +224,15 @@ constexpr int kPairM = 256;
 // short turns; in-place accumulation (reduce-add) was measured best at 16.
 constexpr int kFp8Chunk = 48;
 constexpr int kFp8ChunkBf16Out = 8;
+constexpr int kFp8ChunkBf16OutMixed = 12;   // BF16 output with mixed tile widths
 constexpr int kFp8ChunkInPlace = 16;
-static_assert(kFp8Chunk % 4 == 0 && kFp8ChunkBf16Out % 4 == 0 && kFp8ChunkInPlace % 4 == 0,
+static_assert(kFp8Chunk % 4 == 0 && kFp8ChunkBf16Out % 4 == 0 && kFp8ChunkInPlace % 4 == 0 &&
+                  kFp8ChunkBf16OutMixed % 4 == 0,
               "lane chunks must start on a scale group (four k-blocks)");
+// Mixed tile widths: the lane-0 turns of the wide tiles may reach this
+// percentage of the narrow tiles' count (FP32 output / the other modes).
+constexpr int kMixPercentF32 = 50;
+constexpr int kMixPercent = 100;
 // Epilogue chunk: output columns per staged TMA store box (32 rows high).
 constexpr int kEpiCols = 32;
 // Staging row of kEpiCols elements of `bytes` each is stored with the TMA
