@@ -153,12 +153,10 @@ struct WgradCfg {
   static constexpr int SF_COL0 = kBN + BN1;              // after the two accumulators
   // Tensor-memory scale slots, a ring of SF_TSLOTS (two with mixed widths,
   // whose accumulators leave room for no more).  The copy of a group's scales
-  // into a slot waits until the MMAs of the group that last read the slot
-  // have completed: the tensor pipe orders a copy before later MMAs, but not
-  // after earlier ones.
+  // into a slot is issued only once the MMAs of the group that last read the
+  // slot have completed: the tensor pipe orders a copy before later MMAs, but
+  // not after earlier ones.
   static constexpr int SF_TSLOTS = kMixed ? 2 : SF_SLOTS;
-  static constexpr int SF_TSLOTS_MAX = 5;
-  static_assert(SF_TSLOTS <= SF_TSLOTS_MAX, "scale-slot barriers");
   static constexpr int EC = kEpiCols;                   // output columns per epilogue chunk
   static constexpr int WSTG_BYTES = 32 * EC * 4;        // per epilogue warp and buffer: 32 FP32 rows
   static constexpr int EPI_BUFS = 8 / EPI_WARPS;        // staging buffers per epilogue warp
@@ -174,8 +172,8 @@ struct WgradCfg {
   static constexpr int OFF_UTB = OFF_UTA + SF_SLOTS * UT_A;
   static constexpr int OFF_BAR = (OFF_UTB + SF_SLOTS * UT_B + 7) / 8 * 8;
   // barriers: full[S], empty[S], gate[S], tfull[S], accf[2], acce[2],
-  // cbar[4 warps x 2], sfr/sfe[SLOTS], drain, sfd[TSLOTS_MAX]
-  static constexpr int NUM_BARS = 4 * STAGES + 2 * NUM_ACC + 8 + 2 * SF_SLOTS + 1 + SF_TSLOTS_MAX;
+  // cbar[4 warps x 2], sfr/sfe[SLOTS], drain
+  static constexpr int NUM_BARS = 4 * STAGES + 2 * NUM_ACC + 8 + 2 * SF_SLOTS + 1;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   // The schedule table is read once per chunk by every role; indexed reads
   // of the kernel parameters miss the constant cache, so it is copied here
@@ -418,7 +416,6 @@ __global__ void __launch_bounds__((WgradCfg<kFP8, kBN, kKMajor, kMG, kTransD>::T
   uint64_t *sfr = cbar + 8;        // even CTA: both CTAs' records of a scale group landed
   uint64_t *sfe = sfr + NS;        // scale slot free (its tcgen05.cp completed)
   uint64_t *drain = sfe + NS;
-  uint64_t *sfd = drain + 1;       // even CTA: MMAs of the scale group in tensor-memory slot i completed
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Cfg::OFF_MISC);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + Cfg::OFF_MISC + 4);
 
@@ -455,7 +452,6 @@ __global__ void __launch_bounds__((WgradCfg<kFP8, kBN, kKMajor, kMG, kTransD>::T
       mbar_init(&sfe[i], 1);
     }
     mbar_init(drain, 1);
-    for (int i = 0; i < Cfg::SF_TSLOTS_MAX; ++i) mbar_init(&sfd[i], 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -587,7 +583,9 @@ __global__ void __launch_bounds__((WgradCfg<kFP8, kBN, kKMajor, kMG, kTransD>::T
       constexpr uint32_t kIdescNarrow = kFP8 ? idesc_mxf8(2 * Cfg::BM, Cfg::BN1, 0, 0) : kIdescBase;
       uint32_t ig = 0;             // scale groups issued
       int ts = 0;                  // tensor-memory slot of the next group (ig mod SF_TSLOTS)
-      uint32_t tw = 0;             // parity of ig / SF_TSLOTS
+      int n_st = 0;                // stages issued (stage n_st uses `empty[n_st % S]`, phase n_st / S)
+      int gstart = 0;              // first stage of the current scale group
+      uint32_t glens = 0;          // lengths (at most 7) of the last SF_TSLOTS - 1 groups, 3 bits each
       // Descriptors of stage 0 / scale slot 0; later stages and k-steps add
       // their byte offset >> 4 to the start-address field (shared addresses
       // stay below 256 KB, so the field never carries out).
@@ -628,35 +626,6 @@ __global__ void __launch_bounds__((WgradCfg<kFP8, kBN, kKMajor, kMG, kTransD>::T
           constexpr uint32_t idesc_t = decltype(id_c)::value;
           for (int j = ch.j0; j < ch.j1; ++j) {
             const int jj = rot_stage(j, rot);   // k-block of this position
-            if constexpr (kFP8) {
-              if ((jj & gs_mask) == 0) {
-                DG_T0(w1);
-                ok = DG_MMA_OK(mbar_wait(&sfr[g], gph, abort_flag, lim, p.status, W_MMA_SFR, t));
-                DG_TACC(2, w1);
-                if (!ok) break;
-                // The MMAs of the previous group are committed to its slot's
-                // sfd; this group's copy overwrites the slot of group
-                // ig - SF_TSLOTS, whose MMAs must have completed.
-                constexpr int T = Cfg::SF_TSLOTS;
-                if (ig >= 1) DG_ISSUE mma_commit_pair(&sfd[ts == 0 ? T - 1 : ts - 1], 0x1);
-                if (ig >= static_cast<uint32_t>(T))
-                  ok = DG_MMA_OK(mbar_wait(&sfd[ts], tw ^ 1, abort_flag, lim, p.status, W_MMA_SFD, t));
-                if (!ok) break;
-                tc_fence_after();
-                sfa_t = tmem_base + Cfg::SF_COL0 + ts * Cfg::SF_COLS;
-                ++ig;
-                if (++ts == T) { ts = 0; tw ^= 1; }
-                sfb_t = sfa_t + 4;
-                DG_ISSUE tmem_cp_32x128b_warpx4_pair(sfa_t, uta_desc0 + static_cast<uint64_t>(g * (Cfg::UT_A >> 4)));
-#pragma unroll
-                for (int c = 0; c < Cfg::SF_CHUNKS_B; ++c)
-                  DG_ISSUE tmem_cp_32x128b_warpx4_pair(
-                      sfb_t + 4 * c,
-                      utb_desc0 + static_cast<uint64_t>(g * (Cfg::UT_B >> 4) + c * (512 >> 4)));
-                DG_ISSUE mma_commit_pair(&sfe[g], 0x3);
-                if (++g == NS) { g = 0; gph ^= 1; }
-              }
-            }
             DG_T0(w2);
             // A stage is complete once both CTAs' bytes land (`full`); an
             // expert's last, partial BF16 stage once warp 6 has also masked the
@@ -671,6 +640,54 @@ __global__ void __launch_bounds__((WgradCfg<kFP8, kBN, kKMajor, kMG, kTransD>::T
             DG_TACC(2, w2);
             if (!ok) break;
             tc_fence_after();
+            if constexpr (kFP8) {
+              if ((jj & gs_mask) == 0) {
+                DG_T0(w1);
+                ok = DG_MMA_OK(mbar_wait(&sfr[g], gph, abort_flag, lim, p.status, W_MMA_SFR, t));
+                DG_TACC(2, w1);
+                if (!ok) break;
+                // This group's copy overwrites tensor-memory slot ts, last read
+                // by the MMAs of group ig - SF_TSLOTS, which ended `between`
+                // stages before this one (the lengths of the groups since).
+                // Stage n_st's bytes have landed, so the producer has seen
+                // stage n_st - S consumed (its `empty` commit), and with it
+                // every earlier MMA: with between >= S - 1 the slot is free.
+                // Otherwise (short groups) wait for the `empty` phase of that
+                // group's last stage, which cannot have been reused yet (the
+                // stage's next use is not issued).
+                constexpr int T = Cfg::SF_TSLOTS;
+                constexpr uint32_t kLenMask = (1u << (3 * (T - 1))) - 1u;
+                if (ig >= 1) {
+                  const int len = min(n_st - gstart, 7);
+                  glens = ((glens << 3) | static_cast<uint32_t>(len)) & kLenMask;
+                }
+                gstart = n_st;
+                if (ig >= static_cast<uint32_t>(T)) {
+                  int between = 0;
+#pragma unroll
+                  for (int i = 0; i < T - 1; ++i) between += static_cast<int>((glens >> (3 * i)) & 7u);
+                  if (between < S - 1) {
+                    const int last = n_st - 1 - between;
+                    ok = DG_MMA_OK(mbar_wait(&empty[last % S], static_cast<uint32_t>(last / S) & 1u,
+                                             abort_flag, lim, p.status, W_MMA_SFD, t));
+                  }
+                }
+                if (!ok) break;
+                tc_fence_after();
+                sfa_t = tmem_base + Cfg::SF_COL0 + ts * Cfg::SF_COLS;
+                ++ig;
+                if (++ts == T) ts = 0;
+                sfb_t = sfa_t + 4;
+                DG_ISSUE tmem_cp_32x128b_warpx4_pair(sfa_t, uta_desc0 + static_cast<uint64_t>(g * (Cfg::UT_A >> 4)));
+#pragma unroll
+                for (int c = 0; c < Cfg::SF_CHUNKS_B; ++c)
+                  DG_ISSUE tmem_cp_32x128b_warpx4_pair(
+                      sfb_t + 4 * c,
+                      utb_desc0 + static_cast<uint64_t>(g * (Cfg::UT_B >> 4) + c * (512 >> 4)));
+                DG_ISSUE mma_commit_pair(&sfe[g], 0x3);
+                if (++g == NS) { g = 0; gph ^= 1; }
+              }
+            }
             // gran_k 128: byte j%4 of each scale word holds this k-block's
             // scale; gran_k 32: byte ks holds this 32-token sub-block's.
             const uint32_t idesc_j = idesc_t | ((gs == 4) ? (static_cast<uint32_t>(jj & 3) * 0x20000010u) : 0u);
@@ -686,6 +703,7 @@ __global__ void __launch_bounds__((WgradCfg<kFP8, kBN, kKMajor, kMG, kTransD>::T
               }
             }
             DG_ISSUE mma_commit_pair(&empty[s], 0x3);
+            ++n_st;
             if (++s == S) {
               s = 0;
               ph ^= 1;
