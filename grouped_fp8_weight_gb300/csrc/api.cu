@@ -188,6 +188,11 @@ bool deterministic_requested() {
   return v != nullptr && *v != '\0' && *v != '0';
 }
 
+bool pdl_requested() {
+  const char *v = std::getenv("DG_PDL");
+  return v == nullptr || *v != '0';
+}
+
 // DG_MIXED_TILES in the environment (read at each call): 0 keeps every FP8
 // tile 224 columns wide; a positive number is the percentage of the narrow
 // tiles' count that the wide tiles' lane-0 turns may reach (see
@@ -568,6 +573,7 @@ dg_status run_grouped(const GroupedArgs &x) {
       cudaFreeAsync(scratch, x.stream);
       return fail(DG_ERR_CUDA, "%s: scale pack launch failed: %s", fn, cudaGetErrorString(e));
     }
+    p.pdl = dg::pdl_requested() ? 1 : 0;   // the GEMM may start beside the pack pass
   }
 
   // ---- launch: one persistent CTA pair per two SMs (or per tile when fewer)
@@ -765,6 +771,7 @@ dg_status run_mgrouped(const void *a, const uint8_t *sfa, const void *w, const u
     return fail(DG_ERR_CUDA, "%s: scale pack launch failed: %s", fn, cudaGetErrorString(e));
   }
   dg::set_derived(p, n_ent);
+  p.pdl = dg::pdl_requested() ? 1 : 0;   // the GEMM may start beside the second pack pass
   const int pairs = static_cast<int>(std::min<int64_t>(dev->sms / 2, tiles));
   e = w_kmajor ? dg::launch_mgrouped_fp8_nt(p, bn, pairs, stream)
                : dg::launch_mgrouped_fp8(p, bn, pairs, stream);

@@ -33,6 +33,11 @@ uint64_t wait_limit_ns();
 // reproducible, at some cost in balance when one expert holds most tokens.
 bool deterministic_requested();
 
+// DG_PDL=0 in the environment (read at each call) launches an FP8 GEMM only
+// after its scale-pack pass has completed, instead of as a programmatic
+// dependent that starts beside it.
+bool pdl_requested();
+
 struct GroupedArgs {
   const char *fn;   // entry-point name for messages
   bool fp8;

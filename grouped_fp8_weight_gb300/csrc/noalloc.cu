@@ -172,6 +172,7 @@ extern "C" dg_status dg_k_grouped_fp8_wgrad_noalloc(
     return dg::failf(DG_ERR_CUDA, "%s: clearing scratch: %s", fn, cudaGetErrorString(e));
   if (g.sf_bytes > 0 && (e = dg::launch_pack_scales(pk, st)) != cudaSuccess)
     return dg::failf(DG_ERR_CUDA, "%s: scale pack launch failed: %s", fn, cudaGetErrorString(e));
+  p.pdl = (g.sf_bytes > 0 && dg::pdl_requested()) ? 1 : 0;
   if ((e = dg::grouped_launch(x, g, p, dev->sms)) != cudaSuccess)
     return dg::failf(DG_ERR_CUDA, "%s: launch failed: %s", fn, cudaGetErrorString(e));
   dg::set_last_error("");

@@ -295,6 +295,17 @@ template <int N>
 __device__ __forceinline__ void bulk_wait() {
   asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
 }
+// Programmatic dependent launch: a grid launched as a programmatic dependent
+// may start while the grid before it in the stream is still running; a thread
+// that needs that grid's results waits here until it has completed and its
+// memory is visible (a no-op in a grid launched without the dependency).  The
+// earlier grid lets its dependents start with launch_dependents.
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }

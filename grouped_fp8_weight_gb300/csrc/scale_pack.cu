@@ -28,6 +28,7 @@ namespace dg {
 namespace {
 
 __global__ void __launch_bounds__(128) pack_scales_kernel(const __grid_constant__ PackParams p) {
+  griddep_launch_dependents();   // the GEMM may start its prologue and operand loads now
   const int gp = blockIdx.x;
   // schedule entry owning this group (g_off is increasing over entries)
   int lo = 0, hi = p.n_entries - 1;
@@ -70,6 +71,7 @@ __global__ void __launch_bounds__(128) pack_scales_kernel(const __grid_constant_
 // A's records for the M-grouped data gradient: one CTA per (group, token
 // chunk); thread 4l + q packs the four scale columns of token 128 tc + 32 q + l.
 __global__ void __launch_bounds__(128) pack_token_scales_kernel(const __grid_constant__ TokenPackParams p) {
+  griddep_launch_dependents();
   const int j = blockIdx.x, tc = blockIdx.y;
   const int t = threadIdx.x;
   const int l = t >> 2, q = t & 3;

@@ -809,6 +809,8 @@ __global__ void __launch_bounds__((WgradCfg<kFP8, kBN, kKMajor, kMG, kTransD>::T
       if (lane == 0) {
         prefetch_tmap(&p.tmSFA);
         prefetch_tmap(&p.tmSFB);
+        // the records come from the pack pass this grid may have started beside
+        griddep_wait();
         const uint64_t keep = l2_policy_evict_last();   // B's records serve every M tile
         const uint32_t sfr_leader = mapa_shared(smem_u32(&sfr[0]), 0);
         LaneSched L;
@@ -1238,11 +1240,15 @@ cudaError_t launch_wgrad_variant(const WgradParams &p, int pairs, cudaStream_t s
   auto kern = kgrouped_wgrad_kernel<kFP8, kBN, kOut, kKMajor, kTransD, kMG>;
   // the schedule length and the division constants come from set_derived()
   if (p.num_tiles > 0 && (p.n_sched <= 0 || p.n_sched > kMaxGroups)) return cudaErrorInvalidValue;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  // After the scale-pack pass: start while it runs (only the scale loader
+  // waits for its records, griddepcontrol.wait).
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(Cfg::THREADS, 1, 1);
   cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
@@ -1267,6 +1273,7 @@ cudaError_t launch_wgrad_variant(const WgradParams &p, int pairs, cudaStream_t s
   if (setup.err != cudaSuccess) return setup.err;
   if (setup.max_pairs > 0) pairs = min(pairs, setup.max_pairs);
   cfg.gridDim = dim3(2 * pairs, 1, 1);
+  if (kFP8 && p.pdl) cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, kern, p);
 }
 

@@ -89,6 +89,9 @@ struct WgradParams {
   // (sf_gw scale groups of n_tiles_w tiles each).  Zero otherwise.
   int n_wide, wide_tiles, n_tiles_w, tpg_w, sf_gw;
   FastDiv div_tpg_w, div_nt_w;
+  // FP8: the GEMM is launched as a programmatic dependent of the scale-pack
+  // pass just before it (host only: selects the launch attribute).
+  int pdl;
   uint64_t wait_limit_ns;
   DevStatus *status;
   const int *ks_dev;
