@@ -974,7 +974,7 @@ dg_status dg_swiglu_backward_quant_fp8(const void *h, const void *da, int64_t T,
     return fail(DG_ERR_INVALID_ARG, "%s: I = %d must be a positive multiple of 16", fn, I);
   if ((q_a == nullptr) != (sf_a == nullptr))
     return fail(DG_ERR_INVALID_ARG, "%s: q_a and sf_a go together", fn);
-  if ((I + 127) / 128 > 65535 || (T + 127) / 128 > 0x7FFFFFFFll)
+  if ((I + 127) / 128 > 65535 || ((T + 127) / 128) * ((I + 31) / 32) > 0x7FFFFFFFll)
     return fail(DG_ERR_UNSUPPORTED, "%s: T or I too large", fn);
   if (T == 0) return ok();
   if (h == nullptr || da == nullptr || q_dh == nullptr || sf_dh == nullptr || !aligned16(h) ||
@@ -985,9 +985,31 @@ dg_status dg_swiglu_backward_quant_fp8(const void *h, const void *da, int64_t T,
   DeviceState *dev = nullptr;
   dg_status s = device_state(&dev);
   if (s != DG_OK) return s;
-  dg::SwigluArgs a{h, da, T, I, static_cast<uint8_t *>(q_dh), sf_dh,
-                   static_cast<uint8_t *>(q_a), sf_a};
-  cudaError_t e = dg::launch_swiglu_bwd_cast(a, gran_k, reinterpret_cast<cudaStream_t>(stream));
+  static thread_local dg::SwigluArgs a;
+  std::memset(&a, 0, sizeof(a));
+  // h as {2I, T} and da as {I, T}, BF16, boxes of 32 channels x 128 tokens
+  const uint64_t dh[2] = {2 * static_cast<uint64_t>(I), static_cast<uint64_t>(T)};
+  const uint64_t sh[1] = {4 * static_cast<uint64_t>(I)};
+  const uint64_t dd[2] = {static_cast<uint64_t>(I), static_cast<uint64_t>(T)};
+  const uint64_t sd[1] = {2 * static_cast<uint64_t>(I)};
+  const uint32_t box[2] = {32, 128};
+  if ((s = encode(&a.tm_h, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, h, 2, dh, sh, box,
+                  CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B, "h")) ||
+      (s = encode(&a.tm_da, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, da, 2, dd, sd, box,
+                  CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B, "da")))
+    return s;
+  a.T = T;
+  a.I = I;
+  a.n_tt = static_cast<int>((T + 127) / 128);
+  a.n_tc = (I + 31) / 32;
+  a.q_dh = static_cast<uint8_t *>(q_dh);
+  a.sf_dh = sf_dh;
+  a.q_a = static_cast<uint8_t *>(q_a);
+  a.sf_a = sf_a;
+  a.status = dev->status;
+  a.wait_limit_ns = dg::wait_limit_ns();
+  cudaError_t e = dg::launch_swiglu_bwd_cast(a, gran_k, 2 * dev->sms,
+                                             reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess)
     return fail(DG_ERR_CUDA, "%s: launch failed: %s", fn, cudaGetErrorString(e));
   return ok();

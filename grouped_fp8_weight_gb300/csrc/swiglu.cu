@@ -8,12 +8,14 @@
 // and, optionally, the recomputed a (the down-projection's B operand) with one
 // UE8M0 scale per column per gran_k tokens, token-major.
 //
-// One CTA covers 128 tokens x 64 channels of I; each thread loads 4 rows x
-// 8 channels of g, u and da (16-byte loads), then
-//   pass 1: evaluates them once in FP32, parks the values in shared memory
-//           (96 KB) and keeps column maxima of |dg|, |du|, |a|; the CTA
-//           combines the maxima per token block;
-//   pass 2: scales the parked values by 2^-e and converts with the hardware's
+// Persistent CTAs (two per SM) walk tiles of 128 tokens x 32 channels of I.
+// Thread 0 brings each tile's g, u and da in by TMA (24 KB) into a ring of
+// four buffers, so the next three tiles land while this one is processed.  Each thread
+// takes 2 rows x 8 channels:
+//   pass 1: evaluates them once in FP32, keeps the 48 values in registers and
+//           column maxima of |dg|, |du|, |a|; the CTA combines the maxima per
+//           token block;
+//   pass 2: scales the values by 2^-e and converts with the hardware's
 //           saturating RNE E4M3 conversion.
 // The evaluation uses explicitly rounded operations (no contraction):
 // t = e^-|g| from expf (no overflow), r = 1 / (1 + t) from the hardware
@@ -28,16 +30,17 @@ namespace dg {
 
 namespace {
 
-constexpr int kSgT = 128;                    // tokens per CTA
-constexpr int kSgC = 64;                     // channels of I per CTA
+constexpr int kSgT = 128;                    // tokens per tile
+constexpr int kSgC = 32;                     // channels of I per tile
+constexpr int kSgCg = kSgC / 8;              // channel groups of 8 per tile
 constexpr int kSgCols = 24;                  // output columns per thread: 8 dg, 8 du, 8 a
-constexpr int kSgRows = 4;                   // rows per thread
-// Evaluated values parked between the passes: per thread 4 rows x 24 floats,
-// as float4 slot j of thread t at [j][t] (consecutive threads, consecutive
-// 16 bytes: conflict-free).
-constexpr int kSgVals = kSgRows * kSgCols / 4 * 256 * 16;      // 96 KB
-constexpr int kSgRed = 8 * 8 * kSgCols * 4;                    // per-warp partial maxima
-constexpr int kSgSmem = kSgVals + kSgRed;
+constexpr int kSgRows = 2;                   // rows per thread
+constexpr int kSgIn = kSgT * kSgC * 2;       // one BF16 input tile (8 KB)
+constexpr int kSgBuf = 3 * kSgIn;            // g, u, da of one tile
+constexpr int kSgRed = 8 * kSgCg * kSgCols * 4;   // per-warp partial maxima
+constexpr int kSgStages = 4;                 // input buffers per CTA
+constexpr int kSgBytes = 4 * kSgCg * kSgCols;      // scale bytes of up to four token blocks
+constexpr int kSgSmem = kSgStages * kSgBuf + kSgRed + kSgBytes + 8 * kSgStages + 16;   // + barriers, abort flag
 
 __device__ __forceinline__ float rcp_approx(float x) {
   float r;
@@ -91,43 +94,55 @@ __device__ __forceinline__ uint32_t quant4(float4 v, const float *m) {
 }
 
 template <int kGran, bool kWithA>
-__global__ void __launch_bounds__(256, 2) swiglu_bwd_cast_kernel(const SwigluArgs p) {
-  extern __shared__ __align__(16) uint8_t sg_smem[];
-  float4 *vals = reinterpret_cast<float4 *>(sg_smem);                       // [24][256]
-  float *red = reinterpret_cast<float *>(sg_smem + kSgVals);                // [8 warps][8][24]
+__global__ void __launch_bounds__(256, 2) swiglu_bwd_cast_kernel(const __grid_constant__ SwigluArgs p) {
+  extern __shared__ __align__(128) uint8_t sg_smem[];
+  float *red = reinterpret_cast<float *>(sg_smem + kSgStages * kSgBuf);     // [8 warps][4][24]
+  uint8_t *sbytes = sg_smem + kSgStages * kSgBuf + kSgRed;                 // [blocks][4][24]
+  uint64_t *full = reinterpret_cast<uint64_t *>(sg_smem + kSgStages * kSgBuf + kSgRed + kSgBytes);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(full + kSgStages);
   const int tid = threadIdx.x;
   const int w = tid >> 5, l = tid & 31;
-  const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kSgT;
   const int I = p.I;
-  // thread: channel group cg (8 channels), rows 16w + 4i + rs (i = 0..3)
-  const int cg = l & 7, rs = l >> 3;
-  const int col = blockIdx.y * kSgC + 8 * cg;
-  const bool col_ok = col < I;
-  const uint16_t *h = static_cast<const uint16_t *>(p.h);
-  const uint16_t *dap = static_cast<const uint16_t *>(p.da);
+  // thread: channel group cg (8 channels), rows 16w + 8i + rs (i = 0, 1)
+  const int cg = l & 3, rs = l >> 2;
+  const int n_tiles = p.n_tt * p.n_tc;
 
-  // ---- loads: 4 rows x (g, u, da), 16 bytes each (rows past T read as 0)
-  uint4 gv[kSgRows], uv[kSgRows], dv[kSgRows];
-#pragma unroll
-  for (int i = 0; i < kSgRows; ++i) {
-    const int64_t t = t0 + 16 * w + 4 * i + rs;
-    const bool ok = col_ok && t < p.T;
-    gv[i] = ok ? __ldcs(reinterpret_cast<const uint4 *>(h + t * 2 * I + col)) : make_uint4(0, 0, 0, 0);
-    uv[i] = ok ? __ldcs(reinterpret_cast<const uint4 *>(h + t * 2 * I + I + col)) : make_uint4(0, 0, 0, 0);
-    dv[i] = ok ? __ldcs(reinterpret_cast<const uint4 *>(dap + t * I + col)) : make_uint4(0, 0, 0, 0);
+  if (tid == 0) {
+    for (int k = 0; k < kSgStages; ++k) mbar_init(&full[k], 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  // g at channel c0, u at I + c0 (columns past 2I read as 0; those past I
+  // in g's box are u's and are never used), da at c0; rows past T read as 0
+  auto issue = [&](int u, int b) {
+    const int tt = u / p.n_tc, tc = u - tt * p.n_tc;
+    uint8_t *dst = sg_smem + b * kSgBuf;
+    mbar_arrive_expect_tx(&full[b], kSgBuf);
+    tma_load_2d(dst, &p.tm_h, &full[b], tc * kSgC, tt * kSgT);
+    tma_load_2d(dst + kSgIn, &p.tm_h, &full[b], I + tc * kSgC, tt * kSgT);
+    tma_load_2d(dst + 2 * kSgIn, &p.tm_da, &full[b], tc * kSgC, tt * kSgT);
+  };
+  int issued = 0;
+  if (tid == 0) {
+    for (int k = 0; k < kSgStages; ++k) {
+      const int u = blockIdx.x + k * gridDim.x;
+      if (u < n_tiles) {
+        issue(u, k);
+        ++issued;
+      }
+    }
   }
 
-  // ---- pass 1: evaluate once, park the values, keep column maxima
-  // (non-negative float bit patterns order like the floats: integer maxima)
-  uint32_t mx[kSgCols];
-#pragma unroll
-  for (int k = 0; k < kSgCols; ++k) mx[k] = 0;
-#pragma unroll
-  for (int i = 0; i < kSgRows; ++i) {
-    const uint32_t gw[4] = {gv[i].x, gv[i].y, gv[i].z, gv[i].w};
-    const uint32_t uw[4] = {uv[i].x, uv[i].y, uv[i].z, uv[i].w};
-    const uint32_t dw[4] = {dv[i].x, dv[i].y, dv[i].z, dv[i].w};
-    float vg[8], vu[8], va[8];
+  // Column-wise evaluation of this thread's row i of the tile in buffer b.
+  auto eval_row = [&](const uint8_t *buf, int i, float (&vg)[8], float (&vu)[8], float (&va)[8]) {
+    const int r = 16 * w + 8 * i + rs;
+    const uint4 gv = *reinterpret_cast<const uint4 *>(buf + r * (kSgC * 2) + 16 * cg);
+    const uint4 uv = *reinterpret_cast<const uint4 *>(buf + kSgIn + r * (kSgC * 2) + 16 * cg);
+    const uint4 dv = *reinterpret_cast<const uint4 *>(buf + 2 * kSgIn + r * (kSgC * 2) + 16 * cg);
+    const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+    const uint32_t uw[4] = {uv.x, uv.y, uv.z, uv.w};
+    const uint32_t dw[4] = {dv.x, dv.y, dv.z, dv.w};
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
       const bool hi = k & 1;
@@ -135,115 +150,154 @@ __global__ void __launch_bounds__(256, 2) swiglu_bwd_cast_kernel(const SwigluArg
       const float u = hi ? bf16_hi(uw[k >> 1]) : bf16_lo(uw[k >> 1]);
       const float d = hi ? bf16_hi(dw[k >> 1]) : bf16_lo(dw[k >> 1]);
       swiglu_bwd(g, u, d, vg[k], vu[k], va[k]);
-      mx[k] = max(mx[k], __float_as_uint(fabsf(vg[k])));
-      mx[8 + k] = max(mx[8 + k], __float_as_uint(fabsf(vu[k])));
-      if constexpr (kWithA) mx[16 + k] = max(mx[16 + k], __float_as_uint(fabsf(va[k])));
     }
-    const int j = 6 * i;
-    vals[(j + 0) * 256 + tid] = make_float4(vg[0], vg[1], vg[2], vg[3]);
-    vals[(j + 1) * 256 + tid] = make_float4(vg[4], vg[5], vg[6], vg[7]);
-    vals[(j + 2) * 256 + tid] = make_float4(vu[0], vu[1], vu[2], vu[3]);
-    vals[(j + 3) * 256 + tid] = make_float4(vu[4], vu[5], vu[6], vu[7]);
-    if constexpr (kWithA) {
-      vals[(j + 4) * 256 + tid] = make_float4(va[0], va[1], va[2], va[3]);
-      vals[(j + 5) * 256 + tid] = make_float4(va[4], va[5], va[6], va[7]);
-    }
-  }
-  // lanes with the same channel group (rs = 0..3) hold rows of one warp's 16
-#pragma unroll
-  for (int k = 0; k < kSgCols; ++k) {
-    mx[k] = max(mx[k], __shfl_xor_sync(0xffffffffu, mx[k], 8));
-    mx[k] = max(mx[k], __shfl_xor_sync(0xffffffffu, mx[k], 16));
-  }
-  if (l < 8) {
-#pragma unroll
-    for (int k = 0; k < kSgCols; ++k) red[(w * 8 + cg) * kSgCols + k] = __uint_as_float(mx[k]);
-  }
-  __syncthreads();
-  // block maxima: gran 128 over all eight warps, gran 32 over warps 2b, 2b + 1
-  constexpr int kBlocks = kSgT / kGran;
-  constexpr int kWpb = 8 / kBlocks;          // warps per block
-  constexpr int kItems = kBlocks * 8 * kSgCols;
-  constexpr int kPer = (kItems + 255) / 256;
-  uint32_t fin[kPer];
-#pragma unroll
-  for (int i = 0; i < kPer; ++i) {
-    const int idx = tid + 256 * i;
-    fin[i] = 0;
-    if (idx < kItems) {
-      const int b = idx / (8 * kSgCols), rest = idx % (8 * kSgCols);
-#pragma unroll
-      for (int ww = 0; ww < kWpb; ++ww)
-        fin[i] = max(fin[i], __float_as_uint(red[(b * kWpb + ww) * 8 * kSgCols + rest]));
-    }
-  }
-  __syncthreads();
-#pragma unroll
-  for (int i = 0; i < kPer; ++i) {
-    const int idx = tid + 256 * i;
-    if (idx < kItems) red[idx] = __uint_as_float(fin[i]);
-  }
-  __syncthreads();
-  const int blk = (16 * w) / kGran;          // this thread's token block in the tile
-  float mul[kSgCols];
-  uint32_t sfw[6] = {0, 0, 0, 0, 0, 0};
-#pragma unroll
-  for (int k = 0; k < kSgCols; ++k) {
-    const int e = scale_exp_f32(__float_as_uint(red[(blk * 8 + cg) * kSgCols + k]));
-    mul[k] = pow2_neg(e);
-    sfw[k >> 2] |= static_cast<uint32_t>(e + 127) << (8 * (k & 3));
-  }
-  // scale bytes: the lanes holding the block's first row write them
-  const int64_t tb = t0 + 16 * w;
-  if (col_ok && rs == 0 && (16 * w) % kGran == 0 && tb < p.T) {
-    const int64_t srow = tb / kGran;
-    *reinterpret_cast<uint2 *>(p.sf_dh + srow * 2 * I + col) = make_uint2(sfw[0], sfw[1]);
-    *reinterpret_cast<uint2 *>(p.sf_dh + srow * 2 * I + I + col) = make_uint2(sfw[2], sfw[3]);
-    if constexpr (kWithA)
-      *reinterpret_cast<uint2 *>(p.sf_a + srow * I + col) = make_uint2(sfw[4], sfw[5]);
-  }
+  };
 
-  // ---- pass 2: quantise the parked values, store
+  int it = 0;
+  for (int u = blockIdx.x; u < n_tiles; u += gridDim.x, ++it) {
+    const int b = it % kSgStages;
+    const uint32_t par = static_cast<uint32_t>(it / kSgStages) & 1u;
+    const bool got = mbar_wait(&full[b], par, abort_flag, p.wait_limit_ns, p.status, 0x51, u);
+    if (__syncthreads_or(!got)) break;   // the whole CTA leaves together
+    const uint8_t *buf = sg_smem + b * kSgBuf;
+    const int tt = u / p.n_tc, tc = u - tt * p.n_tc;
+    const int64_t t0 = static_cast<int64_t>(tt) * kSgT;
+    const int col = tc * kSgC + 8 * cg;
+    const bool col_ok = col < I;
+
+    // ---- pass 1: evaluate once (values kept in registers), column maxima
+    // (non-negative float bit patterns order like the floats: integer maxima)
+    float vg[kSgRows][8], vu[kSgRows][8], va[kSgRows][8];
+    uint32_t mx[kSgCols];
 #pragma unroll
-  for (int i = 0; i < kSgRows; ++i) {
-    const int64_t t = t0 + 16 * w + 4 * i + rs;
-    const int j = 6 * i;
-    const uint32_t og0 = quant4(vals[(j + 0) * 256 + tid], mul);
-    const uint32_t og1 = quant4(vals[(j + 1) * 256 + tid], mul + 4);
-    const uint32_t ou0 = quant4(vals[(j + 2) * 256 + tid], mul + 8);
-    const uint32_t ou1 = quant4(vals[(j + 3) * 256 + tid], mul + 12);
-    if (col_ok && t < p.T) {
-      __stcs(reinterpret_cast<uint2 *>(p.q_dh + t * 2 * I + col), make_uint2(og0, og1));
-      __stcs(reinterpret_cast<uint2 *>(p.q_dh + t * 2 * I + I + col), make_uint2(ou0, ou1));
+    for (int k = 0; k < kSgCols; ++k) mx[k] = 0;
+#pragma unroll
+    for (int i = 0; i < kSgRows; ++i) {
+      eval_row(buf, i, vg[i], vu[i], va[i]);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        mx[k] = max(mx[k], __float_as_uint(fabsf(vg[i][k])));
+        mx[8 + k] = max(mx[8 + k], __float_as_uint(fabsf(vu[i][k])));
+        if constexpr (kWithA) mx[16 + k] = max(mx[16 + k], __float_as_uint(fabsf(va[i][k])));
+      }
     }
-    if constexpr (kWithA) {
-      const uint32_t oa0 = quant4(vals[(j + 4) * 256 + tid], mul + 16);
-      const uint32_t oa1 = quant4(vals[(j + 5) * 256 + tid], mul + 20);
-      if (col_ok && t < p.T)
-        __stcs(reinterpret_cast<uint2 *>(p.q_a + t * I + col), make_uint2(oa0, oa1));
+    // every read of buffer b is done: it takes the tile kSgStages steps
+    // ahead (issued after the barrier below)
+    // lanes with the same channel group (rs = 0..7) hold rows of one warp's 16
+#pragma unroll
+    for (int k = 0; k < kSgCols; ++k) {
+      mx[k] = max(mx[k], __shfl_xor_sync(0xffffffffu, mx[k], 4));
+      mx[k] = max(mx[k], __shfl_xor_sync(0xffffffffu, mx[k], 8));
+      mx[k] = max(mx[k], __shfl_xor_sync(0xffffffffu, mx[k], 16));
+    }
+    if (l < kSgCg) {
+#pragma unroll
+      for (int k = 0; k < kSgCols; ++k) red[(w * kSgCg + cg) * kSgCols + k] = __uint_as_float(mx[k]);
+    }
+    __syncthreads();
+    if (tid == 0) {
+      const int un = u + kSgStages * gridDim.x;
+      if (un < n_tiles) {
+        issue(un, b);
+        ++issued;
+      }
+    }
+    // block maxima: gran 128 over all eight warps, gran 32 over warps 2b, 2b + 1
+    constexpr int kBlocks = kSgT / kGran;
+    constexpr int kWpb = 8 / kBlocks;          // warps per block
+    constexpr int kItems = kBlocks * kSgCg * kSgCols;
+    constexpr int kPer = (kItems + 255) / 256;
+    uint32_t fin[kPer];
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int idx = tid + 256 * i;
+      fin[i] = 0;
+      if (idx < kItems) {
+        const int bb = idx / (kSgCg * kSgCols), rest = idx % (kSgCg * kSgCols);
+#pragma unroll
+        for (int ww = 0; ww < kWpb; ++ww)
+          fin[i] = max(fin[i], __float_as_uint(red[(bb * kWpb + ww) * kSgCg * kSgCols + rest]));
+      }
+    }
+    __syncthreads();
+    // one scale per (block, column): its factor 2^-e and its byte e + 127
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int idx = tid + 256 * i;
+      if (idx < kItems) {
+        const int e = scale_exp_f32(fin[i]);
+        red[idx] = pow2_neg(e);
+        sbytes[idx] = static_cast<uint8_t>(e + 127);
+      }
+    }
+    __syncthreads();
+    const int blk = (16 * w) / kGran;          // this thread's token block in the tile
+    const int sidx = (blk * kSgCg + cg) * kSgCols;
+    float mul[kSgCols];
+#pragma unroll
+    for (int k = 0; k < kSgCols; k += 4) {
+      const float4 m4 = *reinterpret_cast<const float4 *>(red + sidx + k);
+      mul[k] = m4.x;
+      mul[k + 1] = m4.y;
+      mul[k + 2] = m4.z;
+      mul[k + 3] = m4.w;
+    }
+    // scale bytes: the lanes holding the block's first row write them
+    const int64_t tb = t0 + 16 * w;
+    if (col_ok && rs == 0 && (16 * w) % kGran == 0 && tb < p.T) {
+      const int64_t srow = tb / kGran;
+      const uint2 *sb = reinterpret_cast<const uint2 *>(sbytes + sidx);
+      *reinterpret_cast<uint2 *>(p.sf_dh + srow * 2 * I + col) = sb[0];
+      *reinterpret_cast<uint2 *>(p.sf_dh + srow * 2 * I + I + col) = sb[1];
+      if constexpr (kWithA) *reinterpret_cast<uint2 *>(p.sf_a + srow * I + col) = sb[2];
+    }
+
+    // ---- pass 2: quantise the kept values, store
+#pragma unroll
+    for (int i = 0; i < kSgRows; ++i) {
+      const int64_t t = t0 + 16 * w + 8 * i + rs;
+      if (col_ok && t < p.T) {
+        const uint32_t og0 = quant4(make_float4(vg[i][0], vg[i][1], vg[i][2], vg[i][3]), mul);
+        const uint32_t og1 = quant4(make_float4(vg[i][4], vg[i][5], vg[i][6], vg[i][7]), mul + 4);
+        const uint32_t ou0 = quant4(make_float4(vu[i][0], vu[i][1], vu[i][2], vu[i][3]), mul + 8);
+        const uint32_t ou1 = quant4(make_float4(vu[i][4], vu[i][5], vu[i][6], vu[i][7]), mul + 12);
+        __stcs(reinterpret_cast<uint2 *>(p.q_dh + t * 2 * I + col), make_uint2(og0, og1));
+        __stcs(reinterpret_cast<uint2 *>(p.q_dh + t * 2 * I + I + col), make_uint2(ou0, ou1));
+        if constexpr (kWithA) {
+          const uint32_t oa0 = quant4(make_float4(va[i][0], va[i][1], va[i][2], va[i][3]), mul + 16);
+          const uint32_t oa1 = quant4(make_float4(va[i][4], va[i][5], va[i][6], va[i][7]), mul + 20);
+          __stcs(reinterpret_cast<uint2 *>(p.q_a + t * I + col), make_uint2(oa0, oa1));
+        }
+      }
     }
   }
+  // Leaving early (a wait ran out): let the copies in flight land (bounded).
+  if (tid == 0)
+    for (int k = it; k < issued; ++k)
+      if (!mbar_wait(&full[k % kSgStages], static_cast<uint32_t>(k / kSgStages) & 1u, abort_flag,
+                     drain_limit_ns(p.wait_limit_ns), p.status, 0x52, k, false))
+        break;
 }
 
 template <int kGran, bool kWithA>
-cudaError_t launch_sg(const SwigluArgs &p, cudaStream_t stream) {
+cudaError_t launch_sg(const SwigluArgs &p, int ctas, cudaStream_t stream) {
   // attribute set once per process (thread-safe static initialisation)
   static const cudaError_t setup = cudaFuncSetAttribute(
       swiglu_bwd_cast_kernel<kGran, kWithA>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSgSmem);
   if (setup != cudaSuccess) return setup;
-  const dim3 grid(static_cast<unsigned>((p.T + kSgT - 1) / kSgT),
-                  static_cast<unsigned>((p.I + kSgC - 1) / kSgC));
+  const int64_t tiles = static_cast<int64_t>(p.n_tt) * p.n_tc;
+  const int grid = static_cast<int>(tiles < ctas ? tiles : ctas);
   swiglu_bwd_cast_kernel<kGran, kWithA><<<grid, 256, kSgSmem, stream>>>(p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_swiglu_bwd_cast(const SwigluArgs &p, int gran_k, cudaStream_t stream) {
+cudaError_t launch_swiglu_bwd_cast(const SwigluArgs &p, int gran_k, int ctas, cudaStream_t stream) {
   const bool with_a = (p.q_a != nullptr);
   if (gran_k == 128)
-    return with_a ? launch_sg<128, true>(p, stream) : launch_sg<128, false>(p, stream);
-  return with_a ? launch_sg<32, true>(p, stream) : launch_sg<32, false>(p, stream);
+    return with_a ? launch_sg<128, true>(p, ctas, stream) : launch_sg<128, false>(p, ctas, stream);
+  return with_a ? launch_sg<32, true>(p, ctas, stream) : launch_sg<32, false>(p, ctas, stream);
 }
 
 }  // namespace dg

@@ -207,14 +207,18 @@ size_t moe_plan_scratch_bytes(int64_t n, int G);
 
 // SwiGLU backward fused with the column-block cast (swiglu.cu).
 struct SwigluArgs {
-  const void *h;        // BF16 [T, 2I] = [g | u]
-  const void *da;       // BF16 [T, I]
+  CUtensorMap tm_h;     // h as {2I, T} BF16, boxes of 32 channels x 128 tokens
+  CUtensorMap tm_da;    // da as {I, T} BF16, same boxes
   int64_t T;
   int I;
+  int n_tt, n_tc;       // tiles along tokens (128) and along channels of I (32)
   uint8_t *q_dh, *sf_dh;   // E4M3 [T, 2I], UE8M0 [T / gran_k, 2I]
   uint8_t *q_a, *sf_a;     // E4M3 [T, I], UE8M0 [T / gran_k, I], or null
+  DevStatus *status;       // bounded waits record DEV_TIMEOUT here
+  uint64_t wait_limit_ns;
 };
-cudaError_t launch_swiglu_bwd_cast(const SwigluArgs &p, int gran_k, cudaStream_t stream);
+// `ctas`: persistent CTAs (two per SM fit).
+cudaError_t launch_swiglu_bwd_cast(const SwigluArgs &p, int gran_k, int ctas, cudaStream_t stream);
 cudaError_t launch_moe_layout_plan(const MoePlanArgs &a, int sms, cudaStream_t stream);
 
 // Tile shape: a CTA pair covers 256 rows of M (128 per CTA) and block_n

@@ -72,6 +72,15 @@ def test_swiglu_random(T, I, gran_k):
     _check(h, da, gran_k)
 
 
+@pytest.mark.parametrize("T,I", [(160, 80), (32 * 37, 208)])
+def test_swiglu_ragged_token_tiles(T, I):
+    # gran_k 32: the last 128-token tile is partial (its rows past T arrive
+    # as zeros) and I is not a multiple of the 64-channel tile
+    h = workloads.randn((T, 2 * I), seed=T + 3 * I, dtype=torch.bfloat16)
+    da = workloads.randn((T, I), seed=T + 3 * I + 1, dtype=torch.bfloat16)
+    _check(h, da, 32)
+
+
 def test_swiglu_without_activation_output():
     h = workloads.randn((256, 512), seed=5, dtype=torch.bfloat16)
     da = workloads.randn((256, 256), seed=6, dtype=torch.bfloat16)
