@@ -474,8 +474,8 @@ __global__ void __launch_bounds__(256, 2) requant_tm_kernel(const CastArgs a) {
 }
 
 // BF16 rows gathered into the token-major MoE layout, brought in by TMA: one
-// CTA covers 128 output rows x 256 channels; its first thread issues 32
-// gather4 loads (four indexed rows of 512 bytes each) into a 64 KB shared
+// CTA covers 128 output rows x 256 channels; the lanes of its first warp
+// issue 32 gather4 loads (four indexed rows of 512 bytes each) into a 64 KB shared
 // tile, so that the whole tile is in flight at once without holding
 // registers (three CTAs per SM: 206 KB).  Padding rows (-1) load row 0, which
 // the passes below replace by zeros, so every gathered row is in bounds.
@@ -514,12 +514,11 @@ __global__ void __launch_bounds__(256, 3) gather_cast_kernel(const __grid_consta
     fence_mbar_init();
   }
   __syncthreads();
-  if (tid == 0) {
-    mbar_arrive_expect_tx(bar, kTileT * kTileC * 2);
-#pragma unroll 4
-    for (int j = 0; j < kTileT / 4; ++j)
-      tma_gather4_2d(tile + j * 4 * kTileC * 2, &a.tmx, bar, c0, max(idx[4 * j], 0),
-                     max(idx[4 * j + 1], 0), max(idx[4 * j + 2], 0), max(idx[4 * j + 3], 0));
+  if (w == 0) {   // each lane issues the gather4 of four rows: one warp instruction
+    if (l == 0) mbar_arrive_expect_tx(bar, kTileT * kTileC * 2);
+    __syncwarp();
+    tma_gather4_2d(tile + l * 4 * kTileC * 2, &a.tmx, bar, c0, max(idx[4 * l], 0),
+                   max(idx[4 * l + 1], 0), max(idx[4 * l + 2], 0), max(idx[4 * l + 3], 0));
   }
   if (!mbar_wait(bar, 0, abort_flag, a.wait_limit_ns, a.status, 0x41, blockIdx.x)) {
     // gave up: let the copies in flight land (bounded) before the CTA exits

@@ -118,6 +118,20 @@ def test_moe_layout_cast(src_kind, gran_k, layout):
     _assert_same(got, want)
 
 
+@pytest.mark.parametrize("T,C", [(160, 208), (32 * 45, 400)])
+def test_moe_layout_ragged_tiles(T, C):
+    # gran_k 32: the last 128-row tile is partial and C is not a multiple of
+    # the 128-channel tile; padding rows scattered through the layout
+    rng = np.random.default_rng(T + C)
+    T_src = 300
+    src = rng.integers(0, T_src, T).astype(np.int32)
+    src[rng.random(T) < 0.2] = -1
+    xb = workloads.randn((T_src, C), seed=T + C, dtype=torch.bfloat16)
+    got = _moe_gpu(xb, src, 32, "token")
+    want = oracle.moe_layout_cast(xb.float().numpy(), src, 32, "token")
+    _assert_same(got, want)
+
+
 def test_moe_layout_all_padding_and_empty_source():
     """A layout of padding rows only (T_src = 0) gives zero codes and the
     least scale byte."""
