@@ -86,7 +86,7 @@ def kernel_source_sha() -> str:
 
 
 def fp8_tiles(M: int, N: int) -> str:
-    """Tile widths of the token-major FP8 weight gradient for an M x N output:
+    """Tile widths of the FP8 weight gradient for an M x N output:
     the kernel's N is N, or M when its tiles are transposed (N % 224 != 0 and
     M % 224 == 0); a kernel N that is a multiple of 1792 (of 256 and of 224)
     runs mixed 256 / 224-column tiles unless DG_MIXED_TILES=0."""
@@ -765,7 +765,7 @@ def run_ours(args):
         step_nt()
     ms_nt = time_events(step_nt, max(5, args.steps // 4), stream)
     nt = {"ms_per_step": ms_nt, "value": flops / (ms_nt * 1e-3) / 1e12, "unit": "TFLOP/s",
-          "kernel": "kgrouped_wgrad_kernel<fp8, 224, f32, K-major>",
+          "kernel": f"kgrouped_wgrad_kernel<fp8, {fp8_tiles(w.M, w.N)}, f32, K-major>",
           "operands": "a [M, sum_k], b [N, sum_k] from the channel-major cast",
           "hbm_frac": alg / (ms_nt * 1e-3) / 1e9 / pk["hbm_gbs"],
           "tensor_frac": flops / (ms_nt * 1e-3) / 1e12 / fp8_peak}

@@ -350,8 +350,8 @@ void grouped_schedule(const GroupedArgs &x, int sms, WgradParams &p, PackParams 
   // Mixed tile widths are possible (see below): FP8, token-major operands,
   // kernel N a multiple of both 256 and 224.
   const int mix_pct_env = mixed_tiles_percent();
-  const bool mixable = x.fp8 && !x.kmajor && bn == kNarrowBN && Nk % kWideBN == 0 &&
-                       g.n_mma > 0 && mix_pct_env != 0;
+  const bool mixable = x.fp8 && bn == kNarrowBN && Nk % kWideBN == 0 && g.n_mma > 0 &&
+                       mix_pct_env != 0;
   p.chunk = !x.fp8                  ? kBf16Chunk
             : x.d_dtype == DG_BF16    ? (mixable ? kFp8ChunkBf16OutMixed : kFp8ChunkBf16Out)
             : (x.c == x.d)            ? kFp8ChunkInPlace
@@ -371,10 +371,11 @@ void grouped_schedule(const GroupedArgs &x, int sms, WgradParams &p, PackParams 
                : (x.c == x.d)         ? OUT_F32_REDUCE
                                       : OUT_F32_C;
   p.ks_dev = x.ks_dev;
-  // Mixed tile widths (FP8, token-major operands, kernel N a multiple of both
-  // 256 and 224): the longest entries are cut into 256-column tiles, which
-  // load 12.5 % fewer operand bytes per multiply-add than 224-column ones
-  // (B's 128-byte rows fill whole 32-byte sectors).  Only the first
+  // Mixed tile widths (FP8, kernel N a multiple of both 256 and 224): the
+  // longest entries are cut into 256-column tiles, which load fewer operand
+  // bytes per multiply-add than 224-column ones (12.5 % with token-major
+  // operands, whose 128-byte B rows then fill whole 32-byte sectors; 6.7 %
+  // with K-major ones).  Only the first
   // accumulator holds 256 columns, so only lane 0 takes wide tiles, and each
   // of its turns on them pairs with a narrow tile of lane 1: entries become
   // wide, longest first, while the narrow tiles left still cover the lane-0
@@ -432,6 +433,12 @@ dg_status grouped_maps(const GroupedArgs &x, const GroupedPlan &g, WgradParams &
       if ((s = encode(&p.tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, ka, 2, da, st, box,
                       CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "a")) ||
           (s = encode(&p.tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, kb, 2, db, st, boxb,
+                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "b")))
+        return s;
+      // mixed widths: the narrow tiles' B boxes
+      const uint32_t boxn[2] = {128, static_cast<uint32_t>(kNarrowBN / 2)};
+      if (bn == kWideBN &&
+          (s = encode(&p.tmBn, CU_TENSOR_MAP_DATA_TYPE_UINT8, kb, 2, db, st, boxn,
                       CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "b")))
         return s;
     } else if (x.fp8) {

@@ -7,6 +7,7 @@ namespace dg {
 cudaError_t launch_kgrouped_fp8_nt(const WgradParams &p, int block_n, int pairs,
                                    cudaStream_t stream) {
   switch (block_n) {
+    case 256: return launch_wgrad_bn<true, 256, true>(p, pairs, stream);
     case 224: return launch_wgrad_bn<true, 224, true>(p, pairs, stream);
     case 128: return launch_wgrad_bn<true, 128, true>(p, pairs, stream);
   }

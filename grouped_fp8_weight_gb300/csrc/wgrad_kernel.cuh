@@ -92,12 +92,11 @@ struct WgradCfg {
   static constexpr int THREADS = 32 * (3 + EPI_WARPS);
   static_assert(!kKMajor || kFP8, "K-major operands: FP8 only");
   static_assert(!kMG || kFP8, "M-grouped: FP8");
-  // Mixed tile widths (FP8 weight gradient, token-major operands, block_n
-  // 256): the first accumulator is 256 columns wide and takes the wide tiles
+  // Mixed tile widths (FP8 weight gradient, block_n 256): the first accumulator is 256 columns wide and takes the wide tiles
   // (the longest experts) and narrow ones; the second is BN1 = 224 wide and
   // takes narrow tiles only.  256 + 224 columns leave room for two scale
   // slots in tensor memory.
-  static constexpr bool kMixed = kFP8 && !kMG && !kKMajor && kBN == kWideBN;
+  static constexpr bool kMixed = kFP8 && !kMG && kBN == kWideBN;
   static_assert(!(kFP8 && kBN == kWideBN) || kMixed, "FP8 block_n 256: mixed widths only");
   static constexpr int BN1 = kMixed ? kNarrowBN : kBN;   // second accumulator's width
   // Operand majorness: kKMajor makes both operands K-major (NT weight
@@ -139,7 +138,9 @@ struct WgradCfg {
   // never steps along M/N, so its LBO is set to the K-group stride as well.
   static constexpr int A_LBO = A_ATOMS > 1 ? ATOM_BYTES : 1024;
   static constexpr int B_LBO = B_ATOMS > 1 ? ATOM_BYTES : 1024;
-  static constexpr int STAGES = (A_KM && B_KM) ? 6 : 5;   // all-K-major stages are 30 KB, others 32 KB
+  // all-K-major 224-wide stages are 30 KB, others 32 KB (with mixed widths
+  // the K-major B stage holds 128 rows)
+  static constexpr int STAGES = (A_KM && B_KM && !kMixed) ? 6 : 5;
   static constexpr int NUM_ACC = 2;
   // FP8 scale groups: four UE8M0 rows (four k-blocks at gran_k 128, the four
   // 32-token sub-blocks of one k-block at gran_k 32), in a ring of SF_SLOTS.
@@ -541,7 +542,7 @@ __global__ void __launch_bounds__((WgradCfg<kFP8, kBN, kKMajor, kMG, kTransD>::T
               // the weight stored [G N, K]: K from 0, rows from the expert's first (k_off = e N)
               tma_load_2d_pair(sb, &p.tmB, fbar, ka, nb + tc.k_off, keep);
             } else if constexpr (Cfg::B_KM) {
-              tma_load_2d_pair(sb, &p.tmB, fbar, k, nb, keep);
+              tma_load_2d_pair(sb, tmb, fbar, k, nb, keep);
             } else {
 #pragma unroll
               for (int b = 0; b < Cfg::B_ATOMS; ++b)
@@ -576,11 +577,12 @@ __global__ void __launch_bounds__((WgradCfg<kFP8, kBN, kKMajor, kMG, kTransD>::T
       uint32_t sfa_t = 0, sfb_t = 0;
       bool ok = true;
       // A K-major operand clears its transpose bit (15: A, 16: B).
+      constexpr uint32_t kKMajorMask = (Cfg::A_KM ? ~(1u << 15) : ~0u) & (Cfg::B_KM ? ~(1u << 16) : ~0u);
       constexpr uint32_t kIdescBase =
-          (kFP8 ? idesc_mxf8(2 * Cfg::BM, kBN, 0, 0) : idesc_bf16(2 * Cfg::BM, kBN)) &
-          (Cfg::A_KM ? ~(1u << 15) : ~0u) & (Cfg::B_KM ? ~(1u << 16) : ~0u);
+          (kFP8 ? idesc_mxf8(2 * Cfg::BM, kBN, 0, 0) : idesc_bf16(2 * Cfg::BM, kBN)) & kKMajorMask;
       // mixed widths: the narrow tiles' MMAs (N = BN1)
-      constexpr uint32_t kIdescNarrow = kFP8 ? idesc_mxf8(2 * Cfg::BM, Cfg::BN1, 0, 0) : kIdescBase;
+      constexpr uint32_t kIdescNarrow =
+          kFP8 ? (idesc_mxf8(2 * Cfg::BM, Cfg::BN1, 0, 0) & kKMajorMask) : kIdescBase;
       uint32_t ig = 0;             // scale groups issued
       int ts = 0;                  // tensor-memory slot of the next group (ig mod SF_TSLOTS)
       int n_st = 0;                // stages issued (stage n_st uses `empty[n_st % S]`, phase n_st / S)

@@ -19,6 +19,7 @@ import torch
 from grouped_fp8_weight_gb300 import workloads
 import oracle
 from tests.gpu_helpers import DEV, assert_close, fp8_operands, run_fp8
+from tests.test_gpu_wgrad_nt import run_nt
 
 pytestmark = pytest.mark.gpu
 
@@ -35,15 +36,16 @@ def _case(ks, M, N, seed, gran_k=128):
     return qa, sa, qb, sb
 
 
-def _run_logged(monkeypatch, capfd, mixed, *args, **kw):
-    """run_fp8 with DG_LOG on; returns (D, number of wide entries in the plan)."""
+def _run_logged(monkeypatch, capfd, mixed, *args, run=run_fp8, **kw):
+    """run_fp8 (or run_nt) with DG_LOG on; returns (D, number of wide entries
+    in the plan)."""
     monkeypatch.setenv("DG_LOG", "1")
     if mixed is None:
         monkeypatch.delenv("DG_MIXED_TILES", raising=False)
     else:
         monkeypatch.setenv("DG_MIXED_TILES", str(mixed))
     capfd.readouterr()
-    d = run_fp8(*args, **kw)
+    d = run(*args, **kw)
     err = capfd.readouterr().err
     m = _PLAN.findall(err)
     assert m, f"no plan line in {err!r}"
@@ -113,3 +115,36 @@ def test_mixed_many_tiles_per_pair(monkeypatch, capfd, gran_k):
     for e, (De, Se) in part.items():
         assert_close(dr[e], De, Se, what=f"expert {e} (K = {ks[e]})")
     assert torch.count_nonzero(d[3]).item() == 0
+
+
+@pytest.mark.parametrize("gran_k", [128, 32])
+@pytest.mark.parametrize("out,c_mode", [("f32", "none"), ("f32", "inplace"), ("bf16", "none")])
+def test_mixed_k_major(monkeypatch, capfd, gran_k, out, c_mode):
+    # K-major (NT) operands a [M, sum_k], b [N, sum_k]: the same widths
+    ks = [128 * 12, 128 * 6, 0, 256, 128]
+    M, N = 256, 1792
+    qa, sa, qb, sb = _case(ks, M, N, 49, gran_k)
+    C = workloads.randn((len(ks), M, N), 50).numpy()
+    c = C if c_mode != "none" else None
+    D, S = oracle.kgrouped_fp8_wgrad(qa, sa, qb, sb, ks, gran_k, c)
+    d, n_wide = _run_logged(monkeypatch, capfd, None, qa, sa, qb, sb, ks, gran_k, out, c, c_mode,
+                            run=run_nt)
+    assert n_wide > 0
+    assert_close(d, D, S, out, what=f"K-major {out}/{c_mode}/g{gran_k}")
+    if c_mode == "inplace":
+        assert torch.equal(d[2].cpu(), torch.from_numpy(C[2]))
+
+
+def test_mixed_k_major_transposed_many_tiles(monkeypatch, capfd):
+    # D^T tiles on K-major operands (M = 3584 along the tiles' widths), several
+    # wide and narrow tiles per CTA pair; sampled rows x all N
+    ks = [128 * 40, 128 * 17, 128 * 5, 0, 128 * 2, 128]
+    M, N = 3584, 512
+    qa, sa, qb, sb = _case(ks, M, N, 51)
+    d, n_wide = _run_logged(monkeypatch, capfd, None, qa, sa, qb, sb, ks, 128, run=run_nt)
+    assert n_wide > 0
+    rows = np.sort(np.random.default_rng(51).choice(M, 16, replace=False))
+    part = oracle.kgrouped_fp8_wgrad_rows(qa, sa, qb, sb, ks, rows, 128)
+    dr = d[:, torch.from_numpy(rows).to(DEV)].double().cpu().numpy()
+    for e, (De, Se) in part.items():
+        assert_close(dr[e], De, Se, what=f"K-major transposed expert {e}")
