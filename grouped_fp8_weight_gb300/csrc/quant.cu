@@ -358,15 +358,22 @@ __global__ void __launch_bounds__(256, 2) cast_colblock_kernel(const CastArgs a)
 // with 16-byte loads, so that two CTAs per SM keep as many bytes in flight as
 // the BF16 cast does.  A thread's 16 channels lie in one 128-channel tile of
 // the source scales.  After the maxima the codes wait in shared memory (64 KB)
-// instead of registers, and the quantise pass streams them row by row.
+// instead of registers, and the quantise pass streams them row by row.  Each
+// block scale is computed once per column (not by every thread of its
+// column group) into shared memory.
 constexpr int kRqTileC = 512;
-constexpr int kRqSmem = kTileT * kRqTileC + 8 * 32 * 64;   // codes + per-warp maxima
+constexpr int kRqRed = 8 * kRqTileC * 4;                   // per-warp column maxima
+constexpr int kRqScales = 4 * kRqTileC * 5;                // factors and bytes, up to 4 blocks
+constexpr int kRqSmem = kTileT * kRqTileC + kRqRed + kRqScales;
 
 template <int kGran, bool kGather>
 __global__ void __launch_bounds__(256, 2) requant_tm_kernel(const CastArgs a) {
   extern __shared__ __align__(16) uint8_t rq_smem[];
   uint4 *tile = reinterpret_cast<uint4 *>(rq_smem);                         // [128][32] x 16 B
   uint4 (*red)[32][4] = reinterpret_cast<uint4 (*)[32][4]>(rq_smem + kTileT * kRqTileC);
+  const float *red_f = reinterpret_cast<const float *>(rq_smem + kTileT * kRqTileC);   // [8][512]
+  float *maS = reinterpret_cast<float *>(rq_smem + kTileT * kRqTileC + kRqRed);         // [blocks][512]
+  uint8_t *sbS = rq_smem + kTileT * kRqTileC + kRqRed + 4 * kRqTileC * 4;               // [blocks][512]
   const int w = threadIdx.x >> 5;
   const int l = threadIdx.x & 31;
   const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kTileT;
@@ -411,33 +418,40 @@ __global__ void __launch_bounds__(256, 2) requant_tm_kernel(const CastArgs a) {
                               __float_as_uint(fm[4 * j + 2]), __float_as_uint(fm[4 * j + 3]));
   __syncthreads();
 
-  // Block maxima (float bit patterns of non-negative values: integer maxima).
+  // Block maxima (float bit patterns of non-negative values: integer maxima),
+  // one (token block, column) per item: its factor 2^min(8 - e, 127) and its
+  // scale byte e + 127.
   constexpr int kWarps = (kGran == 128) ? 8 : 2;
-  const int w0 = (kGran == 128) ? 0 : (w & ~1);
+  constexpr int kBlocks = kTileT / kGran;
+  constexpr int kItems = kBlocks * kRqTileC;
+#pragma unroll
+  for (int it = threadIdx.x; it < kItems; it += 256) {
+    const int bb = it / kRqTileC, c = it % kRqTileC;
+    uint32_t m = 0;
+#pragma unroll
+    for (int ww = 0; ww < kWarps; ++ww)
+      m = max(m, __float_as_uint(red_f[(bb * kWarps + ww) * kRqTileC + c]));
+    const int e = scale_exp_from_f32_shifted(m);
+    maS[it] = __uint_as_float(static_cast<uint32_t>(min(8 - e, 127) + 127) << 23);
+    sbS[it] = static_cast<uint8_t>(e + 127);
+  }
+  __syncthreads();
+  const int blk = (16 * w) / kGran;
   float ma[16];
-  uint32_t sfw[4] = {0, 0, 0, 0};
-  bool big = false;
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
-    uint4 r = red[w0][l][j];
-#pragma unroll
-    for (int ww = 1; ww < kWarps; ++ww) {
-      const uint4 o = red[w0 + ww][l][j];
-      r.x = max(r.x, o.x);
-      r.y = max(r.y, o.y);
-      r.z = max(r.z, o.z);
-      r.w = max(r.w, o.w);
-    }
-    const uint32_t ab[4] = {r.x, r.y, r.z, r.w};
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int e = scale_exp_from_f32_shifted(ab[u]);
-      const int sh = 8 - e;
-      ma[4 * j + u] = __uint_as_float(static_cast<uint32_t>(min(sh, 127) + 127) << 23);
-      big |= sh > 127;
-      sfw[j] |= static_cast<uint32_t>(e + 127) << (8 * u);
-    }
+    const float4 f = *reinterpret_cast<const float4 *>(maS + blk * kRqTileC + 16 * l + 4 * j);
+    ma[4 * j] = f.x;
+    ma[4 * j + 1] = f.y;
+    ma[4 * j + 2] = f.z;
+    ma[4 * j + 3] = f.w;
   }
+  const uint4 sb4 = *reinterpret_cast<const uint4 *>(sbS + blk * kRqTileC + 16 * l);
+  const uint32_t sfw[4] = {sb4.x, sb4.y, sb4.z, sb4.w};
+  // a column whose factor 2^(8 - e) needs more than 2^127 (scale byte below 8)
+  bool big = false;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) big |= ((sfw[j] - 0x08080808u) & ~sfw[j] & 0x80808080u) != 0;
   if (col_ok) {
     if constexpr (kGran == 128) {
       if (w == 0)

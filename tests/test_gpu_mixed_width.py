@@ -148,3 +148,23 @@ def test_mixed_k_major_transposed_many_tiles(monkeypatch, capfd):
     dr = d[:, torch.from_numpy(rows).to(DEV)].double().cpu().numpy()
     for e, (De, Se) in part.items():
         assert_close(dr[e], De, Se, what=f"K-major transposed expert {e}")
+
+
+def test_mixed_many_experts_schedule_from_parameters(monkeypatch, capfd):
+    """More schedule entries than shared memory holds (330 experts, 256 kept
+    there): wide and narrow tiles with the schedule read from the kernel
+    parameters, in place, every expert against the oracle."""
+    rng = np.random.default_rng(53)
+    ks = [128 * int(k) for k in rng.choice([0, 1, 1, 2, 2, 3], size=330)]
+    for e in rng.choice(330, size=8, replace=False):
+        ks[int(e)] = 128 * int(rng.integers(12, 33))
+    M, N = 128, 1792
+    qa, sa, qb, sb = _case(ks, M, N, 53)
+    C = workloads.randn((len(ks), M, N), 54).numpy()
+    D, S = oracle.kgrouped_fp8_wgrad(qa, sa, qb, sb, ks, 128, C)
+    d, n_wide = _run_logged(monkeypatch, capfd, None, qa, sa, qb, sb, ks, 128, "f32", C, "inplace")
+    assert n_wide > 0
+    assert_close(d, D, S, what="330 experts, mixed widths, in place")
+    for e, k in enumerate(ks):
+        if k == 0:
+            assert torch.equal(d[e].cpu(), torch.from_numpy(C[e]))
