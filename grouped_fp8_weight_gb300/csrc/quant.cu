@@ -495,7 +495,8 @@ __global__ void __launch_bounds__(256, 2) requant_tm_kernel(const CastArgs a) {
 // the passes below replace by zeros, so every gathered row is in bounds.
 // Then the column-block cast as above, reading the tile twice (maxima, then
 // quantise and store), one 16-byte row chunk at a time.
-constexpr int kGtSmem = kTileT * kTileC * 2 + kTileT * 4 + 8 * 32 * 16 + 16;
+constexpr int kGtScales = 4 * kTileC * 5;   // factors and scale bytes of up to four token blocks
+constexpr int kGtSmem = kTileT * kTileC * 2 + kTileT * 4 + 8 * 32 * 16 + kGtScales + 16;
 
 template <int kGran>
 __global__ void __launch_bounds__(256, 3) gather_cast_kernel(const __grid_constant__ CastArgs a) {
@@ -503,7 +504,10 @@ __global__ void __launch_bounds__(256, 3) gather_cast_kernel(const __grid_consta
   uint8_t *tile = gt_smem;                                                 // [128][512 B]
   int *idx = reinterpret_cast<int *>(gt_smem + kTileT * kTileC * 2);       // [128]
   uint4 *red = reinterpret_cast<uint4 *>(gt_smem + kTileT * kTileC * 2 + kTileT * 4);   // [8][32]
-  uint64_t *bar = reinterpret_cast<uint64_t *>(gt_smem + kTileT * kTileC * 2 + kTileT * 4 + 8 * 32 * 16);
+  float *mulS = reinterpret_cast<float *>(gt_smem + kTileT * kTileC * 2 + kTileT * 4 + 8 * 32 * 16);
+  uint8_t *sbS = reinterpret_cast<uint8_t *>(mulS + 4 * kTileC);
+  uint64_t *bar = reinterpret_cast<uint64_t *>(gt_smem + kTileT * kTileC * 2 + kTileT * 4 + 8 * 32 * 16 +
+                                               kGtScales);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(bar + 1);
   const int tid = threadIdx.x;
   const int w = tid >> 5, l = tid & 31;
@@ -554,29 +558,32 @@ __global__ void __launch_bounds__(256, 3) gather_cast_kernel(const __grid_consta
   }
   red[w * 32 + l] = make_uint4(m[0], m[1], m[2], m[3]);
   __syncthreads();
+  // one scale per (token block, column), computed once: its factor 2^-e and
+  // its byte e + 127 (red as [warp][column] 16-bit maxima)
   constexpr int kWarps = (kGran == 128) ? 8 : 2;
-  const int w0 = (kGran == 128) ? 0 : (w & ~1);
-  uint4 r = red[w0 * 32 + l];
+  constexpr int kItems = (kTileT / kGran) * kTileC;
+  const uint16_t *red16 = reinterpret_cast<const uint16_t *>(red);
 #pragma unroll
-  for (int ww = 1; ww < kWarps; ++ww) {
-    const uint4 o = red[(w0 + ww) * 32 + l];
-    r.x = __vmaxu2(r.x, o.x);
-    r.y = __vmaxu2(r.y, o.y);
-    r.z = __vmaxu2(r.z, o.z);
-    r.w = __vmaxu2(r.w, o.w);
+  for (int it = tid; it < kItems; it += 256) {
+    const int bb = it / kTileC, c = it % kTileC;
+    uint32_t mx = 0;
+#pragma unroll
+    for (int ww = 0; ww < kWarps; ++ww) mx = max(mx, static_cast<uint32_t>(red16[(bb * kWarps + ww) * kTileC + c]));
+    const int e = scale_exp_from_bf16(mx);
+    mulS[it] = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+    sbS[it] = static_cast<uint8_t>(e + 127);
   }
-  const uint32_t aw[4] = {r.x, r.y, r.z, r.w};
+  __syncthreads();
+  const int blk = (16 * w) / kGran;
   float mul[8];
-  uint32_t sfw[2] = {0, 0};
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int e = scale_exp_from_bf16((aw[k] >> (16 * h)) & 0xFFFFu);
-      mul[2 * k + h] = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
-      sfw[k >> 1] |= static_cast<uint32_t>(e + 127) << (8 * (2 * (k & 1) + h));
-    }
+  {
+    const float4 f0 = *reinterpret_cast<const float4 *>(mulS + blk * kTileC + 8 * l);
+    const float4 f1 = *reinterpret_cast<const float4 *>(mulS + blk * kTileC + 8 * l + 4);
+    mul[0] = f0.x; mul[1] = f0.y; mul[2] = f0.z; mul[3] = f0.w;
+    mul[4] = f1.x; mul[5] = f1.y; mul[6] = f1.z; mul[7] = f1.w;
   }
+  const uint2 sb2 = *reinterpret_cast<const uint2 *>(sbS + blk * kTileC + 8 * l);
+  const uint32_t sfw[2] = {sb2.x, sb2.y};
   if (col_ok) {
     if constexpr (kGran == 128) {
       if (w == 0)
