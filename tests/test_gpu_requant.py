@@ -73,6 +73,30 @@ def test_requant_scale_extremes(gran_k, layout):
                  oracle.requant_colblock(q_in, sf_in, gran_k, layout))
 
 
+@pytest.mark.parametrize("layout", ["token", "channel"])
+@pytest.mark.parametrize("gran_k", [128, 32])
+def test_requant_row_scale_spread(gran_k, layout):
+    """One row per 128-token block with a scale byte above the rest (by 15 to
+    26) and zero codes in some channels: there the block maximum comes from
+    rows whose dequantised values, relative to that row's scale, fall to the
+    subnormal range or below it, and in the third block small codes put every
+    such product below 2^-14."""
+    rng = np.random.default_rng(23)
+    T, C = 512, 512
+    q_in = rng.integers(0, 256, size=(T, C)).astype(np.uint8)
+    q_in[(q_in & 0x7F) == 0x7F] = 0x7E                       # no NaN codes
+    sf_in = np.zeros((T, C // 128), dtype=np.uint8)
+    for blk, spread in enumerate((13, 16, 20, 24)):
+        rows = slice(128 * blk, 128 * blk + 128)
+        sf_in[rows, :] = 140 - spread
+        sf_in[128 * blk + 7, :] = 142                        # one row above the rest
+        q_in[128 * blk + 7, : 32 * (blk + 1)] = 0            # ... with zeros in some channels
+    q_in[256:384, :64] = rng.integers(1, 0x30, size=(128, 64)).astype(np.uint8)   # |x| < 0.5
+    q_in[256 + 7, :64] = 0
+    _assert_same(_requant_gpu(q_in, sf_in, gran_k, layout),
+                 oracle.requant_colblock(q_in, sf_in, gran_k, layout))
+
+
 def _moe_src(T_tok, G, topk, seed):
     """An MoE layout from random top-k routing: each expert's (token, slot)
     pairs in token order, padded with -1 to a multiple of 128."""
