@@ -491,7 +491,7 @@ __global__ void __launch_bounds__(256, 2) requant_tm_kernel(const CastArgs a) {
 // CTA covers 128 output rows x 256 channels; the lanes of its first warp
 // issue 32 gather4 loads (four indexed rows of 512 bytes each) into a 64 KB shared
 // tile, so that the whole tile is in flight at once without holding
-// registers (three CTAs per SM: 206 KB).  Padding rows (-1) load row 0, which
+// registers (three CTAs per SM: 220.5 KB).  Padding rows (-1) load row 0, which
 // the passes below replace by zeros, so every gathered row is in bounds.
 // Then the column-block cast as above, reading the tile twice (maxima, then
 // quantise and store), one 16-byte row chunk at a time.
