@@ -536,7 +536,7 @@ def fp8_peak_for(dev, pk):
                 "source": f"assumed 2 x measured BF16 burst (FP8 measurement failed: {exc})"}
 
 
-def cpu_oracle_sample(w, ks, qa, sa, qb, sb, n_rows=16):
+def cpu_oracle_sample(w, ks, qa, sa, qb, sb, n_rows=1024):
     """Time the float64 oracle on all experts x n_rows seeded rows of M x all N."""
     import oracle
     rows = np.sort(np.random.default_rng(w.seed).choice(w.M, n_rows, replace=False))
