@@ -580,14 +580,14 @@ def job_throughput(flops_per_replica: float, ws: int, ms_max: float) -> float:
 
 def run_reference(args):
     """Reference arm: the CPU oracle, timed on a bounded sample of the workload
-    per step (all experts x 8 seeded rows of M x 64 seeded columns of N)."""
+    per step (all experts x 32 seeded rows of M x 256 seeded columns of N)."""
     ws, rank, _ = dist_env()
     if rank != 0:
         return 0
     w = workloads.WORKLOADS[args.workload]
     import oracle
     ks = workloads.counts_for(w.name)
-    n_rows, n_cols = 8, 64
+    n_rows, n_cols = 32, 256
     gen = torch.Generator().manual_seed(w.seed)
     # Operands: N(0, 1) columns quantised by the oracle itself (columns are
     # independent, so the sampled columns are exactly the workload's columns).
