@@ -496,6 +496,21 @@ __global__ void __launch_bounds__(256, 2) requant_tm_kernel(const CastArgs a) {
 // Then the column-block cast as above, reading the tile twice (maxima, then
 // quantise and store), one 16-byte row chunk at a time.
 constexpr int kGtScales = 4 * kTileC * 5;   // factors and scale bytes of up to four token blocks
+constexpr int kGtTmaWarps = 2;              // warps whose rows come by TMA (the rest by cp.async)
+
+// 16-byte asynchronous copy global -> shared through the load path
+// (src_bytes 0: 16 zero bytes), its commit, and the wait for all of them.
+__device__ __forceinline__ void cp_async16(void *dst, const void *src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
+               "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
+}
 constexpr int kGtSmem = kTileT * kTileC * 2 + kTileT * 4 + 8 * 32 * 16 + kGtScales + 16;
 
 template <int kGran>
@@ -532,17 +547,40 @@ __global__ void __launch_bounds__(256, 3) gather_cast_kernel(const __grid_consta
     fence_mbar_init();
   }
   __syncthreads();
-  if (w == 0) {   // each lane issues the gather4 of four rows: one warp instruction
-    if (l == 0) mbar_arrive_expect_tx(bar, kTileT * kTileC * 2);
+  // The rows of the first kGtTmaWarps warps come by TMA (lanes of warp 0
+  // issue one gather4 of four rows each, all on the tile's barrier); every
+  // other warp copies its own 16 rows through the load path (16 bytes per lane
+  // and row, channels past C filled with zeros), so that both copy engines
+  // of the SM bring the tile in.
+  if (kGtTmaWarps > 0 && w == 0) {
+    if (l == 0) mbar_arrive_expect_tx(bar, kGtTmaWarps * 16 * kTileC * 2);
     __syncwarp();
-    tma_gather4_2d(tile + l * 4 * kTileC * 2, &a.tmx, bar, c0, max(idx[4 * l], 0),
-                   max(idx[4 * l + 1], 0), max(idx[4 * l + 2], 0), max(idx[4 * l + 3], 0));
+    if (l < kGtTmaWarps * 4)
+      tma_gather4_2d(tile + l * 4 * kTileC * 2, &a.tmx, bar, c0, max(idx[4 * l], 0),
+                     max(idx[4 * l + 1], 0), max(idx[4 * l + 2], 0), max(idx[4 * l + 3], 0));
   }
-  if (!mbar_wait(bar, 0, abort_flag, a.wait_limit_ns, a.status, 0x41, blockIdx.x)) {
+  if (w >= kGtTmaWarps) {
+    const uint16_t *x = static_cast<const uint16_t *>(a.x);
+    const bool in = col < C;
+#pragma unroll 4
+    for (int i = 0; i < 16; ++i) {
+      const int r = 16 * w + i;
+      const uint16_t *src = x + static_cast<int64_t>(max(idx[r], 0)) * C + (in ? col : 0);
+      cp_async16(tile + r * (kTileC * 2) + l * 16, src, in ? 16u : 0u);
+    }
+    cp_async_commit();
+  }
+  if (kGtTmaWarps > 0 &&
+      !mbar_wait(bar, 0, abort_flag, a.wait_limit_ns, a.status, 0x41, blockIdx.x)) {
     // gave up: let the copies in flight land (bounded) before the CTA exits
     mbar_wait(bar, 0, abort_flag, drain_limit_ns(a.wait_limit_ns), a.status, 0x42, blockIdx.x,
               false);
+    if (w >= kGtTmaWarps) cp_async_wait_all();
     return;
+  }
+  if (w >= kGtTmaWarps) {
+    cp_async_wait_all();
+    __syncwarp();   // every lane's rows are visible to the warp
   }
 
   // ---- pass 1: packed 16-bit maxima of |x| over this thread's 16 rows
