@@ -487,11 +487,14 @@ __global__ void __launch_bounds__(256, 2) requant_tm_kernel(const CastArgs a) {
   }
 }
 
-// BF16 rows gathered into the token-major MoE layout, brought in by TMA: one
-// CTA covers 128 output rows x 256 channels; the lanes of its first warp
-// issue 32 gather4 loads (four indexed rows of 512 bytes each) into a 64 KB shared
-// tile, so that the whole tile is in flight at once without holding
-// registers (three CTAs per SM: 220.5 KB).  Padding rows (-1) load row 0, which
+// BF16 rows gathered into the token-major MoE layout: one CTA covers 128
+// output rows x 256 channels, staged whole in a 64 KB shared tile so that it
+// is in flight at once without holding registers (three CTAs per SM: 220.5
+// KB).  The rows of the first kGtTmaWarps warps come by TMA (lanes of warp 0
+// issue gather4 loads of four indexed rows of 512 bytes each); every other
+// warp copies its own rows with 16-byte cp.async through the load path, so
+// that both of the SM's copy engines work on the tile (a quarter by TMA
+// measured fastest but for within 1 %).  Padding rows (-1) load row 0, which
 // the passes below replace by zeros, so every gathered row is in bounds.
 // Then the column-block cast as above, reading the tile twice (maxima, then
 // quantise and store), one 16-byte row chunk at a time.
