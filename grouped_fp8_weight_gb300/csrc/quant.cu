@@ -493,9 +493,10 @@ __global__ void __launch_bounds__(256, 2) requant_tm_kernel(const CastArgs a) {
 // KB).  The rows of the first kGtTmaWarps warps come by TMA (lanes of warp 0
 // issue gather4 loads of four indexed rows of 512 bytes each); every other
 // warp copies its own rows with 16-byte cp.async through the load path, so
-// that both of the SM's copy engines work on the tile (a quarter by TMA
-// measured fastest but for within 1 %).  Padding rows (-1) load row 0, which
-// the passes below replace by zeros, so every gathered row is in bounds.
+// that both of the SM's copy engines work on the tile (two warps of eight
+// by TMA measured within 1 % of the fastest split).  Padding rows (-1) load
+// row 0, which the passes below replace by zeros, so every gathered row is in
+// bounds.
 // Then the column-block cast as above, reading the tile twice (maxima, then
 // quantise and store), one 16-byte row chunk at a time.
 constexpr int kGtScales = 4 * kTileC * 5;   // factors and scale bytes of up to four token blocks
