@@ -261,7 +261,7 @@ def measure_casts(w, ks, dev, stream, pk, steps):
     against the HBM roofline: re-quantising stored FP8 (1 x 128 tiles, random
     codes and scale bytes) of dY [sum_k, M] and X [sum_k, N]; the BF16 cast of
     X fused with the MoE layout (each expert's rows gathered from sum_k / 2
-    tokens); and the SwiGLU backward fused with the cast of dh [sum_k, M] and
+    tokens), and the same from stored E4M3 rows; and the SwiGLU backward fused with the cast of dh [sum_k, M] and
     of the activation [sum_k, M / 2]."""
     import grouped_fp8_weight_gb300 as dg
     gen = torch.Generator(device=dev).manual_seed(w.seed + 100)
@@ -306,13 +306,38 @@ def measure_casts(w, ks, dev, stream, pk, steps):
     # each distinct source row read once (a row gathered into several experts'
     # slices is re-read from L2), each output row written once
     nb = uniq * w.N * 2 + w.sum_k * w.N + w.sum_k * 4 + (w.sum_k // 128) * w.N
-    out["moe_layout"] = {"ms": ms, "kernel": "gather_cast_kernel<128> (TMA gather4 rows, token-major)",
+    out["moe_layout"] = {"ms": ms, "kernel": "gather_cast_kernel<128> (rows by TMA gather4 and cp.async, token-major)",
                          "launches_per_step": 1, "source_tokens": t_tok, "rows": w.sum_k,
                          "distinct_source_rows": uniq,
                          "bound": "hbm", "achieved": nb / (ms * 1e-3) / 1e9,
                          "peak": pk["hbm_gbs"], "unit": "GB/s",
                          "frac": nb / (ms * 1e-3) / 1e9 / pk["hbm_gbs"], "algorithmic_bytes": nb}
-    del x, q, sf, src
+    del x
+
+    # the same layout from stored E4M3 rows with their 1 x 128 scales
+    # (re-quantised while gathered)
+    x8 = torch.randint(0, 256, (t_tok, w.N), generator=gen, device=dev, dtype=torch.uint8)
+    x8[(x8 & 0x7F) == 0x7F] = 0x7E
+    x8_sf = torch.randint(110, 140, (t_tok, w.N // 128), generator=gen, device=dev,
+                          dtype=torch.uint8)
+
+    def layout_requant():
+        dg.dg_quant_moe_layout_fp8(x8, src, q, sf, x8_sf)
+
+    for _ in range(3):
+        layout_requant()
+    ms = time_events(layout_requant, steps, stream)
+    nb = (uniq * (w.N + w.N // 128) + w.sum_k * w.N + w.sum_k * 4 +
+          (w.sum_k // 128) * w.N)
+    out["moe_layout_fp8"] = {"ms": ms,
+                             "kernel": "requant_tm_kernel<128, gather> (e4m3 1x128 source rows, token-major)",
+                             "launches_per_step": 1, "source_tokens": t_tok, "rows": w.sum_k,
+                             "distinct_source_rows": uniq,
+                             "bound": "hbm", "achieved": nb / (ms * 1e-3) / 1e9,
+                             "peak": pk["hbm_gbs"], "unit": "GB/s",
+                             "frac": nb / (ms * 1e-3) / 1e9 / pk["hbm_gbs"],
+                             "algorithmic_bytes": nb}
+    del x8, x8_sf, q, sf, src
 
     # SwiGLU backward fused with the cast: h = [g | u] [sum_k, M] and da
     # [sum_k, M/2] (BF16) -> dh = [dg | du] (the A operand, [sum_k, M]) and the

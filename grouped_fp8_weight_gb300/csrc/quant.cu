@@ -364,7 +364,7 @@ __global__ void __launch_bounds__(256, 2) cast_colblock_kernel(const CastArgs a)
 constexpr int kRqTileC = 512;
 constexpr int kRqRed = 8 * kRqTileC * 4;                   // per-warp column maxima
 constexpr int kRqScales = 4 * kRqTileC * 5;                // factors and bytes, up to 4 blocks
-constexpr int kRqSmem = kTileT * kRqTileC + kRqRed + kRqScales;
+constexpr int kRqSmem = kTileT * kRqTileC + kRqRed + kRqScales + kTileT * 4;   // + source rows
 
 template <int kGran, bool kGather>
 __global__ void __launch_bounds__(256, 2) requant_tm_kernel(const CastArgs a) {
@@ -374,6 +374,7 @@ __global__ void __launch_bounds__(256, 2) requant_tm_kernel(const CastArgs a) {
   const float *red_f = reinterpret_cast<const float *>(rq_smem + kTileT * kRqTileC);   // [8][512]
   float *maS = reinterpret_cast<float *>(rq_smem + kTileT * kRqTileC + kRqRed);         // [blocks][512]
   uint8_t *sbS = rq_smem + kTileT * kRqTileC + kRqRed + 4 * kRqTileC * 4;               // [blocks][512]
+  int *rows_s = reinterpret_cast<int *>(rq_smem + kTileT * kRqTileC + kRqRed + kRqScales);   // [128]
   const int w = threadIdx.x >> 5;
   const int l = threadIdx.x & 31;
   const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kTileT;
@@ -382,6 +383,21 @@ __global__ void __launch_bounds__(256, 2) requant_tm_kernel(const CastArgs a) {
   const bool col_ok = col < C;
   const uint8_t *x = static_cast<const uint8_t *>(a.x);
   const int tiles = C / 128;
+  // Gather: the tile's 128 source rows, read and checked once (an entry
+  // outside [-1, T_src) is recorded and read as a row of zeros), so that
+  // every thread's code loads can be issued together.
+  if constexpr (kGather) {
+    if (threadIdx.x < kTileT) {
+      const int64_t t = t0 + threadIdx.x;
+      int s = t < a.T ? __ldg(a.src_rows + t) : -1;
+      if (s < -1 || s >= a.T_src) {
+        atomicCAS(&a.status->code, DEV_OK, DEV_BAD_ROW);
+        s = -1;
+      }
+      rows_s[threadIdx.x] = s;
+    }
+    __syncthreads();
+  }
 
   uint32_t sbw[4] = {0, 0, 0, 0};   // scale byte of row i in byte i % 4 of word i / 4
   float fm[16];
@@ -392,7 +408,11 @@ __global__ void __launch_bounds__(256, 2) requant_tm_kernel(const CastArgs a) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       const int64_t t = t0 + 16 * w + i;
-      const int64_t r = source_row<kGather>(a, t, col_ok && t < a.T, l);
+      int64_t r;
+      if constexpr (kGather)
+        r = col_ok ? rows_s[16 * w + i] : -1;
+      else
+        r = (col_ok && t < a.T) ? t : -1;
       v[i] = r >= 0 ? __ldcs(reinterpret_cast<const uint4 *>(x + r * C + col))
                     : make_uint4(0, 0, 0, 0);
       const uint32_t b = r >= 0 ? __ldg(a.x_sf + r * tiles + col / 128) : 0u;

@@ -165,16 +165,26 @@ def test_moe_layout_all_padding_and_empty_source():
     assert not q.any() and not sf.any()
 
 
-def test_moe_layout_out_of_range_index_is_reported():
-    x = workloads.randn((200, 64), seed=4, dtype=torch.bfloat16)
+@pytest.mark.parametrize("src_kind", ["bf16", "fp8"])
+def test_moe_layout_out_of_range_index_is_reported(src_kind):
+    C = 64 if src_kind == "bf16" else 128          # stored E4M3 rows: whole 128-channel tiles
+    x = workloads.randn((200, C), seed=4, dtype=torch.bfloat16)
     src = np.arange(256, dtype=np.int32) % 200
     src[7] = 200                                   # one past the end
-    q, sf = _out(256, 64, 128, "token")
-    dg.dg_quant_moe_layout_fp8(x.cuda(), torch.from_numpy(src).cuda(), q, sf)
+    q, sf = _out(256, C, 128, "token")
+    if src_kind == "bf16":
+        dg.dg_quant_moe_layout_fp8(x.cuda(), torch.from_numpy(src).cuda(), q, sf)
+    else:
+        qs, ss = oracle.quant_rowtile(x.float().numpy())
+        dg.dg_quant_moe_layout_fp8(torch.from_numpy(qs).cuda(), torch.from_numpy(src).cuda(), q,
+                                   sf, torch.from_numpy(ss).cuda())
     with pytest.raises(dg.DGError, match="src_rows"):
         dg.dg_sync_check()
     src[7] = -1                                    # the row it wrote: zeros
-    want = oracle.moe_layout_cast(x.float().numpy(), src, 128)
+    if src_kind == "bf16":
+        want = oracle.moe_layout_cast(x.float().numpy(), src, 128)
+    else:
+        want = oracle.moe_layout_cast(qs, src, 128, sf_row=ss)
     _assert_same((q.cpu().numpy(), sf.cpu().numpy()), want)
     dg.dg_sync_check()                             # the status word was cleared
 
