@@ -126,19 +126,36 @@ __device__ __forceinline__ uint2 requant8(uint2 c, float p, const float *ma, con
   return make_uint2(out[0], out[1]);
 }
 
-// Source row of output row t (-1: not read).  Gather: src_rows[t]; an entry
-// outside [-1, T_src) is not read and is recorded in the status word.
+// Gather: the source rows of a tile's 128 output rows t0.., read once into
+// shared memory by the first 128 threads (past T: -1; an entry outside
+// [-1, T_src) is recorded in the status word and read as -1), so that every
+// thread's row loads can then be issued together.  Ends with a barrier.
 template <bool kGather>
-__device__ __forceinline__ int64_t source_row(const CastArgs &a, int64_t t, bool in, int lane) {
+__device__ __forceinline__ void stage_rows(const CastArgs &a, int64_t t0, int *rows_s) {
   if constexpr (kGather) {
-    const int s = in ? __ldg(a.src_rows + t) : -1;
-    if (s < -1 || s >= a.T_src) {
-      if (lane == 0) atomicCAS(&a.status->code, DEV_OK, DEV_BAD_ROW);
-      return -1;
+    if (threadIdx.x < kTileT) {
+      const int64_t t = t0 + threadIdx.x;
+      int s = t < a.T ? __ldg(a.src_rows + t) : -1;
+      if (s < -1 || s >= a.T_src) {
+        atomicCAS(&a.status->code, DEV_OK, DEV_BAD_ROW);
+        s = -1;
+      }
+      rows_s[threadIdx.x] = s;
     }
-    return s;
+    __syncthreads();
+  }
+}
+
+// Source row of the tile's row i (-1: not read): the staged entry, or t0 + i
+// itself without the gather.
+template <bool kGather>
+__device__ __forceinline__ int64_t tile_source_row(const CastArgs &a, const int *rows_s,
+                                                   int64_t t0, int i, bool col_ok) {
+  if constexpr (kGather) {
+    return col_ok ? rows_s[i] : -1;
   } else {
-    return in ? t : -1;
+    const int64_t t = t0 + i;
+    return (col_ok && t < a.T) ? t : -1;
   }
 }
 
@@ -159,6 +176,7 @@ template <int kGran, bool kChannel, bool kFp8Src, bool kGather>
 __global__ void __launch_bounds__(256, 2) cast_colblock_kernel(const CastArgs a) {
   __shared__ uint4 red[8][32][kFp8Src ? 2 : 1];
   __shared__ __align__(16) uint8_t tq[kChannel ? kTileC * kTileT : 16];
+  __shared__ int rows_s[kGather ? kTileT : 1];
   const int w = threadIdx.x >> 5;
   const int l = threadIdx.x & 31;
   const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kTileT;
@@ -166,6 +184,7 @@ __global__ void __launch_bounds__(256, 2) cast_colblock_kernel(const CastArgs a)
   const int c0 = blockIdx.y * kTileC;
   const int col = c0 + 8 * l;
   const bool col_ok = col < C;
+  stage_rows<kGather>(a, t0, rows_s);
 
   // ---- loads and column maxima
   uint4 v[kFp8Src ? 1 : 16];
@@ -177,8 +196,7 @@ __global__ void __launch_bounds__(256, 2) cast_colblock_kernel(const CastArgs a)
     const uint16_t *x = static_cast<const uint16_t *>(a.x);
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
-      const int64_t t = t0 + 16 * w + i;
-      const int64_t r = source_row<kGather>(a, t, col_ok && t < a.T, l);
+      const int64_t r = tile_source_row<kGather>(a, rows_s, t0, 16 * w + i, col_ok);
       v[i] = r >= 0 ? __ldcs(reinterpret_cast<const uint4 *>(x + r * C + col))
                     : make_uint4(0, 0, 0, 0);
     }
@@ -196,8 +214,7 @@ __global__ void __launch_bounds__(256, 2) cast_colblock_kernel(const CastArgs a)
     const int tiles = C / 128;
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
-      const int64_t t = t0 + 16 * w + i;
-      const int64_t r = source_row<kGather>(a, t, col_ok && t < a.T, l);
+      const int64_t r = tile_source_row<kGather>(a, rows_s, t0, 16 * w + i, col_ok);
       v8[i] = r >= 0 ? __ldcs(reinterpret_cast<const uint2 *>(x + r * C + col)) : make_uint2(0, 0);
       const uint32_t b = r >= 0 ? __ldg(a.x_sf + r * tiles + col / 128) : 0u;
       sbw[i >> 2] |= b << (8 * (i & 3));
@@ -383,21 +400,7 @@ __global__ void __launch_bounds__(256, 2) requant_tm_kernel(const CastArgs a) {
   const bool col_ok = col < C;
   const uint8_t *x = static_cast<const uint8_t *>(a.x);
   const int tiles = C / 128;
-  // Gather: the tile's 128 source rows, read and checked once (an entry
-  // outside [-1, T_src) is recorded and read as a row of zeros), so that
-  // every thread's code loads can be issued together.
-  if constexpr (kGather) {
-    if (threadIdx.x < kTileT) {
-      const int64_t t = t0 + threadIdx.x;
-      int s = t < a.T ? __ldg(a.src_rows + t) : -1;
-      if (s < -1 || s >= a.T_src) {
-        atomicCAS(&a.status->code, DEV_OK, DEV_BAD_ROW);
-        s = -1;
-      }
-      rows_s[threadIdx.x] = s;
-    }
-    __syncthreads();
-  }
+  stage_rows<kGather>(a, t0, rows_s);
 
   uint32_t sbw[4] = {0, 0, 0, 0};   // scale byte of row i in byte i % 4 of word i / 4
   float fm[16];
@@ -407,12 +410,7 @@ __global__ void __launch_bounds__(256, 2) requant_tm_kernel(const CastArgs a) {
     uint4 v[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
-      const int64_t t = t0 + 16 * w + i;
-      int64_t r;
-      if constexpr (kGather)
-        r = col_ok ? rows_s[16 * w + i] : -1;
-      else
-        r = (col_ok && t < a.T) ? t : -1;
+      const int64_t r = tile_source_row<kGather>(a, rows_s, t0, 16 * w + i, col_ok);
       v[i] = r >= 0 ? __ldcs(reinterpret_cast<const uint4 *>(x + r * C + col))
                     : make_uint4(0, 0, 0, 0);
       const uint32_t b = r >= 0 ? __ldg(a.x_sf + r * tiles + col / 128) : 0u;
