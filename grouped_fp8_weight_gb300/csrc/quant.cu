@@ -177,6 +177,8 @@ __global__ void __launch_bounds__(256, 2) cast_colblock_kernel(const CastArgs a)
   __shared__ uint4 red[8][32][kFp8Src ? 2 : 1];
   __shared__ __align__(16) uint8_t tq[kChannel ? kTileC * kTileT : 16];
   __shared__ int rows_s[kGather ? kTileT : 1];
+  __shared__ __align__(16) float fac_s[4 * kTileC];     // per (token block, column): factor
+  __shared__ __align__(8) uint8_t sb_s[4 * kTileC];     // and scale byte
   const int w = threadIdx.x >> 5;
   const int l = threadIdx.x & 31;
   const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kTileT;
@@ -236,60 +238,53 @@ __global__ void __launch_bounds__(256, 2) cast_colblock_kernel(const CastArgs a)
   }
   __syncthreads();
 
-  // ---- block maxima -> scale exponents and quantisation factors
-  // (non-negative float bit patterns order like the floats: integer maxima)
+  // ---- block maxima -> scale exponents and quantisation factors, one per
+  // (token block, column), computed once (red as [warp][column] maxima:
+  // BF16 bit patterns, or float bit patterns of non-negative values, both
+  // ordered like the values they encode)
   constexpr int kWarps = (kGran == 128) ? 8 : 2;
-  const int w0 = (kGran == 128) ? 0 : (w & ~1);
+  constexpr int kItems = (kTileT / kGran) * kTileC;
+#pragma unroll
+  for (int it = threadIdx.x; it < kItems; it += 256) {
+    const int bb = it / kTileC, c = it % kTileC;
+    uint32_t mx = 0;
+    int e;
+    if constexpr (!kFp8Src) {
+      const uint16_t *red16 = reinterpret_cast<const uint16_t *>(&red[0][0][0]);
+#pragma unroll
+      for (int ww = 0; ww < kWarps; ++ww)
+        mx = max(mx, static_cast<uint32_t>(red16[(bb * kWarps + ww) * kTileC + c]));
+      e = scale_exp_from_bf16(mx);
+      fac_s[it] = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+    } else {
+      const uint32_t *red32 = reinterpret_cast<const uint32_t *>(&red[0][0][0]);
+#pragma unroll
+      for (int ww = 0; ww < kWarps; ++ww) mx = max(mx, red32[(bb * kWarps + ww) * kTileC + c]);
+      e = scale_exp_from_f32_shifted(mx);
+      // y = (x * 2^-8) * 2^sh with sh = 8 - e in [-119, 135]: the first factor
+      // 2^min(sh, 127), the rest applied where a column needs it
+      fac_s[it] = __uint_as_float(static_cast<uint32_t>(min(8 - e, 127) + 127) << 23);
+    }
+    sb_s[it] = static_cast<uint8_t>(e + 127);
+  }
+  __syncthreads();
+  const int blk = (16 * w) / kGran;
   float mul[8], ma[8];
-  uint32_t sfw[2] = {0, 0};
-  bool big = false;   // E4M3 source: a column needs the second factor (sh > 127)
-  if constexpr (!kFp8Src) {
-    uint4 r = red[w0][l][0];
-#pragma unroll
-    for (int ww = 1; ww < kWarps; ++ww) {
-      const uint4 o = red[w0 + ww][l][0];
-      r.x = __vmaxu2(r.x, o.x);
-      r.y = __vmaxu2(r.y, o.y);
-      r.z = __vmaxu2(r.z, o.z);
-      r.w = __vmaxu2(r.w, o.w);
-    }
-    const uint32_t aw[4] = {r.x, r.y, r.z, r.w};
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int e = scale_exp_from_bf16((aw[k] >> (16 * h)) & 0xFFFFu);
-        mul[2 * k + h] = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
-        sfw[k >> 1] |= static_cast<uint32_t>(e + 127) << (8 * (2 * (k & 1) + h));
-      }
-    }
-  } else {
-    uint32_t ab[8];
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      uint4 r = red[w0][l][j];
-#pragma unroll
-      for (int ww = 1; ww < kWarps; ++ww) {
-        const uint4 o = red[w0 + ww][l][j];
-        r.x = max(r.x, o.x);
-        r.y = max(r.y, o.y);
-        r.z = max(r.z, o.z);
-        r.w = max(r.w, o.w);
-      }
-      ab[4 * j] = r.x;
-      ab[4 * j + 1] = r.y;
-      ab[4 * j + 2] = r.z;
-      ab[4 * j + 3] = r.w;
-    }
+  {
+    const float4 f0 = *reinterpret_cast<const float4 *>(fac_s + blk * kTileC + 8 * l);
+    const float4 f1 = *reinterpret_cast<const float4 *>(fac_s + blk * kTileC + 8 * l + 4);
+    const float f[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
-      const int e = scale_exp_from_f32_shifted(ab[k]);
-      const int sh = 8 - e;   // y = (x * 2^-8) * 2^sh, sh in [-119, 135]
-      ma[k] = __uint_as_float(static_cast<uint32_t>(min(sh, 127) + 127) << 23);
-      big |= sh > 127;
-      sfw[k >> 2] |= static_cast<uint32_t>(e + 127) << (8 * (k & 3));
+      mul[k] = f[k];
+      ma[k] = f[k];
     }
   }
+  const uint2 sb2 = *reinterpret_cast<const uint2 *>(sb_s + blk * kTileC + 8 * l);
+  const uint32_t sfw[2] = {sb2.x, sb2.y};
+  // E4M3 source: a column needs the second factor (sh > 127: scale byte below 8)
+  const bool big = kFp8Src && ((((sfw[0] - 0x08080808u) & ~sfw[0] & 0x80808080u) |
+                                ((sfw[1] - 0x08080808u) & ~sfw[1] & 0x80808080u)) != 0);
   if (col_ok) {
     if constexpr (kGran == 128) {
       if (w == 0)
